@@ -1,0 +1,193 @@
+"""CPU float64 oracle for the target-verify step (test infrastructure only).
+
+This package is TEST INFRASTRUCTURE.  Only ``tests/``, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import it.
+The product library (``speculative_decoding_target_gb300``) never imports,
+links or calls anything here, and this package imports nothing from it: the
+two share no code.  Inputs reach both sides from the seeded generators in
+``speculative_decoding_target_gb300.workloads``, which hold none of the
+method's arithmetic.
+
+The arithmetic lives in ``spec_oracle.c`` (plain C, float64, OpenMP over
+output rows only); this module compiles it with gcc and wraps it with
+ctypes.  Every function cites the passage it follows in the C file.
+
+Pins (see ``tests/test_oracle.py``): torch float64 scaled-dot-product
+attention on gathered dense K/V, torch's float8_e4m3fn and numpy's float16
+decoders on every bit pattern, closed forms (identical keys, dominant key,
+two-key sigmoid), the invariants the pages fix (q_len=1 equals decode, row i
+equals a q_len=1 call over prefix + drafts 1..i, merge of split partials
+equals the unsplit result, permuted pages and poisoned slots change nothing),
+numpy argmax on exhaustive tiny tie patterns, the pages' worked accept
+examples, and a serial-greedy simulation of the commit stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libspec_oracle.so")
+_lib = None
+
+ORACLE_OK = 0
+ORACLE_ERR_ARG = -1
+ORACLE_ERR_PAGE = -2
+ORACLE_ERR_NOMEM = -3
+
+
+def build(force: bool = False) -> str:
+    """Compile spec_oracle.c into a shared library with gcc (portable flags)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    P = ctypes.c_void_p
+    i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    lib.oracle_verify_attention.argtypes = [
+        i32, i32, i32, i32, i32, i32, i32, i32, i32,
+        P, P, P, P, P, P, P, f64, P, i64, i64, i64, P, P, i32]
+    lib.oracle_verify_attention.restype = ctypes.c_int
+    lib.oracle_lse_merge.argtypes = [i32, i32, P, P, P, P]
+    lib.oracle_lse_merge.restype = None
+    lib.oracle_greedy_accept.argtypes = [P, P, i32, i32, i64, P, P, P, P, i32]
+    lib.oracle_greedy_accept.restype = ctypes.c_int
+    for name in ("oracle_decode_bf16", "oracle_decode_fp16"):
+        getattr(lib, name).argtypes = [P, i64, P]
+        getattr(lib, name).restype = None
+    lib.oracle_decode_e4m3.argtypes = [P, i64, P]
+    lib.oracle_decode_e4m3.restype = None
+    _lib = lib
+    return lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def decode_bf16(bits) -> np.ndarray:
+    x = _c(bits, np.uint16).ravel()
+    out = np.empty(x.size, np.float64)
+    _load().oracle_decode_bf16(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def decode_fp16(bits) -> np.ndarray:
+    x = _c(bits, np.uint16).ravel()
+    out = np.empty(x.size, np.float64)
+    _load().oracle_decode_fp16(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def decode_e4m3(bytes_) -> np.ndarray:
+    x = _c(bytes_, np.uint8).ravel()
+    out = np.empty(x.size, np.float64)
+    _load().oracle_decode_e4m3(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def verify_attention(q_bits, k_pages, v_pages, page_table, seq_lens, *,
+                     num_kv_heads: int, scale: float, k_scales=None,
+                     v_scales=None, rows=None, key_begin: int = 0,
+                     key_end: int = -1, threads: int = 0,
+                     return_lse: bool = False):
+    """Verify attention in float64.
+
+    q_bits:   uint16 bf16 bits [B, q_len, Hq, D]
+    k_pages, v_pages: uint16 bf16 bits, or uint8 E4M3 bytes when scales are
+              given, [num_pages, Hkv, page_size, D]
+    k_scales, v_scales: uint16 fp16 bits [num_pages, Hkv, page_size, D/64]
+    page_table: int32 [B, max_pages];  seq_lens: int32 [B] (block included)
+    rows:     optional flat row ids (b*q_len + i)*Hq + h; default every row.
+    Returns out float64 [n_rows, D] (and lse [n_rows] if requested).
+    """
+    q = _c(q_bits, np.uint16)
+    B, q_len, hq, d = q.shape
+    fp8 = k_scales is not None
+    kv_dtype = np.uint8 if fp8 else np.uint16
+    kp = _c(k_pages, kv_dtype)
+    vp = _c(v_pages, kv_dtype)
+    num_pages, hkv, page_size, d2 = kp.shape
+    assert d2 == d and hkv == num_kv_heads and vp.shape == kp.shape
+    ks = _c(k_scales, np.uint16) if fp8 else None
+    vs = _c(v_scales, np.uint16) if fp8 else None
+    pt = _c(page_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    assert pt.ndim == 2 and pt.shape[0] == B and sl.shape == (B,)
+    r = None if rows is None else _c(rows, np.int64).ravel()
+    n = B * q_len * hq if r is None else r.size
+    out = np.zeros((n, d), np.float64)
+    lse = np.zeros(n, np.float64)
+    rc = _load().oracle_verify_attention(
+        B, q_len, hq, hkv, d, page_size, num_pages, pt.shape[1], int(fp8),
+        _ptr(q), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(pt), _ptr(sl),
+        float(scale), _ptr(r), n, int(key_begin), int(key_end), _ptr(out),
+        _ptr(lse), int(threads or default_threads()))
+    if rc != ORACLE_OK:
+        raise ValueError(f"oracle_verify_attention failed with code {rc}")
+    return (out, lse) if return_lse else out
+
+
+def lse_merge(lse_parts, o_parts):
+    """Merge split partials: lse [S], o [S, D] -> (out [D], lse)."""
+    lse = _c(lse_parts, np.float64).ravel()
+    o = _c(o_parts, np.float64)
+    S, d = o.shape
+    assert lse.size == S
+    out = np.zeros(d, np.float64)
+    lse_out = np.zeros(1, np.float64)
+    _load().oracle_lse_merge(S, d, _ptr(lse), _ptr(o), _ptr(out), _ptr(lse_out))
+    return out, float(lse_out[0])
+
+
+def greedy_accept(logits, draft_ids, *, threads: int = 0):
+    """Greedy acceptance.  logits fp32 [B*q_len, V]; draft_ids int32 [B, q_len].
+
+    Returns dict with accept_len [B], next_token [B], out_tokens [B, q_len],
+    argmax [B*q_len].
+    """
+    lg = _c(logits, np.float32)
+    dr = _c(draft_ids, np.int32)
+    B, q_len = dr.shape
+    assert lg.ndim == 2 and lg.shape[0] == B * q_len
+    vocab = lg.shape[1]
+    acc = np.zeros(B, np.int32)
+    nxt = np.zeros(B, np.int32)
+    toks = np.zeros((B, q_len), np.int32)
+    am = np.zeros(B * q_len, np.int32)
+    rc = _load().oracle_greedy_accept(
+        _ptr(lg), _ptr(dr), B, q_len, vocab, _ptr(acc), _ptr(nxt), _ptr(toks),
+        _ptr(am), int(threads or default_threads()))
+    if rc != ORACLE_OK:
+        raise ValueError(f"oracle_greedy_accept failed with code {rc}")
+    return {"accept_len": acc, "next_token": nxt, "out_tokens": toks,
+            "argmax": am}

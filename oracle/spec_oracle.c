@@ -1,0 +1,366 @@
+/*
+ * spec_oracle.c -- CPU float64 oracle for the target-verify step of
+ * speculative decoding.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: it exists so that tests, the smoke check and the CPU
+ * baseline of the benchmark can compare the CUDA kernels against a plain,
+ * slow, obviously correct definition.  It shares no code, header, table or
+ * helper with the CUDA library.
+ *
+ * What it computes (the pages' definitions, written out):
+ *
+ *  1. Verify attention.  A request's verify block holds q_len known tokens
+ *     [boundary, d1 .. dk] whose K/V already sit at the end of the request's
+ *     paged KV cache.  Block row i attends causally to every cached key up to
+ *     and including its own position, i.e. to the first
+ *         L_i = seq_len - q_len + i + 1
+ *     keys ("MTP and DFlash2 at long context on XPU", Part II "Why the target
+ *     output stayed the same" and Part III "Reducing an eight-query verify
+ *     with a severe shape cliff": each position gets its own cache length;
+ *     "DFlash to dLLM self-spec, part 1", section 1.1, table of known inputs
+ *     per verify row).  Query head h reads KV head h / (Hq/Hkv) (contiguous
+ *     GQA groups).  Scores s_t = scale * <q, k_t>, softmax over t < L_i, and
+ *     out = sum_t softmax_t * v_t.  The oracle uses the two-pass form:
+ *     m = max_t s_t, w_t = exp(s_t - m), out = sum w_t v_t / sum w_t.
+ *     No online softmax, no splits, no blocking.
+ *
+ *  2. Split merge ("Qwen3.8-27B-FP8" page, "Implemented execution path":
+ *     split-context decode keeps compact online-softmax partials that a
+ *     merge step combines).  A part s carries (o_s, lse_s) with
+ *     lse_s = ln sum_{t in part} e^{s_t} and o_s the part's normalised
+ *     output; the merge is lse = ln sum_s e^{lse_s},
+ *     out = sum_s e^{lse_s - lse} o_s.
+ *
+ *  3. FP8 KV ("Qwen3.8-27B-FP8" page, "Implemented execution path": FP8 E4M3
+ *     cache with per-token / per-KV-head FP16 scales over 64-channel
+ *     blocks): element c of a cached K or V row is
+ *         e4m3(byte_c) * fp16(scale[c / 64]).
+ *     E4M3 is decoded from the OCP 8-bit floating point definition (bias 7,
+ *     subnormals m * 2^-9, S.1111.111 is NaN, no infinities); FP16 and BF16
+ *     from the IEEE binary16 / upper-half-of-binary32 definitions.
+ *
+ *  4. Greedy acceptance ("MTP and DFlash2 at long context on XPU", Part II:
+ *     the runtime commits the accepted drafts and the target's token at the
+ *     first disagreement; "DFlash to dLLM self-spec, part 1", section 1.1
+ *     table and glossary "bonus token", section 1.6.1 commit_lens =
+ *     accept_len + 1).  t_r = argmax over the fp32 logits of row r, lowest
+ *     index on ties, NaN greater than every number (first NaN wins), -0 ==
+ *     +0.  accept a = number of leading j = 1..k with draft[j] == t[j-1];
+ *     next = t[a].
+ *
+ * Parity of this oracle against any engine on the pages is unpinned: the
+ * pages print no output for a concrete input tensor.  It is pinned instead
+ * by tests against library routines (torch scaled-dot-product attention in
+ * float64, torch's float8_e4m3fn and numpy's float16 decoders, numpy
+ * argmax), closed forms, invariants and the pages' worked accept examples.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG (-1)
+#define ORACLE_ERR_PAGE (-2)
+#define ORACLE_ERR_NOMEM (-3)
+
+/* ---- exact decoders, written from the format definitions ---------------- */
+
+double oracle_bf16_to_double(uint16_t h) {
+  /* bfloat16 is the upper half of an IEEE binary32 */
+  uint32_t bits = ((uint32_t)h) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+double oracle_fp16_to_double(uint16_t h) {
+  int s = (h >> 15) & 1, e = (h >> 10) & 0x1F, m = h & 0x3FF;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)m, -24); /* subnormal: m * 2^-14 * 2^-10 */
+  } else if (e == 31) {
+    v = m ? NAN : INFINITY;
+  } else {
+    v = ldexp(1.0 + (double)m / 1024.0, e - 15);
+  }
+  return s ? -v : v;
+}
+
+double oracle_e4m3_to_double(uint8_t b) {
+  int s = (b >> 7) & 1, e = (b >> 3) & 0xF, m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN; /* S.1111.111: the only NaN, no inf */
+  if (e == 0) {
+    v = ldexp((double)m, -9); /* subnormal: m/8 * 2^(1-7) */
+  } else {
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  }
+  return s ? -v : v;
+}
+
+void oracle_decode_bf16(const uint16_t* x, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_double(x[i]);
+}
+void oracle_decode_fp16(const uint16_t* x, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_fp16_to_double(x[i]);
+}
+void oracle_decode_e4m3(const uint8_t* x, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_to_double(x[i]);
+}
+
+/* ---- verify attention ------------------------------------------------------ */
+
+typedef struct {
+  int32_t batch, q_len, hq, hkv, d, page_size, num_pages, max_pages, kv_fp8;
+  const uint16_t* q;       /* bf16 bits [batch, q_len, hq, d] */
+  const void* k_pages;     /* bf16 bits or e4m3 bytes [num_pages, hkv, page_size, d] */
+  const void* v_pages;
+  const uint16_t* k_scales; /* fp16 bits [num_pages, hkv, page_size, d/64] (fp8 only) */
+  const uint16_t* v_scales;
+  const int32_t* page_table; /* [batch, max_pages] */
+  const int32_t* seq_lens;   /* [batch], block included */
+} oracle_attn_problem;
+
+/* Element c of the cached K (or V) row of token t of request b, KV head g.
+ * Returns 0 and writes the row, or ORACLE_ERR_PAGE for a page id outside the
+ * pool. */
+static int load_kv_row(const oracle_attn_problem* p, int is_v, int b, int g,
+                       int64_t t, double* row) {
+  const int ps = p->page_size, d = p->d;
+  int64_t page_slot = t / ps;
+  if (page_slot >= p->max_pages) return ORACLE_ERR_PAGE;
+  int32_t page = p->page_table[(int64_t)b * p->max_pages + page_slot];
+  if (page < 0 || page >= p->num_pages) return ORACLE_ERR_PAGE;
+  int64_t slot = t % ps;
+  int64_t base = (((int64_t)page * p->hkv + g) * ps + slot) * d;
+  if (!p->kv_fp8) {
+    const uint16_t* src = (const uint16_t*)(is_v ? p->v_pages : p->k_pages);
+    for (int c = 0; c < d; ++c) row[c] = oracle_bf16_to_double(src[base + c]);
+  } else {
+    const uint8_t* src = (const uint8_t*)(is_v ? p->v_pages : p->k_pages);
+    const uint16_t* sc = is_v ? p->v_scales : p->k_scales;
+    int64_t sbase = (((int64_t)page * p->hkv + g) * ps + slot) * (d / 64);
+    for (int c = 0; c < d; ++c)
+      row[c] = oracle_e4m3_to_double(src[base + c]) *
+               oracle_fp16_to_double(sc[sbase + c / 64]);
+  }
+  return ORACLE_OK;
+}
+
+/* One output row: request b, block row i, query head h, keys restricted to
+ * [key_begin, key_end) intersected with the causal window [0, L_i). */
+static int attention_row(const oracle_attn_problem* p, int b, int i, int h,
+                         int64_t key_begin, int64_t key_end, double scale,
+                         double* s_buf, double* krow, double* out, double* lse) {
+  const int d = p->d;
+  const int group = p->hq / p->hkv;
+  const int g = h / group;
+  const int64_t causal = (int64_t)p->seq_lens[b] - p->q_len + i + 1;
+  int64_t lo = key_begin > 0 ? key_begin : 0;
+  int64_t hi = causal;
+  if (key_end >= 0 && key_end < hi) hi = key_end;
+  for (int c = 0; c < d; ++c) out[c] = 0.0;
+  if (hi <= lo) {
+    *lse = -INFINITY;
+    return ORACLE_OK;
+  }
+  double qrow[1024];
+  const uint16_t* qsrc = p->q + (((int64_t)b * p->q_len + i) * p->hq + h) * d;
+  for (int c = 0; c < d; ++c) qrow[c] = oracle_bf16_to_double(qsrc[c]);
+
+  /* pass 1: all scores and their maximum */
+  double m = -INFINITY;
+  for (int64_t t = lo; t < hi; ++t) {
+    int rc = load_kv_row(p, 0, b, g, t, krow);
+    if (rc) return rc;
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += qrow[c] * krow[c];
+    double s = scale * acc;
+    s_buf[t - lo] = s;
+    if (s > m) m = s;
+  }
+  /* pass 2: weights and the weighted sum of V rows */
+  double den = 0.0;
+  for (int64_t t = lo; t < hi; ++t) {
+    double w = exp(s_buf[t - lo] - m);
+    den += w;
+    int rc = load_kv_row(p, 1, b, g, t, krow);
+    if (rc) return rc;
+    for (int c = 0; c < d; ++c) out[c] += w * krow[c];
+  }
+  for (int c = 0; c < d; ++c) out[c] /= den;
+  *lse = m + log(den);
+  return ORACLE_OK;
+}
+
+/*
+ * Verify attention for a list of rows.
+ *   rows:  flat row ids r = (b * q_len + i) * hq + h, or NULL for all
+ *          batch * q_len * hq rows in that order.
+ *   key_begin/key_end: restrict the keys to [key_begin, key_end) (key_end < 0
+ *          means no upper limit) on top of the causal window; used to form
+ *          split partials.
+ *   out:   [n_rows, d] float64;  lse: [n_rows] (natural log) or NULL.
+ * Returns 0, ORACLE_ERR_ARG for bad shapes, ORACLE_ERR_PAGE for a page id
+ * outside the pool, ORACLE_ERR_NOMEM.
+ */
+int oracle_verify_attention(int32_t batch, int32_t q_len, int32_t hq,
+                            int32_t hkv, int32_t d, int32_t page_size,
+                            int32_t num_pages, int32_t max_pages,
+                            int32_t kv_fp8, const uint16_t* q,
+                            const void* k_pages, const void* v_pages,
+                            const uint16_t* k_scales, const uint16_t* v_scales,
+                            const int32_t* page_table, const int32_t* seq_lens,
+                            double scale, const int64_t* rows, int64_t n_rows,
+                            int64_t key_begin, int64_t key_end, double* out,
+                            double* lse, int32_t nthreads) {
+  if (batch < 0 || q_len < 1 || hq < 1 || hkv < 1 || hq % hkv || d < 1 ||
+      d > 1024 || page_size < 1 || num_pages < 0 || max_pages < 0)
+    return ORACLE_ERR_ARG;
+  if (kv_fp8 && (d % 64 || !k_scales || !v_scales)) return ORACLE_ERR_ARG;
+  oracle_attn_problem p = {batch,   q_len,     hq,       hkv,      d,
+                           page_size, num_pages, max_pages, kv_fp8, q,
+                           k_pages, v_pages,   k_scales, v_scales, page_table,
+                           seq_lens};
+  const int64_t total = (int64_t)batch * q_len * hq;
+  if (!rows) n_rows = total;
+  int64_t max_len = 0;
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] > max_len) max_len = seq_lens[b];
+  int err = ORACLE_OK;
+#ifdef _OPENMP
+  if (nthreads < 1) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+  {
+    double* s_buf = (double*)malloc(sizeof(double) * (size_t)(max_len + 1));
+    double* krow = (double*)malloc(sizeof(double) * (size_t)d);
+    double dummy;
+    if (!s_buf || !krow) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+      err = ORACLE_ERR_NOMEM;
+    } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+      for (int64_t n = 0; n < n_rows; ++n) {
+        int64_t r = rows ? rows[n] : n;
+        if (r < 0 || r >= total) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+          err = ORACLE_ERR_ARG;
+          continue;
+        }
+        int h = (int)(r % hq);
+        int i = (int)((r / hq) % q_len);
+        int b = (int)(r / ((int64_t)hq * q_len));
+        int rc = attention_row(&p, b, i, h, key_begin, key_end, scale, s_buf,
+                               krow, out + n * d, lse ? lse + n : &dummy);
+        if (rc) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+          err = rc;
+        }
+      }
+    }
+    free(s_buf);
+    free(krow);
+  }
+  return err;
+}
+
+/*
+ * Merge of split partials: lse = ln sum_s e^{lse_s},
+ * out = sum_s e^{lse_s - lse} o_s.  o: [n_parts, d]; parts with
+ * lse_s = -inf carry no weight; all parts empty gives out = 0, lse = -inf.
+ */
+void oracle_lse_merge(int32_t n_parts, int32_t d, const double* lse,
+                      const double* o, double* out, double* lse_out) {
+  double m = -INFINITY;
+  for (int s = 0; s < n_parts; ++s)
+    if (lse[s] > m) m = lse[s];
+  for (int c = 0; c < d; ++c) out[c] = 0.0;
+  if (m == -INFINITY) {
+    *lse_out = -INFINITY;
+    return;
+  }
+  double den = 0.0;
+  for (int s = 0; s < n_parts; ++s) den += exp(lse[s] - m);
+  double total = m + log(den);
+  for (int s = 0; s < n_parts; ++s) {
+    if (lse[s] == -INFINITY) continue;
+    double w = exp(lse[s] - total);
+    for (int c = 0; c < d; ++c) out[c] += w * o[(int64_t)s * d + c];
+  }
+  *lse_out = total;
+}
+
+/* ---- greedy acceptance ------------------------------------------------------ */
+
+/* argmax with the lowest index on ties; NaN ranks above every number and
+ * the first NaN wins; -0 and +0 compare equal. */
+static int64_t row_argmax(const float* x, int64_t n) {
+  int64_t best = 0;
+  float bv = x[0];
+  if (isnan(bv)) return 0;
+  for (int64_t v = 1; v < n; ++v) {
+    float xv = x[v];
+    if (isnan(xv)) return v;
+    if (xv > bv) {
+      bv = xv;
+      best = v;
+    }
+  }
+  return best;
+}
+
+/*
+ * logits: [batch * q_len, vocab] fp32, row (b, j) scores the token after
+ *         block position j.
+ * draft_ids: [batch, q_len]; column 0 is the boundary token (not compared),
+ *         columns 1..q_len-1 are the drafts d1..dk.
+ * accept_len/next_token: [batch].  out_tokens [batch, q_len] (optional):
+ *         d1..da, then next, then -1.  argmax_rows [batch * q_len] (optional).
+ */
+int oracle_greedy_accept(const float* logits, const int32_t* draft_ids,
+                         int32_t batch, int32_t q_len, int64_t vocab,
+                         int32_t* accept_len, int32_t* next_token,
+                         int32_t* out_tokens, int32_t* argmax_rows,
+                         int32_t nthreads) {
+  if (batch < 0 || q_len < 1 || vocab < 1) return ORACLE_ERR_ARG;
+  const int64_t rows = (int64_t)batch * q_len;
+  int32_t* t = (int32_t*)malloc(sizeof(int32_t) * (size_t)(rows ? rows : 1));
+  if (!t) return ORACLE_ERR_NOMEM;
+#ifdef _OPENMP
+  if (nthreads < 1) nthreads = omp_get_max_threads();
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1)
+#endif
+  for (int64_t r = 0; r < rows; ++r)
+    t[r] = (int32_t)row_argmax(logits + r * vocab, vocab);
+  for (int b = 0; b < batch; ++b) {
+    const int32_t* dr = draft_ids + (int64_t)b * q_len;
+    const int32_t* tb = t + (int64_t)b * q_len;
+    int a = 0;
+    while (a + 1 < q_len && dr[a + 1] == tb[a]) ++a;
+    accept_len[b] = a;
+    next_token[b] = tb[a];
+    if (out_tokens) {
+      int32_t* ot = out_tokens + (int64_t)b * q_len;
+      for (int j = 0; j < q_len; ++j) ot[j] = -1;
+      for (int j = 0; j < a; ++j) ot[j] = dr[j + 1];
+      ot[a] = tb[a];
+    }
+  }
+  if (argmax_rows) memcpy(argmax_rows, t, sizeof(int32_t) * (size_t)rows);
+  free(t);
+  return ORACLE_OK;
+}
