@@ -1,0 +1,442 @@
+#!/usr/bin/env python3
+"""Benchmark of the target-verify step: paged GQA verify attention followed
+by greedy acceptance, on seeded synthetic inputs, through the C ABI.
+
+One step = spec_verify_attention (split-KV kernel + LSE merge) over every
+request's verify block, then spec_greedy_accept over the block's logits.
+Default workload: batch 8, q_len 8, 24/4 heads, head_dim 256, 32,768-token
+prefixes in 64-token pages of a permuted pool, bf16 KV; logits
+[64 x 248,320] fp32 with drafts planted at p = 0.6.
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+replica of the workload on its own GPU (the step has no cross-GPU exchange),
+timing is the max over ranks, and value counts the steps of all ranks.
+
+--impl reference times the CPU float64 oracle on the host cores instead
+(rank 0 only), on a bounded sample of rows per step, extrapolated to the
+whole workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_target_gb300 import workloads as wl  # noqa: E402
+
+METRIC = ("verify steps/s and KV-read GB/s (fraction of GB300 HBM peak) at "
+          "1 GPU")
+UNIT = "steps/s"
+DEFAULT_WORKLOAD = "b8_q8_p32k"
+KERNEL_LAUNCHES_PER_STEP = 4   # split, merge, argmax partial, accept finalize
+
+# DRAM traffic per attention call measured by ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum of the split and merge kernels), keyed by workload,
+# valid only for the kernel sources whose hash is recorded with it.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_target_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            ident = str(device_index)
+        self.ident = ident
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.ident,
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def algorithmic_bytes(w: wl.VerifyWorkload, seq_lens):
+    kv = wl.kv_bytes(seq_lens, w.num_kv_heads, w.head_dim, w.kv_dtype)
+    logits = w.batch * w.q_len * w.vocab * 4
+    return kv, logits
+
+
+# ----------------------------------------------------------------- GPU arm --
+
+def run_gpu(args, w: wl.VerifyWorkload):
+    import speculative_decoding_target_gb300 as sv
+    from speculative_decoding_target_gb300 import _native
+
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sv.load()
+
+    inp = wl.workload_inputs(w, device=dev)
+    seq_lens = inp["seq_lens"].tolist()
+    desc = sv.desc_for(inp["q"], inp["k_pages"], inp["page_table"])
+    attn_ws = sv.alloc_workspace(sv.verify_workspace_size(desc), dev)
+    rows = w.batch * w.q_len
+    acc_ws = sv.alloc_workspace(sv.accept_workspace_size(rows, w.vocab), dev)
+    out = torch.empty_like(inp["q"])
+    acc = torch.empty(w.batch, dtype=torch.int32, device=dev)
+    nxt = torch.empty(w.batch, dtype=torch.int32, device=dev)
+    toks = torch.empty((w.batch, w.q_len), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev_a=None, ev_b=None):
+        if ev_a is not None:
+            ev_a.record(stream)
+        _native.verify_attention_into(
+            desc, inp["q"], inp["k_pages"], inp["v_pages"], inp["k_scales"],
+            inp["v_scales"], inp["page_table"], inp["seq_lens"], inp["scale"],
+            out, attn_ws, stream)
+        if ev_b is not None:
+            ev_b.record(stream)
+        _native.greedy_accept_into(inp["logits"], inp["draft_ids"], acc, nxt,
+                                   toks, acc_ws, stream)
+
+    def barrier():
+        if ws_n > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    evs = [(torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(*evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    if ws_n > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # end to end through the public API with host buffers: every step copies
+    # its inputs from pinned host memory and reads its results back
+    e2e = None
+    if not args.no_e2e:
+        host = {k: inp[k].cpu().pin_memory()
+                for k in ("q", "page_table", "seq_lens", "logits",
+                          "draft_ids")}
+        dev_in = {k: torch.empty_like(inp[k]) for k in host}
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_acc = torch.empty(w.batch, dtype=torch.int32).pin_memory()
+        h_nxt = torch.empty(w.batch, dtype=torch.int32).pin_memory()
+        h_tok = torch.empty((w.batch, w.q_len), dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size()
+                  for t in (h_out, h_acc, h_nxt, h_tok))
+
+        def e2e_step():
+            for k, t in host.items():
+                dev_in[k].copy_(t, non_blocking=True)
+            _native.verify_attention_into(
+                desc, dev_in["q"], inp["k_pages"], inp["v_pages"],
+                inp["k_scales"], inp["v_scales"], dev_in["page_table"],
+                dev_in["seq_lens"], inp["scale"], out, attn_ws, stream)
+            _native.greedy_accept_into(dev_in["logits"], dev_in["draft_ids"],
+                                       acc, nxt, toks, acc_ws, stream)
+            h_out.copy_(out, non_blocking=True)
+            h_acc.copy_(acc, non_blocking=True)
+            h_nxt.copy_(nxt, non_blocking=True)
+            h_tok.copy_(toks, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        if ws_n > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(ws_n * args.steps / (e_ms / 1e3), 3),
+               "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h),
+               "note": "KV pool resident in HBM (it is the cache state); "
+                       "per-step q, page table, seq_lens, logits and drafts "
+                       "copied in, out/accept/next/tokens copied back"}
+
+    kv_b, logit_b = algorithmic_bytes(w, seq_lens)
+    attn_avg_s = statistics.mean(attn_ms) / 1e3
+    peak, peak_kind = measured_peaks()
+    achieved = kv_b / attn_avg_s / 1e9
+    src_hash = kernel_source_hash()
+    traffic = None
+    rec = NCU_TRAFFIC.get(w.name)
+    if rec and rec.get("source_hash") == src_hash:
+        traffic = rec["bytes_per_launch"]
+    result = {
+        "metric": METRIC,
+        "value": round(ws_n * args.steps / (elapsed_ms / 1e3), 3),
+        "unit": UNIT,
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3",
+        "data": "synthetic (seeded; random bf16 Q/K/V ~N(0,1), fp32 logits "
+                "~N(0,4), planted drafts)",
+        "config": {
+            "workload": w.name, "batch": w.batch, "q_len": w.q_len,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "prefix": w.prefix or "U[1024,131072]",
+            "page_size": w.page_size, "kv_dtype": w.kv_dtype,
+            "vocab": w.vocab, "accept_p": w.accept_p,
+            "kv_bytes_per_step": kv_b, "logits_bytes_per_step": logit_b,
+            "l2": f"inputs larger than L2 ({(kv_b + logit_b) / 1e9:.3f} GB "
+                  "read per step), no flush",
+            "parallelism": f"replicas x{ws_n}",
+        },
+        "kv_read_gbs": round(achieved, 1),
+        "roofline": {
+            "kernel": "verify attention (split-KV kernel + LSE merge, one "
+                      "C-ABI call)",
+            "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "algorithmic_bytes_per_launch": kv_b,
+            "avg_launch_ms": round(attn_avg_s * 1e3, 5),
+        },
+        "gpu_launches": KERNEL_LAUNCHES_PER_STEP * args.steps,
+        "kernel_source_hash": src_hash,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        result["e2e"] = e2e
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        host_inp = {k: (v.cpu() if torch.is_tensor(v) else v)
+                    for k, v in inp.items()}
+        result["cpu_baseline"] = cpu_baseline(w, host_inp, args.cpu_seconds)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result, rank
+
+
+# ----------------------------------------------------------- CPU baseline --
+
+def _oracle_step_estimate(w, host_inp, n_rows: int, n_acc_rows: int, rng):
+    """Time the oracle on n_rows attention rows and n_acc_rows accept rows;
+    return the extrapolated seconds of one full step."""
+    import oracle
+    bits = wl.to_numpy_bits
+    total_rows = w.batch * w.q_len * w.num_q_heads
+    rows = np.sort(rng.choice(total_rows, size=min(n_rows, total_rows),
+                              replace=False)).astype(np.int64)
+    fp8 = host_inp["k_scales"] is not None
+    args = (bits(host_inp["q"]), bits(host_inp["k_pages"]),
+            bits(host_inp["v_pages"]), host_inp["page_table"].numpy(),
+            host_inp["seq_lens"].numpy())
+    t = time.perf_counter()
+    oracle.verify_attention(
+        *args, num_kv_heads=w.num_kv_heads, scale=host_inp["scale"],
+        k_scales=bits(host_inp["k_scales"]) if fp8 else None,
+        v_scales=bits(host_inp["v_scales"]) if fp8 else None, rows=rows)
+    t_attn = time.perf_counter() - t
+    acc_total = w.batch * w.q_len
+    nb = max(1, min(w.batch, n_acc_rows // w.q_len))
+    lg = host_inp["logits"].numpy()[:nb * w.q_len]
+    dr = host_inp["draft_ids"].numpy()[:nb]
+    t = time.perf_counter()
+    oracle.greedy_accept(lg, dr)
+    t_acc = time.perf_counter() - t
+    return (t_attn * total_rows / rows.size
+            + t_acc * acc_total / (nb * w.q_len)), rows.size, nb * w.q_len
+
+
+def cpu_baseline(w, host_inp, budget_s: float):
+    import oracle
+    rng = np.random.default_rng(w.seed)
+    n = 8
+    t0 = time.perf_counter()
+    while True:
+        est, nr, na = _oracle_step_estimate(w, host_inp, n, 2 * w.q_len, rng)
+        spent = time.perf_counter() - t0
+        total = w.batch * w.q_len * w.num_q_heads
+        if spent > budget_s / 3 or nr >= total:
+            break
+        n = min(total, n * 4)
+    return {"value": round(1.0 / est, 6), "unit": UNIT,
+            "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": f"{nr} of {w.batch * w.q_len * w.num_q_heads} attention "
+                      f"rows and {na} of {w.batch * w.q_len} logits rows of "
+                      f"one step, extrapolated by row count "
+                      f"({spent:.1f} s of CPU time)"}
+
+
+# ------------------------------------------------------- reference arm --
+
+def run_reference(args, w):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return None, rank
+    import oracle
+    host_inp = wl.workload_inputs(w, device="cpu")
+    rng = np.random.default_rng(w.seed + 1)
+    n_rows = max(1, args.ref_rows)
+    for _ in range(args.warmup):
+        _oracle_step_estimate(w, host_inp, n_rows, w.q_len, rng)
+    ests = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        est, nr, na = _oracle_step_estimate(w, host_inp, n_rows, w.q_len, rng)
+        ests.append(est)
+    spent = time.perf_counter() - t0
+    value = 1.0 / statistics.mean(ests)
+    sample = (f"{nr} of {w.batch * w.q_len * w.num_q_heads} attention rows "
+              f"and {na} logits rows per step, extrapolated by row count")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 / value, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded, generated on the host)",
+        "config": {"workload": w.name, "batch": w.batch, "q_len": w.q_len,
+                   "prefix": w.prefix or "U[1024,131072]",
+                   "page_size": w.page_size, "kv_dtype": w.kv_dtype},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT,
+                         "cores": oracle.default_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT,
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(spent, 2),
+    }, rank
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=wl.WORKLOAD_ORDER)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--ref-rows", type=int, default=48)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        res, rank = run_reference(args, w)
+    else:
+        res, rank = run_gpu(args, w)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+"""ctypes binding of libspecverify.so (argument marshalling only).
+
+Every step of the verify path runs in the library's CUDA kernels; this module
+only turns torch tensors into device pointers and sizes, and the current torch
+stream into a cudaStream_t.  There is no fallback: if the library is missing
+or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libspecverify.so")
+
+SPEC_OK = 0
+SPEC_ERR_ARG = -1
+SPEC_ERR_ALIGN = -2
+SPEC_ERR_WORKSPACE = -3
+SPEC_ERR_UNSUPPORTED = -4
+SPEC_ERR_CUDA = -5
+SPEC_KV_BF16 = 0
+SPEC_KV_FP8_E4M3 = 1
+SPEC_FLAG_CHECKED = 1
+SPEC_STATUS_BAD_PAGE = 1
+
+EXPORTED = (
+    "spec_verify_workspace_size", "spec_verify_attention",
+    "spec_verify_status", "spec_accept_workspace_size", "spec_greedy_accept",
+    "spec_last_error", "spec_version",
+)
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"spec_verify error {code}: {msg}")
+        self.code = code
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("max_pages_per_seq", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} not found: build it with "
+            "`python -m speculative_decoding_target_gb300.build`")
+    lib = ctypes.CDLL(path)
+    P, i32, u32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32
+    sz = ctypes.c_size_t
+    lib.spec_verify_workspace_size.argtypes = [ctypes.POINTER(AttnDesc)]
+    lib.spec_verify_workspace_size.restype = sz
+    lib.spec_verify_attention.argtypes = [
+        ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P, ctypes.c_float, P, P,
+        sz, P]
+    lib.spec_verify_attention.restype = ctypes.c_int
+    lib.spec_verify_status.argtypes = [P, ctypes.POINTER(u32), i32, P]
+    lib.spec_verify_status.restype = ctypes.c_int
+    lib.spec_accept_workspace_size.argtypes = [i32, i32]
+    lib.spec_accept_workspace_size.restype = sz
+    lib.spec_greedy_accept.argtypes = [P, P, i32, i32, i32, P, P, P, P, sz, P]
+    lib.spec_greedy_accept.restype = ctypes.c_int
+    lib.spec_last_error.argtypes = []
+    lib.spec_last_error.restype = ctypes.c_char_p
+    lib.spec_version.argtypes = []
+    lib.spec_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != SPEC_OK:
+        raise SpecError(rc, load().spec_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_desc(*, batch, q_len, num_q_heads, num_kv_heads, head_dim,
+              page_size, num_pages, max_pages_per_seq, kv_dtype="bf16",
+              checked=False) -> AttnDesc:
+    return AttnDesc(batch, q_len, num_q_heads, num_kv_heads, head_dim,
+                    page_size, num_pages, max_pages_per_seq,
+                    SPEC_KV_BF16 if kv_dtype == "bf16" else SPEC_KV_FP8_E4M3,
+                    SPEC_FLAG_CHECKED if checked else 0)
+
+
+def desc_for(q: torch.Tensor, k_pages: torch.Tensor,
+             page_table: torch.Tensor, checked: bool = False) -> AttnDesc:
+    B, q_len, hq, d = q.shape
+    num_pages, hkv, ps, d2 = k_pages.shape
+    assert d2 == d
+    return make_desc(batch=B, q_len=q_len, num_q_heads=hq, num_kv_heads=hkv,
+                     head_dim=d, page_size=ps, num_pages=num_pages,
+                     max_pages_per_seq=page_table.shape[1],
+                     kv_dtype="fp8" if k_pages.dtype == torch.uint8 else "bf16",
+                     checked=checked)
+
+
+def verify_workspace_size(desc: AttnDesc) -> int:
+    n = load().spec_verify_workspace_size(ctypes.byref(desc))
+    if n == 0:
+        raise SpecError(SPEC_ERR_ARG, load().spec_last_error().decode())
+    return int(n)
+
+
+def accept_workspace_size(rows: int, vocab: int) -> int:
+    return int(load().spec_accept_workspace_size(rows, vocab))
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator hands out 512-byte aligned blocks
+    return torch.empty(max(1, nbytes), dtype=torch.uint8, device=device)
+
+
+def verify_attention_into(desc: AttnDesc, q, k_pages, v_pages, k_scales,
+                          v_scales, page_table, seq_lens, scale: float, out,
+                          workspace: torch.Tensor, stream=None) -> None:
+    _check(load().spec_verify_attention(
+        ctypes.byref(desc), _ptr(q), _ptr(k_pages), _ptr(v_pages),
+        _ptr(k_scales), _ptr(v_scales), _ptr(page_table), _ptr(seq_lens),
+        float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+
+
+def verify_attention(q, k_pages, v_pages, page_table, seq_lens, *,
+                     scale: float, k_scales=None, v_scales=None,
+                     out: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None,
+                     checked: bool = False, stream=None) -> torch.Tensor:
+    """Verify attention on device tensors; returns out bf16 [B, q_len, Hq, D]."""
+    desc = desc_for(q, k_pages, page_table, checked)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_workspace(verify_workspace_size(desc), q.device)
+    verify_attention_into(desc, q, k_pages, v_pages, k_scales, v_scales,
+                          page_table, seq_lens, scale, out, workspace, stream)
+    return out
+
+
+def verify_status(workspace: torch.Tensor, clear: bool = True,
+                  stream=None) -> int:
+    st = ctypes.c_uint32(0)
+    _check(load().spec_verify_status(_ptr(workspace), ctypes.byref(st),
+                                     int(clear), _stream(stream)))
+    return int(st.value)
+
+
+def greedy_accept_into(logits, draft_ids, accept_len, next_token, out_tokens,
+                       workspace: torch.Tensor, stream=None) -> None:
+    B, q_len = draft_ids.shape
+    _check(load().spec_greedy_accept(
+        _ptr(logits), _ptr(draft_ids), B, q_len, logits.shape[-1],
+        _ptr(accept_len), _ptr(next_token), _ptr(out_tokens),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def greedy_accept(logits: torch.Tensor, draft_ids: torch.Tensor, *,
+                  workspace: Optional[torch.Tensor] = None,
+                  with_tokens: bool = True, stream=None):
+    """Returns (accept_len [B], next_token [B], out_tokens [B, q_len] or None)."""
+    B, q_len = draft_ids.shape
+    dev = logits.device
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = (torch.empty((B, q_len), dtype=torch.int32, device=dev)
+            if with_tokens else None)
+    if workspace is None:
+        workspace = alloc_workspace(
+            accept_workspace_size(B * q_len, logits.shape[-1]), dev)
+    greedy_accept_into(logits, draft_ids, acc, nxt, toks, workspace, stream)
+    return acc, nxt, toks

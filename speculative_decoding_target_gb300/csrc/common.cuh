@@ -1,0 +1,155 @@
+// Internal definitions shared by the verify-attention kernels and the C ABI.
+//
+// Work plan of the split-KV verify attention.  The KV of every (request b,
+// KV head g) pair -- a "segment" -- is cut into 64-token units.  Segments are
+// laid end to end in (b, g) order, giving U units in total; CTA c of the
+// fixed grid of P CTAs takes the contiguous unit range
+// [floor(c*U/P), floor((c+1)*U/P)), where P is the launched grid capped at
+// U so that no CTA's range is empty.  A segment touched by several CTAs is
+// "split": each touching CTA writes an fp32 partial (normalised output row
+// and base-2 log-sum-exp per block row) and the merge kernel combines them
+// ("Qwen3.8-27B-FP8" page, "Implemented execution path": split-context decode
+// with compact online-softmax partials and a merge).  A segment owned by one
+// CTA is written straight to the output.  Every kernel derives the same plan
+// from seq_lens on the device, so the grid never depends on host-side
+// lengths and the launch is graph-capturable.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace specv {
+
+constexpr int kHeadDim = 256;
+constexpr int kUnit = 64;        // tokens per plan unit
+constexpr int kMaxRows = 128;    // q_len * group rows of one KV head
+constexpr int kMaxBatch = 1024;  // requests per call (shared-memory prefix)
+constexpr int kWsHeader = 256;   // bytes; word 0 = status
+
+struct AttnParams {
+  const __nv_bfloat16* q;
+  const void* k_pages;
+  const void* v_pages;
+  const __half* k_scales;
+  const __half* v_scales;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  __nv_bfloat16* out;
+  float* part_o;      // [nslots, rows, 256]
+  float* part_lse;    // [nslots, rows] (base 2)
+  uint32_t* status;   // workspace word 0
+  int batch, q_len, hq, hkv, group, rows;
+  int page_size, log2_ps, num_pages, max_pages;
+  int max_tokens;     // max_pages * page_size: seq_lens clamp
+  int grid;           // P: CTAs of the split kernel
+  float scale_log2;   // softmax scale * log2(e)
+};
+
+__device__ __forceinline__ int clamp_len(int len, int cap) {
+  return len < 0 ? 0 : (len > cap ? cap : len);
+}
+
+__device__ __forceinline__ int units_of(int len) {
+  return (len + kUnit - 1) / kUnit;
+}
+
+// First unit of CTA c.
+__device__ __forceinline__ long long cta_start(int c, long long U, int P) {
+  return (long long)c * U / P;
+}
+
+// CTA whose range holds unit u (0 <= u < U).
+__device__ __forceinline__ int cta_of(long long u, long long U, int P) {
+  return (int)(((u + 1) * (long long)P - 1) / U);
+}
+
+// Number of CTAs that touch a segment starting at unit s0 with nt units.
+__device__ __forceinline__ int seg_splits(long long s0, int nt, long long U,
+                                          int P) {
+  if (nt <= 0) return 0;
+  return cta_of(s0 + nt - 1, U, P) - cta_of(s0, U, P) + 1;
+}
+
+// Exclusive prefix of units per request into s_pre[0..batch] (s_pre[0]=0).
+// Called by the whole block; ends with __syncthreads().
+__device__ __forceinline__ void plan_prefix(const AttnParams& p, int* s_pre) {
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    int carry = 0;
+    const int lane = tid;
+    for (int base = 0; base < p.batch; base += 32) {
+      int b = base + lane;
+      int v = b < p.batch ? units_of(clamp_len(p.seq_lens[b], p.max_tokens))
+                          : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+      }
+      if (b < p.batch) s_pre[b + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_pre[0] = 0;
+  }
+  __syncthreads();
+}
+
+// Effective grid: the launched grid capped at U (every CTA below it owns at
+// least one unit, so consecutive CTAs of a segment have consecutive ids).
+__device__ __forceinline__ int effective_grid(int grid, long long U) {
+  return U < grid ? (int)U : grid;
+}
+
+// Sum of splits of every segment before segment k (the partial-slot base of
+// segment k).  Called by one full warp; all lanes return the same value.
+__device__ __forceinline__ int slot_base_warp(const AttnParams& p,
+                                              const int* s_pre, int k,
+                                              long long U, int P) {
+  const int lane = threadIdx.x & 31;
+  int acc = 0;
+  for (int kk = lane; kk < k; kk += 32) {
+    int b = kk / p.hkv, g = kk - b * p.hkv;
+    int nt = s_pre[b + 1] - s_pre[b];
+    long long s0 = (long long)p.hkv * s_pre[b] + (long long)g * nt;
+    acc += seg_splits(s0, nt, U, P);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  return acc;
+}
+
+// Request owning unit u: the largest b with hkv * s_pre[b] <= u.
+__device__ __forceinline__ int find_request(const int* s_pre, int batch,
+                                            int hkv, long long u) {
+  int lo = 0, hi = batch - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if ((long long)hkv * s_pre[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Launchers (defined in the kernel translation units).
+cudaError_t launch_verify_split_bf16(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_verify_merge(const AttnParams& p, cudaStream_t s);
+int verify_split_bf16_ctas_per_sm(int rows);
+
+struct AcceptParams {
+  const float* logits;
+  const int32_t* draft_ids;
+  int32_t* accept_len;
+  int32_t* next_token;
+  int32_t* out_tokens;
+  float* part_val;   // [rows, chunks]
+  int32_t* part_idx; // [rows, chunks]
+  int batch, q_len, vocab, rows, chunks;
+  int vec4;          // logits rows are 16-byte aligned and vocab % 4 == 0
+};
+constexpr int kAcceptChunk = 8192;   // logits per argmax-partial CTA
+constexpr int kAcceptThreads = 256;
+
+cudaError_t launch_greedy_accept(const AcceptParams& p, cudaStream_t s);
+
+}  // namespace specv

@@ -1,0 +1,302 @@
+// C ABI of the verify library: host-side validation, workspace layout and
+// kernel launches.  Every error is detected here, before anything is
+// enqueued, except a failed launch (SPEC_ERR_CUDA).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "spec_verify.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sms[kMaxDevices];
+int g_occ[kMaxDevices][9];  // split-kernel CTAs per SM by compute warps
+
+int current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess)
+    return fail(SPEC_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (*dev < 0 || *dev >= kMaxDevices)
+    return fail(SPEC_ERR_UNSUPPORTED, "device ordinal %d too large", *dev);
+  return SPEC_OK;
+}
+
+// Split-kernel grid for `rows` query rows per KV head on the current device:
+// every SM filled with as many CTAs as fit.
+int split_grid(int rows, int* grid) {
+  int dev;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  const int w = (rows + 15) / 16;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    cudaError_t e =
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || n <= 0)
+      return fail(SPEC_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
+    g_sms[dev] = n;
+  }
+  if (!g_occ[dev][w]) {
+    int occ = specv::verify_split_bf16_ctas_per_sm(rows);
+    if (occ <= 0)
+      return fail(SPEC_ERR_CUDA, "split kernel does not fit on an SM");
+    g_occ[dev][w] = occ;
+  }
+  *grid = g_sms[dev] * g_occ[dev][w];
+  return SPEC_OK;
+}
+
+int check_desc(const spec_attn_desc* d) {
+  if (!d) return fail(SPEC_ERR_ARG, "desc is NULL");
+  if (d->batch < 0 || d->batch > specv::kMaxBatch)
+    return fail(SPEC_ERR_ARG, "batch %d outside [0, %d]", d->batch,
+                specv::kMaxBatch);
+  if (d->q_len < 1 || d->q_len > 16)
+    return fail(SPEC_ERR_ARG, "q_len %d outside [1, 16]", d->q_len);
+  if (d->num_q_heads < 1 || d->num_kv_heads < 1 ||
+      d->num_q_heads % d->num_kv_heads)
+    return fail(SPEC_ERR_ARG, "num_q_heads %d not a multiple of num_kv_heads %d",
+                d->num_q_heads, d->num_kv_heads);
+  if (d->head_dim != specv::kHeadDim)
+    return fail(SPEC_ERR_UNSUPPORTED, "head_dim %d (only 256)", d->head_dim);
+  const long long rows =
+      (long long)d->q_len * (d->num_q_heads / d->num_kv_heads);
+  if (rows > specv::kMaxRows)
+    return fail(SPEC_ERR_UNSUPPORTED, "q_len * group = %lld > %d", rows,
+                specv::kMaxRows);
+  if (d->page_size < 1 || d->page_size > 4096 ||
+      (d->page_size & (d->page_size - 1)))
+    return fail(SPEC_ERR_ARG, "page_size %d is not a power of two in [1, 4096]",
+                d->page_size);
+  if (d->num_pages < 1 || d->max_pages_per_seq < 1)
+    return fail(SPEC_ERR_ARG, "num_pages %d / max_pages_per_seq %d must be >= 1",
+                d->num_pages, d->max_pages_per_seq);
+  const long long max_tokens = (long long)d->max_pages_per_seq * d->page_size;
+  if (max_tokens > (1LL << 30))
+    return fail(SPEC_ERR_ARG, "max_pages_per_seq * page_size exceeds 2^30");
+  const long long units = (long long)d->batch * d->num_kv_heads *
+                          ((max_tokens + specv::kUnit - 1) / specv::kUnit);
+  if (units > (1LL << 30))
+    return fail(SPEC_ERR_ARG, "batch * kv heads * units exceeds 2^30");
+  if (d->batch * (long long)d->num_kv_heads > 65535)
+    return fail(SPEC_ERR_ARG, "batch * num_kv_heads exceeds 65535");
+  if (d->kv_dtype != SPEC_KV_BF16 && d->kv_dtype != SPEC_KV_FP8_E4M3)
+    return fail(SPEC_ERR_ARG, "kv_dtype %d", d->kv_dtype);
+  if (d->flags & ~SPEC_FLAG_CHECKED)
+    return fail(SPEC_ERR_ARG, "unknown flags 0x%x", d->flags);
+  return SPEC_OK;
+}
+
+struct Layout {
+  int rows, grid, nslots;
+  size_t o_off, lse_off, bytes;
+};
+
+int layout(const spec_attn_desc* d, Layout* L) {
+  L->rows = d->q_len * (d->num_q_heads / d->num_kv_heads);
+  int rc = split_grid(L->rows, &L->grid);
+  if (rc) return rc;
+  L->nslots = L->grid + d->batch * d->num_kv_heads;
+  const size_t o_bytes =
+      (size_t)L->nslots * L->rows * specv::kHeadDim * sizeof(float);
+  const size_t lse_bytes = (size_t)L->nslots * L->rows * sizeof(float);
+  L->o_off = specv::kWsHeader;
+  L->lse_off = L->o_off + round_up(o_bytes, 256);
+  L->bytes = L->lse_off + round_up(lse_bytes, 256);
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spec_last_error(void) { return g_err; }
+
+const char* spec_version(void) { return "spec_verify 0.1 (sm_103a)"; }
+
+size_t spec_verify_workspace_size(const spec_attn_desc* desc) {
+  if (check_desc(desc)) return 0;
+  Layout L;
+  if (layout(desc, &L)) return 0;
+  return L.bytes;
+}
+
+int spec_verify_attention(const spec_attn_desc* desc, const void* q,
+                          const void* k_pages, const void* v_pages,
+                          const void* k_scales, const void* v_scales,
+                          const int32_t* page_table, const int32_t* seq_lens,
+                          float scale, void* out, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (desc->batch == 0) return SPEC_OK;
+  if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !out)
+    return fail(SPEC_ERR_ARG, "NULL tensor pointer");
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
+    return fail(SPEC_ERR_ARG, "scale is not finite");
+  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+      !aligned(out, 16))
+    return fail(SPEC_ERR_ALIGN, "q, k_pages, v_pages and out must be 16-byte aligned");
+  if (!aligned(page_table, 4) || !aligned(seq_lens, 4))
+    return fail(SPEC_ERR_ALIGN, "page_table and seq_lens must be 4-byte aligned");
+  if (desc->kv_dtype == SPEC_KV_FP8_E4M3) {
+    if (!k_scales || !v_scales)
+      return fail(SPEC_ERR_ARG, "FP8 KV needs k_scales and v_scales");
+    if (!aligned(k_scales, 8) || !aligned(v_scales, 8))
+      return fail(SPEC_ERR_ALIGN, "scales must be 8-byte aligned");
+    return fail(SPEC_ERR_UNSUPPORTED, "FP8 KV is not built yet");
+  }
+  Layout L;
+  rc = layout(desc, &L);
+  if (rc) return rc;
+  if (!workspace) return fail(SPEC_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 256))
+    return fail(SPEC_ERR_ALIGN, "workspace must be 256-byte aligned");
+  if (workspace_bytes < L.bytes)
+    return fail(SPEC_ERR_WORKSPACE, "workspace %zu bytes < %zu needed",
+                workspace_bytes, L.bytes);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  specv::AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_pages = k_pages;
+  p.v_pages = v_pages;
+  p.k_scales = static_cast<const __half*>(k_scales);
+  p.v_scales = static_cast<const __half*>(v_scales);
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.part_o = reinterpret_cast<float*>(ws + L.o_off);
+  p.part_lse = reinterpret_cast<float*>(ws + L.lse_off);
+  p.status = nullptr;
+  p.batch = desc->batch;
+  p.q_len = desc->q_len;
+  p.hq = desc->num_q_heads;
+  p.hkv = desc->num_kv_heads;
+  p.group = desc->num_q_heads / desc->num_kv_heads;
+  p.rows = L.rows;
+  p.page_size = desc->page_size;
+  p.log2_ps = 0;
+  while ((1 << p.log2_ps) < desc->page_size) ++p.log2_ps;
+  p.num_pages = desc->num_pages;
+  p.max_pages = desc->max_pages_per_seq;
+  p.max_tokens = desc->max_pages_per_seq * desc->page_size;
+  p.grid = L.grid;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  cudaError_t e;
+  if (desc->flags & SPEC_FLAG_CHECKED) {
+    p.status = reinterpret_cast<uint32_t*>(ws);
+    e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess)
+      return fail(SPEC_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
+  }
+  e = specv::launch_verify_split_bf16(p, s);
+  if (e != cudaSuccess)
+    return fail(SPEC_ERR_CUDA, "split kernel launch: %s", cudaGetErrorString(e));
+  e = specv::launch_verify_merge(p, s);
+  if (e != cudaSuccess)
+    return fail(SPEC_ERR_CUDA, "merge kernel launch: %s", cudaGetErrorString(e));
+  return SPEC_OK;
+}
+
+int spec_verify_status(const void* workspace, uint32_t* status_out,
+                       int32_t clear, void* stream) {
+  g_err[0] = 0;
+  if (!workspace || !status_out)
+    return fail(SPEC_ERR_ARG, "NULL workspace or status_out");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(status_out, workspace, sizeof(uint32_t),
+                                  cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear)
+    e = cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess)
+    return fail(SPEC_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  return SPEC_OK;
+}
+
+size_t spec_accept_workspace_size(int32_t rows, int32_t vocab) {
+  if (rows < 0 || vocab < 1) {
+    fail(SPEC_ERR_ARG, "rows %d / vocab %d", rows, vocab);
+    return 0;
+  }
+  const size_t chunks = ((size_t)vocab + specv::kAcceptChunk - 1) /
+                        specv::kAcceptChunk;
+  return round_up((size_t)rows * chunks * sizeof(float), 256) +
+         round_up((size_t)rows * chunks * sizeof(int32_t), 256) + 256;
+}
+
+int spec_greedy_accept(const float* logits, const int32_t* draft_ids,
+                       int32_t batch, int32_t q_len, int32_t vocab,
+                       int32_t* accept_len, int32_t* next_token,
+                       int32_t* out_tokens, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  if (batch < 0) return fail(SPEC_ERR_ARG, "batch %d < 0", batch);
+  if (q_len < 1 || q_len > 16)
+    return fail(SPEC_ERR_ARG, "q_len %d outside [1, 16]", q_len);
+  if (vocab < 1) return fail(SPEC_ERR_ARG, "vocab %d < 1", vocab);
+  if ((long long)batch * q_len > 65535)
+    return fail(SPEC_ERR_ARG, "batch * q_len exceeds 65535");
+  if (batch == 0) return SPEC_OK;
+  if (!logits || !draft_ids || !accept_len || !next_token)
+    return fail(SPEC_ERR_ARG, "NULL tensor pointer");
+  if (!aligned(logits, 4) || !aligned(draft_ids, 4) || !aligned(accept_len, 4) ||
+      !aligned(next_token, 4) || (out_tokens && !aligned(out_tokens, 4)))
+    return fail(SPEC_ERR_ALIGN, "logits and int32 buffers must be 4-byte aligned");
+  if (!workspace) return fail(SPEC_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 16))
+    return fail(SPEC_ERR_ALIGN, "workspace must be 16-byte aligned");
+  const int rows = batch * q_len;
+  const size_t need = spec_accept_workspace_size(rows, vocab);
+  if (workspace_bytes < need)
+    return fail(SPEC_ERR_WORKSPACE, "workspace %zu bytes < %zu needed",
+                workspace_bytes, need);
+  specv::AcceptParams p;
+  p.logits = logits;
+  p.draft_ids = draft_ids;
+  p.accept_len = accept_len;
+  p.next_token = next_token;
+  p.out_tokens = out_tokens;
+  p.batch = batch;
+  p.q_len = q_len;
+  p.vocab = vocab;
+  p.rows = rows;
+  p.chunks = (vocab + specv::kAcceptChunk - 1) / specv::kAcceptChunk;
+  p.vec4 = (vocab % 4 == 0) && aligned(logits, 16);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.part_val = reinterpret_cast<float*>(ws);
+  p.part_idx = reinterpret_cast<int32_t*>(
+      ws + round_up((size_t)rows * p.chunks * sizeof(float), 256));
+  cudaError_t e = specv::launch_greedy_accept(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(SPEC_ERR_CUDA, "accept kernel launch: %s", cudaGetErrorString(e));
+  return SPEC_OK;
+}
+
+}  // extern "C"

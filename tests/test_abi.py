@@ -1,0 +1,125 @@
+"""The C-ABI library builds, loads and exports every declared symbol, and its
+host-side argument checks reject bad calls before anything reaches a GPU
+(no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_target_gb300 import _native, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(spec_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _native.load()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert "spec_verify_attention" in declared
+    assert "spec_greedy_accept" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(_native.EXPORTED) == set(declared)
+
+
+def test_version_string(lib):
+    assert b"sm_103a" in lib.spec_version()
+
+
+def _desc(**kw):
+    base = dict(batch=2, q_len=8, num_q_heads=24, num_kv_heads=4,
+                head_dim=256, page_size=16, num_pages=64,
+                max_pages_per_seq=8)
+    base.update(kw)
+    return _native.make_desc(**base)
+
+
+FAKE = ctypes.c_void_p(0x100000)   # never dereferenced: checks come first
+
+
+def _attn(lib, desc, q=FAKE, scale=0.0625, ws_bytes=1 << 30, out=FAKE,
+          k_scales=None, v_scales=None):
+    return lib.spec_verify_attention(
+        ctypes.byref(desc) if desc is not None else None, q, FAKE, FAKE,
+        k_scales, v_scales, FAKE, FAKE, scale, out, FAKE, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q_len=0), _native.SPEC_ERR_ARG),
+    (dict(q_len=17), _native.SPEC_ERR_ARG),
+    (dict(num_q_heads=25), _native.SPEC_ERR_ARG),
+    (dict(num_kv_heads=0), _native.SPEC_ERR_ARG),
+    (dict(head_dim=128), _native.SPEC_ERR_UNSUPPORTED),
+    (dict(page_size=24), _native.SPEC_ERR_ARG),
+    (dict(page_size=0), _native.SPEC_ERR_ARG),
+    (dict(num_pages=0), _native.SPEC_ERR_ARG),
+    (dict(batch=-1), _native.SPEC_ERR_ARG),
+    (dict(batch=5000), _native.SPEC_ERR_ARG),
+    (dict(q_len=16, num_q_heads=36, num_kv_heads=4), _native.SPEC_ERR_UNSUPPORTED),
+])
+def test_bad_descriptors_rejected(lib, kw, code):
+    assert _attn(lib, _desc(**kw)) == code
+    assert lib.spec_last_error()
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    assert _attn(lib, None) == _native.SPEC_ERR_ARG
+    assert _attn(lib, _desc(), q=None) == _native.SPEC_ERR_ARG
+    assert _attn(lib, _desc(), q=ctypes.c_void_p(0x100008)) == \
+        _native.SPEC_ERR_ALIGN
+    assert _attn(lib, _desc(), out=ctypes.c_void_p(0x100002)) == \
+        _native.SPEC_ERR_ALIGN
+    assert _attn(lib, _desc(), scale=float("nan")) == _native.SPEC_ERR_ARG
+    assert _attn(lib, _desc(), scale=float("inf")) == _native.SPEC_ERR_ARG
+    fp8 = _desc(kv_dtype="fp8")
+    assert _attn(lib, fp8) == _native.SPEC_ERR_ARG          # scales missing
+
+
+def test_empty_batch_is_a_noop(lib):
+    assert _attn(lib, _desc(batch=0), q=None) == _native.SPEC_OK
+
+
+def test_accept_argument_checks(lib):
+    f = lib.spec_greedy_accept
+    ok = dict(batch=2, q_len=8, vocab=1000)
+
+    def call(batch=2, q_len=8, vocab=1000, logits=FAKE, ws=FAKE,
+             ws_bytes=1 << 20, drafts=FAKE):
+        return f(logits, drafts, batch, q_len, vocab, FAKE, FAKE, None, ws,
+                 ws_bytes, None)
+
+    assert call(q_len=0) == _native.SPEC_ERR_ARG
+    assert call(q_len=17) == _native.SPEC_ERR_ARG
+    assert call(vocab=0) == _native.SPEC_ERR_ARG
+    assert call(batch=-3) == _native.SPEC_ERR_ARG
+    assert call(batch=0, logits=None) == _native.SPEC_OK
+    assert call(logits=None) == _native.SPEC_ERR_ARG
+    assert call(drafts=ctypes.c_void_p(0x100001)) == _native.SPEC_ERR_ALIGN
+    assert call(ws=None) == _native.SPEC_ERR_WORKSPACE
+    need = lib.spec_accept_workspace_size(16, 1000)
+    assert call(ws_bytes=need - 1) == _native.SPEC_ERR_WORKSPACE
+    assert ok
+
+
+def test_accept_workspace_size_formula(lib):
+    # one (fp32 value, int32 index) pair per row and 8192-entry vocab chunk
+    chunks = -(-248320 // 8192)
+    n = lib.spec_accept_workspace_size(64, 248320)
+    assert n >= 64 * chunks * 8
+    assert n <= 64 * chunks * 8 + 3 * 256
+    assert lib.spec_accept_workspace_size(-1, 10) == 0

@@ -1,0 +1,135 @@
+"""GPU verify attention (through the C ABI) against the CPU float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from speculative_decoding_target_gb300 import workloads as wl
+from gpu_helpers import (assert_attention_close, gpu_attention,
+                         oracle_attention, rows_of)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _case(B, q_len, prefix, ps, kv_dtype="bf16", hq=24, hkv=4, seed=0,
+          **kw):
+    prefixes = [prefix, prefix // 2 + 3, prefix + 5][:B] if B <= 3 else \
+        list(prefix)
+    return wl.make_attention_inputs(
+        batch=B, q_len=q_len, num_q_heads=hq, num_kv_heads=hkv, head_dim=256,
+        page_size=ps, prefix_lens=prefixes, kv_dtype=kv_dtype, seed=seed,
+        device=DEV, **kw)
+
+
+def _check_all(inp, what):
+    out = gpu_attention(inp)
+    ref = oracle_attention(inp)
+    assert_attention_close(rows_of(out), ref, inp["k_scales"] is not None,
+                           what)
+    return out
+
+
+PREFIXES = [0, 1, 15, 16, 17, 63, 64, 65, 321, 4096]
+
+
+@pytest.mark.parametrize("q_len", [1, 8, 16])
+@pytest.mark.parametrize("pi", range(len(PREFIXES)))
+def test_grid_bf16(q_len, pi):
+    prefix = PREFIXES[pi]
+    ps = 16 if pi % 2 == 0 else 64
+    B = 1 if pi % 3 == 0 else 3
+    inp = _case(B, q_len, prefix, ps, seed=100 * q_len + pi)
+    _check_all(inp, f"q_len={q_len} prefix={prefix} ps={ps} B={B}")
+
+
+@pytest.mark.parametrize("hq,hkv,q_len", [(8, 8, 8), (32, 4, 16), (4, 1, 16),
+                                          (24, 4, 3), (12, 2, 5)])
+def test_gqa_shapes(hq, hkv, q_len):
+    inp = _case(2, q_len, 200, 16, hq=hq, hkv=hkv, seed=hq + q_len)
+    _check_all(inp, f"Hq={hq} Hkv={hkv} q_len={q_len}")
+
+
+@pytest.mark.parametrize("ps", [1, 4, 128, 256])
+def test_page_sizes(ps):
+    inp = _case(2, 8, 300, ps, seed=ps)
+    _check_all(inp, f"page_size={ps}")
+
+
+def test_many_ragged_requests_exercise_the_plan():
+    g = torch.Generator().manual_seed(5)
+    prefixes = torch.randint(0, 3000, (40,), generator=g).tolist()
+    prefixes[3] = 0
+    prefixes[7] = 64 * 20 - 8
+    inp = _case(40, 8, prefixes, 64, seed=77)
+    _check_all(inp, "40 ragged requests")
+
+
+def test_short_and_empty_windows_give_zero_rows():
+    # seq_len < q_len: rows whose causal window is empty output zeros;
+    # seq_len = 0: every row of that request is zero.
+    inp = _case(3, 8, 10, 16, seed=3)
+    inp["seq_lens"] = torch.tensor([5, 0, 8], dtype=torch.int32, device=DEV)
+    out = _check_all(inp, "short windows")
+    o = out.float().view(3, 8, 24, 256)
+    assert torch.all(o[0, :3] == 0) and torch.any(o[0, 3:] != 0)
+    assert torch.all(o[1] == 0)
+
+
+def test_result_independent_of_workspace_contents_and_repeatable():
+    inp = _case(2, 16, 5000, 64, seed=9)
+    import speculative_decoding_target_gb300 as sv
+    desc = sv.desc_for(inp["q"], inp["k_pages"], inp["page_table"])
+    ws = torch.full((sv.verify_workspace_size(desc),), 0xFF,
+                    dtype=torch.uint8, device=DEV)   # NaN-patterned garbage
+    a = gpu_attention(inp, workspace=ws)
+    b = gpu_attention(inp, workspace=ws)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    ref = oracle_attention(inp)
+    assert_attention_close(rows_of(a), ref, False, "garbage workspace")
+
+
+def test_bad_page_id_sets_status_without_fault():
+    import speculative_decoding_target_gb300 as sv
+    inp = _case(1, 8, 500, 16, seed=4)
+    inp["page_table"][0, 3] = 1 << 20      # outside the pool
+    desc = sv.desc_for(inp["q"], inp["k_pages"], inp["page_table"],
+                       checked=True)
+    ws = sv.alloc_workspace(sv.verify_workspace_size(desc), DEV)
+    sv.verify_attention(inp["q"], inp["k_pages"], inp["v_pages"],
+                        inp["page_table"], inp["seq_lens"],
+                        scale=inp["scale"], checked=True, workspace=ws)
+    assert sv.verify_status(ws) == sv._native.SPEC_STATUS_BAD_PAGE
+    # a clean call afterwards reports nothing
+    inp["page_table"][0, 3] = 0
+    sv.verify_attention(inp["q"], inp["k_pages"], inp["v_pages"],
+                        inp["page_table"], inp["seq_lens"],
+                        scale=inp["scale"], checked=True, workspace=ws)
+    assert sv.verify_status(ws) == 0
+
+
+def _sample_rows(w, n, seed):
+    total = w.batch * w.q_len * w.num_q_heads
+    g = np.random.default_rng(seed)
+    rows = set(g.choice(total, size=min(n, total), replace=False).tolist())
+    for b in range(w.batch):            # first and last block row of each
+        for i in (0, w.q_len - 1):
+            rows.add((b * w.q_len + i) * w.num_q_heads + (b * 7) % 24)
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", [n for n in wl.WORKLOAD_ORDER
+                                  if wl.WORKLOADS[n].kv_dtype == "bf16"])
+def test_full_size_workloads_sampled_rows(name):
+    w = wl.WORKLOADS[name]
+    inp = wl.workload_inputs(w, device=DEV, with_accept=False)
+    out = gpu_attention(inp)
+    torch.cuda.synchronize()
+    # property at any size: every output is a convex combination of V rows
+    vmax = inp["v_pages"].float().nan_to_num(0.0).abs().max().item()
+    o = out.float()
+    assert torch.isfinite(o).all()
+    assert o.abs().max().item() <= vmax * (1 + 2 ** -7)
+    n = 24 if w.batch * w.q_len * w.num_q_heads > 256 else 10 ** 9
+    rows = _sample_rows(w, n, w.seed)
+    ref = oracle_attention(inp, rows=np.asarray(rows, np.int64))
+    assert_attention_close(rows_of(out, rows), ref, False, name)
