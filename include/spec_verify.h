@@ -17,7 +17,9 @@
  *     spec_verify_status, and the returned strings is a DEVICE pointer of the
  *     current CUDA device.  The caller owns every buffer, including the
  *     workspaces; the library allocates no device memory and keeps no state
- *     between calls besides a per-device cache of the SM count.
+ *     between calls besides a per-device cache of the SM count (and the
+ *     fixed scratch array of spec_verify_attention_noalloc, which the CUDA
+ *     runtime reserves when it loads the library's GPU code on a device).
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
  *     enqueue kernels on it: no host synchronisation, no host<->device copy
  *     (spec_verify_status excepted).  The result is visible to later work on
@@ -184,6 +186,39 @@ int spec_greedy_accept(const float* logits, const int32_t* draft_ids,
                        int32_t* accept_len, int32_t* next_token,
                        int32_t* out_tokens, void* workspace,
                        size_t workspace_bytes, void* stream);
+
+/*
+ * Verify attention without a caller workspace, for callers that cannot
+ * allocate device memory (no cudaMalloc and no pool of their own: e.g. code
+ * handed only the input and output buffers of an engine that owns all device
+ * memory).  The pages have no counterpart of this entry point; it is an
+ * addition of this library.
+ *
+ * Arguments, layouts, results and errors are those of spec_verify_attention,
+ * minus the workspace.  The split partials live instead in a fixed device
+ * array of SPEC_NOALLOC_SCRATCH_BYTES inside the library, reserved on every
+ * GPU that loads the library until the process exits; the call allocates
+ * nothing.
+ *   - A shape whose workspace (spec_verify_workspace_size) exceeds
+ *     SPEC_NOALLOC_SCRATCH_BYTES is rejected with SPEC_ERR_WORKSPACE.
+ *   - SPEC_FLAG_CHECKED is rejected with SPEC_ERR_UNSUPPORTED (its status
+ *     word lives in a caller workspace).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, which may load the library's GPU code on that
+ *     device); make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; nothing in it needs to start at zero.  Calls whose kernels
+ *     overlap on the GPU (on different streams, or from different threads)
+ *     race on it: order them on one stream, or give each its own workspace
+ *     through spec_verify_attention.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int spec_verify_attention_noalloc(const spec_attn_desc* desc, const void* q,
+                                  const void* k_pages, const void* v_pages,
+                                  const void* k_scales, const void* v_scales,
+                                  const int32_t* page_table,
+                                  const int32_t* seq_lens, float scale,
+                                  void* out, void* stream);
 
 /* Message for the last nonzero return on this thread ("" if none). */
 const char* spec_last_error(void);

@@ -30,8 +30,9 @@ SPEC_STATUS_BAD_PAGE = 1
 EXPORTED = (
     "spec_verify_workspace_size", "spec_verify_attention",
     "spec_verify_status", "spec_accept_workspace_size", "spec_greedy_accept",
-    "spec_last_error", "spec_version",
+    "spec_last_error", "spec_version", "spec_verify_attention_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 class SpecError(RuntimeError):
@@ -70,6 +71,9 @@ def load(path: str = LIB_PATH):
         ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P, ctypes.c_float, P, P,
         sz, P]
     lib.spec_verify_attention.restype = ctypes.c_int
+    lib.spec_verify_attention_noalloc.argtypes = [
+        ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P, ctypes.c_float, P, P]
+    lib.spec_verify_attention_noalloc.restype = ctypes.c_int
     lib.spec_verify_status.argtypes = [P, ctypes.POINTER(u32), i32, P]
     lib.spec_verify_status.restype = ctypes.c_int
     lib.spec_accept_workspace_size.argtypes = [i32, i32]
@@ -159,6 +163,22 @@ def verify_attention(q, k_pages, v_pages, page_table, seq_lens, *,
         workspace = alloc_workspace(verify_workspace_size(desc), q.device)
     verify_attention_into(desc, q, k_pages, v_pages, k_scales, v_scales,
                           page_table, seq_lens, scale, out, workspace, stream)
+    return out
+
+
+def verify_attention_noalloc(q, k_pages, v_pages, page_table, seq_lens, *,
+                             scale: float, k_scales=None, v_scales=None,
+                             out: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
+    """Verify attention with the library's fixed scratch instead of a
+    workspace (for callers that cannot allocate device memory)."""
+    desc = desc_for(q, k_pages, page_table)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().spec_verify_attention_noalloc(
+        ctypes.byref(desc), _ptr(q), _ptr(k_pages), _ptr(v_pages),
+        _ptr(k_scales), _ptr(v_scales), _ptr(page_table), _ptr(seq_lens),
+        float(scale), _ptr(out), _stream(stream)))
     return out
 
 

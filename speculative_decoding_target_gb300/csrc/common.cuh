@@ -131,6 +131,9 @@ __device__ __forceinline__ int find_request(const int* s_pre, int batch,
   return lo;
 }
 
+// Record an error message for spec_last_error() and return `code`.
+int set_error(int code, const char* fmt, ...);
+
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_verify_split_bf16(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_verify_merge(const AttnParams& p, cudaStream_t s);

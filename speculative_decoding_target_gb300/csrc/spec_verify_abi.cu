@@ -129,6 +129,16 @@ int layout(const spec_attn_desc* d, Layout* L) {
 
 }  // namespace
 
+namespace specv {
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+}  // namespace specv
+
 extern "C" {
 
 const char* spec_last_error(void) { return g_err; }
