@@ -49,6 +49,8 @@ extern "C" {
 
 /* Device-side status bits (see spec_verify_status). */
 #define SPEC_STATUS_BAD_PAGE 1u   /* a page id outside [0, num_pages) */
+#define SPEC_STATUS_TIMEOUT 2u    /* a kernel wait ran past its bound (a bug,
+                                     not a data condition); output invalid */
 
 typedef enum {
   SPEC_KV_BF16 = 0,     /* K/V elements are bf16 */
@@ -127,9 +129,9 @@ size_t spec_verify_workspace_size(const spec_attn_desc* desc);
  *   workspace device scratch of >= spec_verify_workspace_size(desc) bytes,
  *             256-byte aligned; contents need no initialisation
  *
- * Page ids outside [0, num_pages) are never dereferenced: their tokens read
- * as zeros, and with SPEC_FLAG_CHECKED the status word records
- * SPEC_STATUS_BAD_PAGE.  The KV is split into contiguous runs of 64-token
+ * Page ids outside [0, num_pages) are never dereferenced; the rows that
+ * would read them get unspecified output, and with SPEC_FLAG_CHECKED the
+ * status word records SPEC_STATUS_BAD_PAGE.  The KV is split into contiguous runs of 64-token
  * tiles, one run per CTA of a fixed grid; runs that cover part of a
  * (request, KV head) produce fp32 partials (o, lse) that a second kernel
  * merges ("Qwen3.8-27B-FP8" page, "Implemented execution path": split-context

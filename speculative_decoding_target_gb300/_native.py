@@ -26,6 +26,7 @@ SPEC_KV_BF16 = 0
 SPEC_KV_FP8_E4M3 = 1
 SPEC_FLAG_CHECKED = 1
 SPEC_STATUS_BAD_PAGE = 1
+SPEC_STATUS_TIMEOUT = 2
 
 EXPORTED = (
     "spec_verify_workspace_size", "spec_verify_attention",

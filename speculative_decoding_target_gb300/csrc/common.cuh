@@ -15,6 +15,7 @@
 // lengths and the launch is graph-capturable.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -44,6 +45,7 @@ struct AttnParams {
   int page_size, log2_ps, num_pages, max_pages;
   int max_tokens;     // max_pages * page_size: seq_lens clamp
   int grid;           // P: CTAs of the split kernel
+  int box_rows;       // TMA box height (tcgen05 kernel): min(page_size, 32)
   float scale_log2;   // softmax scale * log2(e)
 };
 
@@ -138,6 +140,13 @@ int set_error(int code, const char* fmt, ...);
 cudaError_t launch_verify_split_bf16(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_verify_merge(const AttnParams& p, cudaStream_t s);
 int verify_split_bf16_ctas_per_sm(int rows);
+cudaError_t launch_verify_split_tc(const AttnParams& p, const CUtensorMap& tm_k,
+                                   const CUtensorMap& tm_v, cudaStream_t s);
+int verify_split_tc_ctas_per_sm();
+int verify_split_tc_box_rows(int page_size);
+// The tcgen05 kernel loads whole 8-row swizzle groups with TMA, so it needs
+// pages of at least 8 tokens; smaller pages take the mma.sync kernel.
+constexpr int kTcMinPageSize = 8;
 
 struct AcceptParams {
   const float* logits;

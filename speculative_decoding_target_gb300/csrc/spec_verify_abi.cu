@@ -6,6 +6,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "spec_verify.h"
 
@@ -30,7 +32,51 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_sms[kMaxDevices];
-int g_occ[kMaxDevices][9];  // split-kernel CTAs per SM by compute warps
+int g_occ[kMaxDevices][10];  // split-kernel CTAs per SM: [w] mma.sync with w
+                             // compute warps, [9] the tcgen05 kernel
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool use_tc(const spec_attn_desc* d) {
+  return d->page_size >= specv::kTcMinPageSize;
+}
+
+int tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion(
+        "cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f)
+      return fail(SPEC_ERR_CUDA, "cuTensorMapEncodeTiled unavailable: %s",
+                  cudaGetErrorString(e));
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  *fn = g_encode;
+  return SPEC_OK;
+}
+
+// 2-D view of a bf16 page pool: rows = num_pages * Hkv * page_size, 256
+// elements (512 bytes) per row; boxes of 64 elements x box_rows rows with
+// the 128-byte swizzle.
+int make_pool_map(CUtensorMap* map, const void* base, long long rows,
+                  int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int rc = tensor_map_encoder(&enc);
+  if (rc) return rc;
+  cuuint64_t dims[2] = {(cuuint64_t)specv::kHeadDim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)specv::kHeadDim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t elem[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, elem,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(SPEC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return SPEC_OK;
+}
 
 int current_device(int* dev) {
   cudaError_t e = cudaGetDevice(dev);
@@ -43,11 +89,11 @@ int current_device(int* dev) {
 
 // Split-kernel grid for `rows` query rows per KV head on the current device:
 // every SM filled with as many CTAs as fit.
-int split_grid(int rows, int* grid) {
+int split_grid(int rows, bool tc, int* grid) {
   int dev;
   int rc = current_device(&dev);
   if (rc) return rc;
-  const int w = (rows + 15) / 16;
+  const int w = tc ? 9 : (rows + 15) / 16;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_sms[dev]) {
     int n = 0;
@@ -58,7 +104,8 @@ int split_grid(int rows, int* grid) {
     g_sms[dev] = n;
   }
   if (!g_occ[dev][w]) {
-    int occ = specv::verify_split_bf16_ctas_per_sm(rows);
+    int occ = tc ? specv::verify_split_tc_ctas_per_sm()
+                 : specv::verify_split_bf16_ctas_per_sm(rows);
     if (occ <= 0)
       return fail(SPEC_ERR_CUDA, "split kernel does not fit on an SM");
     g_occ[dev][w] = occ;
@@ -105,6 +152,9 @@ int check_desc(const spec_attn_desc* d) {
     return fail(SPEC_ERR_ARG, "kv_dtype %d", d->kv_dtype);
   if (d->flags & ~SPEC_FLAG_CHECKED)
     return fail(SPEC_ERR_ARG, "unknown flags 0x%x", d->flags);
+  if ((long long)d->num_pages * d->num_kv_heads * d->page_size >= (1LL << 31))
+    return fail(SPEC_ERR_UNSUPPORTED,
+                "num_pages * num_kv_heads * page_size must be < 2^31");
   return SPEC_OK;
 }
 
@@ -115,7 +165,7 @@ struct Layout {
 
 int layout(const spec_attn_desc* d, Layout* L) {
   L->rows = d->q_len * (d->num_q_heads / d->num_kv_heads);
-  int rc = split_grid(L->rows, &L->grid);
+  int rc = split_grid(L->rows, use_tc(d), &L->grid);
   if (rc) return rc;
   L->nslots = L->grid + d->batch * d->num_kv_heads;
   const size_t o_bytes =
@@ -143,7 +193,7 @@ extern "C" {
 
 const char* spec_last_error(void) { return g_err; }
 
-const char* spec_version(void) { return "spec_verify 0.1 (sm_103a)"; }
+const char* spec_version(void) { return "spec_verify 0.2 (sm_103a)"; }
 
 size_t spec_verify_workspace_size(const spec_attn_desc* desc) {
   if (check_desc(desc)) return 0;
@@ -216,7 +266,17 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
   p.max_pages = desc->max_pages_per_seq;
   p.max_tokens = desc->max_pages_per_seq * desc->page_size;
   p.grid = L.grid;
+  p.box_rows = specv::verify_split_tc_box_rows(desc->page_size);
   p.scale_log2 = scale * 1.4426950408889634f;
+  const bool tc = use_tc(desc);
+  CUtensorMap tm_k, tm_v;
+  if (tc) {
+    const long long pool_rows =
+        (long long)desc->num_pages * desc->num_kv_heads * desc->page_size;
+    rc = make_pool_map(&tm_k, k_pages, pool_rows, p.box_rows);
+    if (!rc) rc = make_pool_map(&tm_v, v_pages, pool_rows, p.box_rows);
+    if (rc) return rc;
+  }
 
   cudaError_t e;
   if (desc->flags & SPEC_FLAG_CHECKED) {
@@ -225,7 +285,8 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
     if (e != cudaSuccess)
       return fail(SPEC_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
   }
-  e = specv::launch_verify_split_bf16(p, s);
+  e = tc ? specv::launch_verify_split_tc(p, tm_k, tm_v, s)
+         : specv::launch_verify_split_bf16(p, s);
   if (e != cudaSuccess)
     return fail(SPEC_ERR_CUDA, "split kernel launch: %s", cudaGetErrorString(e));
   e = specv::launch_verify_merge(p, s);

@@ -1,0 +1,503 @@
+// Split-KV paged GQA verify attention on the 5th-generation tensor cores
+// (tcgen05 MMA with TMEM accumulators, TMA tile loads), bf16 KV.
+//
+// One CTA per SM walks its contiguous run of 64-token units (the plan in
+// common.cuh).  For every (request b, KV head g) piece of the run, all
+// q_len x group query rows that read KV head g form the M = 128 rows of one
+// MMA tile ("MTP and DFlash2 at long context on XPU", Part III: the query
+// positions of a verify block folded into the head dimension, so every KV
+// byte is read once).  Query row r sits at TMEM lane 32*(r / R) + r % R,
+// R = ceil(rows / 4), which spreads the rows over the four TMEM lane
+// quarters; the other lanes carry zero rows.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: gathers each 32-token K and V tile of the
+//               piece page by page from the pool (one 2-D box of 64 channels
+//               x min(page_size, 32) tokens per column block) into a 3-stage
+//               ring.
+//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
+//               S buffers, then O += P_{j-1} V_{j-1} into the TMEM O
+//               accumulator, so the softmax of tile j overlaps the MMAs.
+//   warps 2..5  softmax: one thread per TMEM lane (query row).  Load S_j,
+//               mask the block's causal tail, keep a running max m and sum l
+//               in base 2, write P_j = 2^(s - m) to shared memory as bf16
+//               hi + lo parts (P V is issued twice, so the bf16 rounding of
+//               P does not reach the output), rescale O in TMEM only when the
+//               running max grows by more than 2^8, and finally read O,
+//               divide by l and write the bf16 output or an fp32 partial.
+//
+// Every wait is bounded (about two seconds of clock); a wait that runs out
+// sets SPEC_STATUS_TIMEOUT in the status word (checked mode) and makes every
+// later wait of the CTA return at once, so the kernel always finishes.
+#include "common.cuh"
+#include "spec_verify.h"
+#include "tc_ptx.cuh"
+
+namespace specv {
+namespace {
+
+constexpr int kT = 32;                        // tokens per tile
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr int kQBytes = 4 * 128 * 128;        // Q: 4 column blocks x 128 rows
+constexpr int kHalfBytes = 4 * kT * 128;      // K (or V) of one stage
+constexpr int kStageBytes = 2 * kHalfBytes;
+constexpr int kPBytes = 128 * 128;            // P hi (or lo): 128 rows x 128 B
+constexpr int kOffKV = kQBytes;
+constexpr int kOffPhi = kOffKV + kStages * kStageBytes;
+constexpr int kOffPlo = kOffPhi + kPBytes;
+constexpr int kOffPre = kOffPlo + kPBytes;
+constexpr int kPreBytes = ((kMaxBatch + 1) * 4 + 127) / 128 * 128;
+constexpr int kSmemBytes = kOffPre + kPreBytes + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 256;               // S buffers: columns 256, 288
+constexpr long long kWaitCycles = 4000000000LL;
+constexpr float kRescaleLog2 = 8.0f;          // rescale O when m grows > 2^8
+
+constexpr uint32_t kIdescQK = tc::idesc_bf16(128, kT, 0);
+constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 256, 1);
+
+struct Bars {
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t drain;
+};
+
+struct Ctx {
+  Bars* bars;
+  volatile int* abort;
+  const AttnParams* p;
+};
+
+// Bounded wait on phase `parity` of an mbarrier.  Returns false (and flags
+// the CTA) when the bound runs out or another wait of the CTA already did.
+__device__ __noinline__ bool wait_bar(const Ctx& cx, uint64_t* bar,
+                                      uint32_t parity, bool ignore_abort = false) {
+  const uint32_t a = tc::smem_u32(bar);
+  if (tc::bar_try_wait(a, parity)) return true;
+  if (!ignore_abort && *cx.abort) return false;
+  const long long t0 = clock64();
+  while (true) {
+    if (tc::bar_try_wait(a, parity)) return true;
+    if (!ignore_abort && *cx.abort) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *cx.abort = 1;
+      if (cx.p->status) atomicOr(cx.p->status, SPEC_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+struct Piece {
+  int b, g, nt, len, tok_begin, tok_end, n_tiles;
+  long long s0;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// ---- warp 0, one thread: TMA loads of the piece's K/V tiles ---------------
+__device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* kv,
+                        const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
+  const AttnParams& p = *cx.p;
+  const int rpb = p.box_rows;
+  for (int jt = 0; jt < pc.n_tiles; ++jt) {
+    const int gj = gj0 + jt, st = gj % kStages;
+    if (gj >= kStages)
+      wait_bar(cx, &cx.bars->kv_empty[st], ((gj / kStages) - 1) & 1);
+    const int t0 = pc.tok_begin + jt * kT;
+    const int ntok = min(kT, pc.tok_end - t0);
+    const int nbox = (ntok + rpb - 1) / rpb;
+    const uint32_t full = tc::smem_u32(&cx.bars->kv_full[st]);
+    tc::bar_arrive_expect_tx(full, (uint32_t)(nbox * rpb * 128 * 4 * 2));
+    const uint32_t kdst = tc::smem_u32(kv + st * kStageBytes);
+    const uint32_t vdst = kdst + kHalfBytes;
+    for (int i = 0; i < nbox; ++i) {
+      const int t = t0 + i * rpb;
+      int page = __ldg(p.page_table + (long long)pc.b * p.max_pages +
+                       (t >> p.log2_ps));
+      if (page < 0 || page >= p.num_pages) {
+        if (p.status) atomicOr(p.status, SPEC_STATUS_BAD_PAGE);
+        page = 0;  // in bounds; the affected rows are unspecified
+      }
+      const int y = ((page * p.hkv + pc.g) << p.log2_ps) + (t & (p.page_size - 1));
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        const uint32_t off = cb * (kT * 128) + i * rpb * 128;
+        tc::tma_load_2d(kdst + off, tm_k, full, cb * 64, y);
+        tc::tma_load_2d(vdst + off, tm_v, full, cb * 64, y);
+      }
+    }
+  }
+}
+
+// ---- warp 1, one thread: MMA issue -------------------------------------------
+__device__ __forceinline__ void issue_pv(const Ctx& cx, int gj, bool first,
+                                         uint32_t tmem, uint8_t* smem) {
+  wait_bar(cx, &cx.bars->p_full[gj & 1], (gj >> 1) & 1);
+  tc::fence_after();
+  const int st = gj % kStages, h = gj & 1;
+  const uint32_t vbase = tc::smem_u32(smem + kOffKV + st * kStageBytes) + kHalfBytes;
+  const uint32_t phi = tc::smem_u32(smem + kOffPhi) + h * 64;
+  const uint32_t plo = tc::smem_u32(smem + kOffPlo) + h * 64;
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    const uint64_t bd = tc::desc_sw128(vbase + kk * 2048, kT * 128, 1024);
+    tc::mma_bf16(tmem, tc::desc_sw128(phi + kk * 32, 16, 1024), bd, kIdescPV,
+                 (first && kk == 0) ? 0u : 1u);
+    tc::mma_bf16(tmem, tc::desc_sw128(plo + kk * 32, 16, 1024), bd, kIdescPV, 1u);
+  }
+  tc::commit(tc::smem_u32(&cx.bars->kv_empty[st]));
+  tc::commit(tc::smem_u32(&cx.bars->pv_done[gj & 1]));
+}
+
+__device__ void mma_piece(const Ctx& cx, const Piece& pc, int gj0, uint32_t tmem,
+                          uint8_t* smem) {
+  const uint32_t qbase = tc::smem_u32(smem);
+  for (int jt = 0; jt < pc.n_tiles; ++jt) {
+    const int gj = gj0 + jt, st = gj % kStages;
+    wait_bar(cx, &cx.bars->kv_full[st], (gj / kStages) & 1);
+    if (gj >= 2) wait_bar(cx, &cx.bars->s_free[gj & 1], ((gj >> 1) - 1) & 1);
+    tc::fence_after();
+    const uint32_t kbase = tc::smem_u32(smem + kOffKV + st * kStageBytes);
+    const uint32_t d = tmem + kColS + (gj & 1) * kT;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint64_t ad = tc::desc_sw128(qbase + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+      const uint64_t bd = tc::desc_sw128(kbase + (k >> 2) * (kT * 128) + (k & 3) * 32, 16, 1024);
+      tc::mma_bf16(d, ad, bd, kIdescQK, k > 0 ? 1u : 0u);
+    }
+    tc::commit(tc::smem_u32(&cx.bars->s_full[gj & 1]));
+    if (jt > 0) issue_pv(cx, gj - 1, jt == 1, tmem, smem);
+  }
+  issue_pv(cx, gj0 + pc.n_tiles - 1, pc.n_tiles == 1, tmem, smem);
+}
+
+// ---- warps 2..5: softmax and epilogue ----------------------------------------
+__device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
+                              uint32_t tmem, uint8_t* smem, const int* s_pre,
+                              long long U, int P, int c) {
+  const AttnParams& p = *cx.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w4 = warp & 3, pos = 32 * w4 + lane;
+  const int R = (p.rows + 3) >> 2;
+  const int r = w4 * R + lane;
+  const bool valid = lane < R && r < p.rows;
+  const int i = valid ? r / p.group : 0;
+  const int lim = pc.len - p.q_len + i + 1;
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
+  uint8_t* phi = smem + kOffPhi + pos * 128;
+  uint8_t* plo = smem + kOffPlo + pos * 128;
+  const float sl2 = p.scale_log2;
+
+  float m = -INFINITY, l = 0.f;
+  for (int jt = 0; jt < pc.n_tiles; ++jt) {
+    const int gj = gj0 + jt;
+    wait_bar(cx, &cx.bars->s_full[gj & 1], (gj >> 1) & 1);
+    tc::fence_after();
+    float s[kT];
+    tc::tmem_ld32(lane_base + kColS + (gj & 1) * kT, s);
+    tc::fence_before();
+    __syncwarp();
+    if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->s_free[gj & 1]));
+
+    const int t0 = pc.tok_begin + jt * kT;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kT; ++k) {
+      const float x = (t0 + k < lim) ? s[k] * sl2 : -INFINITY;
+      s[k] = x;
+      mx = fmaxf(mx, x);
+    }
+    bool need = false;
+    float alpha = 1.f;
+    if (jt == 0) {
+      m = mx;
+    } else if (m != -INFINITY) {
+      const float mn = fmaxf(m, mx);
+      if (mn > m + kRescaleLog2) {
+        need = true;
+        alpha = exp2f(m - mn);
+        m = mn;
+      }
+    }
+    bool waited_prev = false;
+    if (__any_sync(0xffffffffu, need)) {
+      // O must be final for tile gj-1 before it is rescaled
+      wait_bar(cx, &cx.bars->pv_done[(gj - 1) & 1], ((gj - 1) >> 1) & 1);
+      tc::fence_after();
+      waited_prev = true;
+#pragma unroll 1
+      for (int cb = 0; cb < 8; ++cb) {
+        float o[32];
+        tc::tmem_ld32(lane_base + cb * 32, o);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) o[k] *= alpha;
+        tc::tmem_st32(lane_base + cb * 32, o);
+      }
+      tc::tmem_wait_st();
+      l *= alpha;
+    }
+    const float mu = m == -INFINITY ? 0.f : m;
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < kT; ++k) {
+      s[k] = exp2f(s[k] - mu);
+      sum += s[k];
+    }
+    l += sum;
+    // the P half this tile writes was last read by PV of tile gj-2
+    if (!waited_prev && gj >= 2)
+      wait_bar(cx, &cx.bars->pv_done[gj & 1], ((gj >> 1) - 1) & 1);
+    // V rows past the piece's last token must be zero (0 * NaN poisons PV)
+    if (t0 + kT > pc.tok_end) {
+      const int st = gj % kStages;
+      wait_bar(cx, &cx.bars->kv_full[st], (gj / kStages) & 1);
+      uint8_t* v = smem + kOffKV + st * kStageBytes + kHalfBytes;
+      const int z0 = pc.tok_end - t0;
+      const int n = (kT - z0) * 4 * 8;  // rows x column blocks x chunks
+      for (int e = threadIdx.x - 64; e < n; e += 128) {
+        const int row = z0 + e / 32, rem = e % 32, cb = rem >> 3, ch = rem & 7;
+        *reinterpret_cast<uint4*>(v + cb * (kT * 128) + row * 128 + (ch << 4)) =
+            make_uint4(0, 0, 0, 0);
+      }
+    }
+    // P_j = hi + lo, 32 tokens = 4 chunks of 8 in half (gj & 1) of the row
+    const int h = gj & 1;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x0 = s[8 * k + 2 * e], x1 = s[8 * k + 2 * e + 1];
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
+        const __nv_bfloat162 ll = __floats2bfloat162_rn(
+            x0 - __low2float(hh), x1 - __high2float(hh));
+        hi[e] = *reinterpret_cast<const uint32_t*>(&hh);
+        lo[e] = *reinterpret_cast<const uint32_t*>(&ll);
+      }
+      const int chunk = (4 * h + k) ^ (pos & 7);
+      *reinterpret_cast<uint4*>(phi + (chunk << 4)) =
+          make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(plo + (chunk << 4)) =
+          make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before();
+    __syncwarp();
+    if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->p_full[gj & 1]));
+  }
+
+  // epilogue: O / l
+  const int gl = gj0 + pc.n_tiles - 1;
+  wait_bar(cx, &cx.bars->pv_done[gl & 1], (gl >> 1) & 1);
+  tc::fence_after();
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float mu = m == -INFINITY ? 0.f : m;
+  const int S = seg_splits(pc.s0, pc.nt, U, P);
+  const int head = pc.g * p.group + (r - i * p.group);
+  if (S == 1) {
+    __nv_bfloat16* dst =
+        p.out + (((long long)pc.b * p.q_len + i) * p.hq + head) * kHeadDim;
+#pragma unroll 1
+    for (int cb = 0; cb < 8; ++cb) {
+      float o[32];
+      tc::tmem_ld32(lane_base + cb * 32, o);
+      if (valid) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 v;
+          __nv_bfloat162 t;
+          t = __floats2bfloat162_rn(o[8 * k] * inv, o[8 * k + 1] * inv);
+          v.x = *reinterpret_cast<uint32_t*>(&t);
+          t = __floats2bfloat162_rn(o[8 * k + 2] * inv, o[8 * k + 3] * inv);
+          v.y = *reinterpret_cast<uint32_t*>(&t);
+          t = __floats2bfloat162_rn(o[8 * k + 4] * inv, o[8 * k + 5] * inv);
+          v.z = *reinterpret_cast<uint32_t*>(&t);
+          t = __floats2bfloat162_rn(o[8 * k + 6] * inv, o[8 * k + 7] * inv);
+          v.w = *reinterpret_cast<uint32_t*>(&t);
+          *reinterpret_cast<uint4*>(dst + cb * 32 + 8 * k) = v;
+        }
+      }
+    }
+  } else {
+    const int k = pc.b * p.hkv + pc.g;
+    const int slot = slot_base_warp(p, s_pre, k, U, P) + (c - cta_of(pc.s0, U, P));
+    float* dst = p.part_o + ((long long)slot * p.rows + r) * kHeadDim;
+#pragma unroll 1
+    for (int cb = 0; cb < 8; ++cb) {
+      float o[32];
+      tc::tmem_ld32(lane_base + cb * 32, o);
+      if (valid) {
+#pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4)
+          *reinterpret_cast<float4*>(dst + cb * 32 + 4 * k4) =
+              make_float4(o[4 * k4] * inv, o[4 * k4 + 1] * inv,
+                          o[4 * k4 + 2] * inv, o[4 * k4 + 3] * inv);
+      }
+    }
+    if (valid)
+      p.part_lse[(long long)slot * p.rows + r] =
+          l > 0.f ? mu + log2f(l) : -INFINITY;
+  }
+}
+
+// Softmax threads write their Q row of piece (b, g) into the swizzled tile.
+__device__ __forceinline__ void load_q_row(const AttnParams& p, const Piece& pc,
+                                           uint8_t* q_s) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w4 = warp & 3, pos = 32 * w4 + lane;
+  const int R = (p.rows + 3) >> 2;
+  const int r = w4 * R + lane;
+  if (!(lane < R && r < p.rows)) return;
+  const int i = r / p.group, h = pc.g * p.group + (r - i * p.group);
+  const uint4* src = reinterpret_cast<const uint4*>(
+      p.q + (((long long)pc.b * p.q_len + i) * p.hq + h) * kHeadDim);
+#pragma unroll 8
+  for (int cidx = 0; cidx < 32; ++cidx) {
+    const uint4 v = __ldg(src + cidx);
+    const int blk = cidx >> 3, ch = cidx & 7;
+    *reinterpret_cast<uint4*>(q_s + blk * 16384 + pos * 128 +
+                              ((ch ^ (pos & 7)) << 4)) = v;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    verify_split_tc_kernel(const AttnParams p,
+                           const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  int* s_pre = reinterpret_cast<int*>(smem + kOffPre);
+  __shared__ __align__(8) Bars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  plan_prefix(p, s_pre);
+  const long long U = (long long)p.hkv * s_pre[p.batch];
+  const int P = effective_grid(p.grid, U);
+  const int c = blockIdx.x;
+  if (c >= P) return;  // uniform over the CTA, before any TMEM or barrier use
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::bar_init(tc::smem_u32(&bars.kv_full[s]), 1);
+      tc::bar_init(tc::smem_u32(&bars.kv_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::bar_init(tc::smem_u32(&bars.s_full[s]), 1);
+      tc::bar_init(tc::smem_u32(&bars.s_free[s]), 4);
+      tc::bar_init(tc::smem_u32(&bars.p_full[s]), 4);
+      tc::bar_init(tc::smem_u32(&bars.pv_done[s]), 1);
+    }
+    tc::bar_init(tc::smem_u32(&bars.drain), 1);
+    s_abort = 0;
+    tc::bar_fence_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&s_tmem), kTmemCols);
+  if (warp >= 2) {  // zero every Q row once; valid rows are rewritten per piece
+    const int pos = 32 * (warp & 3) + lane;
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(smem + blk * 16384 + pos * 128 + ch * 16) =
+            make_uint4(0, 0, 0, 0);
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = s_tmem;
+  Ctx cx{&bars, &s_abort, &p};
+
+  long long u = cta_start(c, U, P);
+  const long long u_end = cta_start(c + 1, U, P);
+  int gj0 = 0;
+  int last_loaded = -1;  // last tile index the producer loaded
+  while (u < u_end) {
+    Piece pc;
+    pc.b = find_request(s_pre, p.batch, p.hkv, u);
+    pc.nt = s_pre[pc.b + 1] - s_pre[pc.b];
+    const long long rb = (long long)p.hkv * s_pre[pc.b];
+    pc.g = (int)((u - rb) / pc.nt);
+    pc.s0 = rb + (long long)pc.g * pc.nt;
+    const int j0 = (int)(u - pc.s0);
+    const int j1 = (int)(u_end - pc.s0 < pc.nt ? u_end - pc.s0 : pc.nt);
+    u = pc.s0 + j1;
+    pc.len = clamp_len(p.seq_lens[pc.b], p.max_tokens);
+    pc.tok_begin = j0 * kUnit;
+    pc.tok_end = min(j1 * kUnit, pc.len);
+    pc.n_tiles = (pc.tok_end - pc.tok_begin + kT - 1) / kT;
+
+    if (warp >= 2) {
+      load_q_row(p, pc, smem);
+      tc::fence_proxy_async_smem();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) {
+      if (lane == 0) produce(cx, pc, gj0, smem + kOffKV, &tm_k, &tm_v);
+      last_loaded = gj0 + pc.n_tiles - 1;
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0) mma_piece(cx, pc, gj0, tmem, smem);
+      __syncwarp();
+    } else {
+      softmax_piece(cx, pc, gj0, tmem, smem, s_pre, U, P, c);
+    }
+    gj0 += pc.n_tiles;
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+  }
+
+  // teardown: no TMA copy or MMA may still be in flight
+  if (warp == 0 && lane == 0) {
+    for (int gj = max(0, last_loaded - kStages + 1); gj <= last_loaded; ++gj)
+      wait_bar(cx, &bars.kv_full[gj % kStages], (gj / kStages) & 1, true);
+  }
+  if (warp == 1 && lane == 0) {
+    tc::commit(tc::smem_u32(&bars.drain));
+    wait_bar(cx, &bars.drain, 0, true);
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_verify_split_tc(const AttnParams& p, const CUtensorMap& tm_k,
+                                   const CUtensorMap& tm_v, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(
+      verify_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      kSmemBytes);
+  if (e != cudaSuccess) return e;
+  verify_split_tc_kernel<<<p.grid, kThreads, kSmemBytes, s>>>(p, tm_k, tm_v);
+  return cudaGetLastError();
+}
+
+int verify_split_tc_ctas_per_sm() {
+  if (cudaFuncSetAttribute(verify_split_tc_kernel,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &n, verify_split_tc_kernel, kThreads, kSmemBytes) != cudaSuccess)
+    return 0;
+  return n < 1 ? 0 : 1;  // TMEM: one 512-column allocation per SM
+}
+
+int verify_split_tc_box_rows(int page_size) { return page_size < kT ? page_size : kT; }
+
+}  // namespace specv
