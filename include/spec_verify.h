@@ -124,7 +124,7 @@ size_t spec_verify_workspace_size(const spec_attn_desc* desc);
  *   seq_lens  int32 [B]: cached tokens of each request INCLUDING the
  *             block; values are clamped to [0, max_pages_per_seq*page_size].
  *             A row whose causal window is empty outputs zeros.
- *   scale     softmax scale (1/sqrt(D) for the pages' model), finite
+ *   scale     softmax scale (1/sqrt(D) for the pages' model), finite, > 0
  *   out       bf16 [B, q_len, Hq, D], 16-byte aligned
  *   workspace device scratch of >= spec_verify_workspace_size(desc) bytes,
  *             256-byte aligned; contents need no initialisation

@@ -214,8 +214,8 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
   if (desc->batch == 0) return SPEC_OK;
   if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !out)
     return fail(SPEC_ERR_ARG, "NULL tensor pointer");
-  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
-    return fail(SPEC_ERR_ARG, "scale is not finite");
+  if (!(scale > 0.f) || scale > 3.0e38f)
+    return fail(SPEC_ERR_ARG, "scale must be finite and > 0");
   if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
       !aligned(out, 16))
     return fail(SPEC_ERR_ALIGN, "q, k_pages, v_pages and out must be 16-byte aligned");

@@ -11,10 +11,10 @@
 // quarters; the other lanes carry zero rows.
 //
 // Warp roles (192 threads):
-//   warp 0      TMA producer: gathers each 32-token K and V tile of the
-//               piece page by page from the pool (one 2-D box of 64 channels
-//               x min(page_size, 32) tokens per column block) into a 3-stage
-//               ring.
+//   warp 0      TMA producer (all 32 lanes): gathers each 32-token K and V
+//               tile of the piece page by page from the pool (one 2-D box of
+//               64 channels x min(page_size, 32) tokens per column block,
+//               lane i issuing box i) into a 3-stage ring.
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
 //               S buffers, then O += P_{j-1} V_{j-1} into the TMEM O
 //               accumulator, so the softmax of tile j overlaps the MMAs.
@@ -75,21 +75,27 @@ struct Ctx {
 
 // Bounded wait on phase `parity` of an mbarrier.  Returns false (and flags
 // the CTA) when the bound runs out or another wait of the CTA already did.
-__device__ __noinline__ bool wait_bar(const Ctx& cx, uint64_t* bar,
-                                      uint32_t parity, bool ignore_abort = false) {
-  const uint32_t a = tc::smem_u32(bar);
-  if (tc::bar_try_wait(a, parity)) return true;
-  if (!ignore_abort && *cx.abort) return false;
+__device__ __noinline__ bool wait_slow(uint32_t a, uint32_t parity,
+                                       volatile int* abort, uint32_t* status,
+                                       bool ignore_abort) {
+  if (!ignore_abort && *abort) return false;
   const long long t0 = clock64();
   while (true) {
     if (tc::bar_try_wait(a, parity)) return true;
-    if (!ignore_abort && *cx.abort) return false;
+    if (!ignore_abort && *abort) return false;
     if (clock64() - t0 > kWaitCycles) {
-      *cx.abort = 1;
-      if (cx.p->status) atomicOr(cx.p->status, SPEC_STATUS_TIMEOUT);
+      *abort = 1;
+      if (status) atomicOr(status, SPEC_STATUS_TIMEOUT);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool wait_bar(const Ctx& cx, uint64_t* bar,
+                                         uint32_t parity,
+                                         bool ignore_abort = false) {
+  const uint32_t a = tc::smem_u32(bar);
+  if (tc::bar_try_wait(a, parity)) return true;
+  return wait_slow(a, parity, cx.abort, cx.p->status, ignore_abort);
 }
 
 struct Piece {
@@ -102,12 +108,31 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
       (reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
-// ---- warp 0, one thread: TMA loads of the piece's K/V tiles ---------------
+// ---- warp 0: TMA loads of the piece's K/V tiles ----------------------------
+// Lane i owns box i of a tile (a run of min(page_size, 32) tokens of one
+// page); its page id for the next tile is loaded while the current tile
+// waits for a free stage, so the page-table latency stays off the pipeline.
+__device__ __forceinline__ int box_page(const AttnParams& p, const Piece& pc,
+                                        int jt, int lane) {
+  const int t = pc.tok_begin + jt * kT + lane * p.box_rows;
+  if (jt >= pc.n_tiles || t >= pc.tok_end || lane * p.box_rows >= kT) return 0;
+  int page = __ldg(p.page_table + (long long)pc.b * p.max_pages +
+                   (t >> p.log2_ps));
+  if (page < 0 || page >= p.num_pages) {
+    if (p.status) atomicOr(p.status, SPEC_STATUS_BAD_PAGE);
+    page = 0;  // in bounds; the affected rows are unspecified
+  }
+  return page;
+}
+
 __device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* kv,
                         const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
   const AttnParams& p = *cx.p;
+  const int lane = threadIdx.x & 31;
   const int rpb = p.box_rows;
+  int page = box_page(p, pc, 0, lane);
   for (int jt = 0; jt < pc.n_tiles; ++jt) {
+    const int next_page = box_page(p, pc, jt + 1, lane);
     const int gj = gj0 + jt, st = gj % kStages;
     if (gj >= kStages)
       wait_bar(cx, &cx.bars->kv_empty[st], ((gj / kStages) - 1) & 1);
@@ -115,33 +140,45 @@ __device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* kv,
     const int ntok = min(kT, pc.tok_end - t0);
     const int nbox = (ntok + rpb - 1) / rpb;
     const uint32_t full = tc::smem_u32(&cx.bars->kv_full[st]);
-    tc::bar_arrive_expect_tx(full, (uint32_t)(nbox * rpb * 128 * 4 * 2));
-    const uint32_t kdst = tc::smem_u32(kv + st * kStageBytes);
-    const uint32_t vdst = kdst + kHalfBytes;
-    for (int i = 0; i < nbox; ++i) {
-      const int t = t0 + i * rpb;
-      int page = __ldg(p.page_table + (long long)pc.b * p.max_pages +
-                       (t >> p.log2_ps));
-      if (page < 0 || page >= p.num_pages) {
-        if (p.status) atomicOr(p.status, SPEC_STATUS_BAD_PAGE);
-        page = 0;  // in bounds; the affected rows are unspecified
-      }
+    if (lane == 0)
+      tc::bar_arrive_expect_tx(full, (uint32_t)(nbox * rpb * 128 * 4 * 2));
+    __syncwarp();
+    if (lane < nbox) {
+      const uint32_t kdst = tc::smem_u32(kv + st * kStageBytes);
+      const uint32_t vdst = kdst + kHalfBytes;
+      const int t = t0 + lane * rpb;
       const int y = ((page * p.hkv + pc.g) << p.log2_ps) + (t & (p.page_size - 1));
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
-        const uint32_t off = cb * (kT * 128) + i * rpb * 128;
+        const uint32_t off = cb * (kT * 128) + lane * rpb * 128;
         tc::tma_load_2d(kdst + off, tm_k, full, cb * 64, y);
         tc::tma_load_2d(vdst + off, tm_v, full, cb * 64, y);
       }
     }
+    page = next_page;
   }
 }
 
 // ---- warp 1, one thread: MMA issue -------------------------------------------
+// S_j = Q K_j^T and O += P_j V_j are issued as soon as their inputs are
+// ready, whichever comes first: a PV never waits behind the next tile's TMA.
+__device__ __forceinline__ void issue_qk(const Ctx& cx, int gj, uint32_t tmem,
+                                         uint8_t* smem) {
+  const int st = gj % kStages;
+  const uint32_t qbase = tc::smem_u32(smem);
+  const uint32_t kbase = tc::smem_u32(smem + kOffKV + st * kStageBytes);
+  const uint32_t d = tmem + kColS + (gj & 1) * kT;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint64_t ad = tc::desc_sw128(qbase + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+    const uint64_t bd = tc::desc_sw128(kbase + (k >> 2) * (kT * 128) + (k & 3) * 32, 16, 1024);
+    tc::mma_bf16(d, ad, bd, kIdescQK, k > 0 ? 1u : 0u);
+  }
+  tc::commit(tc::smem_u32(&cx.bars->s_full[gj & 1]));
+}
+
 __device__ __forceinline__ void issue_pv(const Ctx& cx, int gj, bool first,
                                          uint32_t tmem, uint8_t* smem) {
-  wait_bar(cx, &cx.bars->p_full[gj & 1], (gj >> 1) & 1);
-  tc::fence_after();
   const int st = gj % kStages, h = gj & 1;
   const uint32_t vbase = tc::smem_u32(smem + kOffKV + st * kStageBytes) + kHalfBytes;
   const uint32_t phi = tc::smem_u32(smem + kOffPhi) + h * 64;
@@ -159,24 +196,42 @@ __device__ __forceinline__ void issue_pv(const Ctx& cx, int gj, bool first,
 
 __device__ void mma_piece(const Ctx& cx, const Piece& pc, int gj0, uint32_t tmem,
                           uint8_t* smem) {
-  const uint32_t qbase = tc::smem_u32(smem);
-  for (int jt = 0; jt < pc.n_tiles; ++jt) {
-    const int gj = gj0 + jt, st = gj % kStages;
-    wait_bar(cx, &cx.bars->kv_full[st], (gj / kStages) & 1);
-    if (gj >= 2) wait_bar(cx, &cx.bars->s_free[gj & 1], ((gj >> 1) - 1) & 1);
-    tc::fence_after();
-    const uint32_t kbase = tc::smem_u32(smem + kOffKV + st * kStageBytes);
-    const uint32_t d = tmem + kColS + (gj & 1) * kT;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const uint64_t ad = tc::desc_sw128(qbase + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-      const uint64_t bd = tc::desc_sw128(kbase + (k >> 2) * (kT * 128) + (k & 3) * 32, 16, 1024);
-      tc::mma_bf16(d, ad, bd, kIdescQK, k > 0 ? 1u : 0u);
+  int qk = 0, pv = 0;
+  long long last = clock64();
+  while (pv < pc.n_tiles) {
+    bool did = false;
+    if (qk < pc.n_tiles) {
+      const int gj = gj0 + qk;
+      if (tc::bar_try_wait(tc::smem_u32(&cx.bars->kv_full[gj % kStages]),
+                           (gj / kStages) & 1) &&
+          (gj < 2 || tc::bar_try_wait(tc::smem_u32(&cx.bars->s_free[gj & 1]),
+                                      ((gj >> 1) - 1) & 1))) {
+        tc::fence_after();
+        issue_qk(cx, gj, tmem, smem);
+        ++qk;
+        did = true;
+      }
     }
-    tc::commit(tc::smem_u32(&cx.bars->s_full[gj & 1]));
-    if (jt > 0) issue_pv(cx, gj - 1, jt == 1, tmem, smem);
+    if (pv < qk) {
+      const int gj = gj0 + pv;
+      if (tc::bar_try_wait(tc::smem_u32(&cx.bars->p_full[gj & 1]),
+                           (gj >> 1) & 1)) {
+        tc::fence_after();
+        issue_pv(cx, gj, pv == 0, tmem, smem);
+        ++pv;
+        did = true;
+      }
+    }
+    if (did) {
+      last = clock64();
+    } else if (*cx.abort) {
+      break;
+    } else if (clock64() - last > kWaitCycles) {
+      *cx.abort = 1;
+      if (cx.p->status) atomicOr(cx.p->status, SPEC_STATUS_TIMEOUT);
+      break;
+    }
   }
-  issue_pv(cx, gj0 + pc.n_tiles - 1, pc.n_tiles == 1, tmem, smem);
 }
 
 // ---- warps 2..5: softmax and epilogue ----------------------------------------
@@ -208,13 +263,16 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
     if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->s_free[gj & 1]));
 
     const int t0 = pc.tok_begin + jt * kT;
-    float mx = -INFINITY;
+    if (t0 + kT > lim) {  // the causal tail of the block reaches this tile
 #pragma unroll
-    for (int k = 0; k < kT; ++k) {
-      const float x = (t0 + k < lim) ? s[k] * sl2 : -INFINITY;
-      s[k] = x;
-      mx = fmaxf(mx, x);
+      for (int k = 0; k < kT; ++k)
+        if (t0 + k >= lim) s[k] = -INFINITY;
     }
+    float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+    for (int k = 4; k < kT; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], s[k]);
+    // scale > 0, so the max of the raw scores gives the max of the scaled
+    float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
     bool need = false;
     float alpha = 1.f;
     if (jt == 0) {
@@ -245,13 +303,13 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
       l *= alpha;
     }
     const float mu = m == -INFINITY ? 0.f : m;
-    float sum = 0.f;
+    float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < kT; ++k) {
-      s[k] = exp2f(s[k] - mu);
-      sum += s[k];
+      s[k] = exp2f(fmaf(s[k], sl2, -mu));
+      sum4[k & 3] += s[k];
     }
-    l += sum;
+    l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
     // the P half this tile writes was last read by PV of tile gj-2
     if (!waited_prev && gj >= 2)
       wait_bar(cx, &cx.bars->pv_done[gj & 1], ((gj >> 1) - 1) & 1);
@@ -444,7 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after();
     if (warp == 0) {
-      if (lane == 0) produce(cx, pc, gj0, smem + kOffKV, &tm_k, &tm_v);
+      // the whole warp: lanes issue the boxes of their pages
+      produce(cx, pc, gj0, smem + kOffKV, &tm_k, &tm_v);
       last_loaded = gj0 + pc.n_tiles - 1;
       __syncwarp();
     } else if (warp == 1) {

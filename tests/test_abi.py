@@ -86,6 +86,8 @@ def test_null_and_misaligned_pointers_rejected(lib):
         _native.SPEC_ERR_ALIGN
     assert _attn(lib, _desc(), scale=float("nan")) == _native.SPEC_ERR_ARG
     assert _attn(lib, _desc(), scale=float("inf")) == _native.SPEC_ERR_ARG
+    assert _attn(lib, _desc(), scale=0.0) == _native.SPEC_ERR_ARG
+    assert _attn(lib, _desc(), scale=-0.5) == _native.SPEC_ERR_ARG
     fp8 = _desc(kv_dtype="fp8")
     assert _attn(lib, fp8) == _native.SPEC_ERR_ARG          # scales missing
 
