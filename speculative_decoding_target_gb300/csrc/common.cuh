@@ -45,7 +45,7 @@ struct AttnParams {
   int page_size, log2_ps, num_pages, max_pages;
   int max_tokens;     // max_pages * page_size: seq_lens clamp
   int grid;           // P: CTAs of the split kernel
-  int box_rows;       // TMA box height (tcgen05 kernel): min(page_size, 32)
+  int box_rows;       // TMA box height (tcgen05 kernel): min(page_size, 64)
   float scale_log2;   // softmax scale * log2(e)
 };
 

@@ -11,20 +11,25 @@
 // quarters; the other lanes carry zero rows.
 //
 // Warp roles (192 threads):
-//   warp 0      TMA producer (all 32 lanes): gathers each 32-token K and V
+//   warp 0      TMA producer (all 32 lanes): gathers each 64-token K and V
 //               tile of the piece page by page from the pool (one 2-D box of
-//               64 channels x min(page_size, 32) tokens per column block,
-//               lane i issuing box i) into a 3-stage ring.
+//               64 channels x min(page_size, 64) tokens per column block,
+//               lane i issuing box i) into a 2-stage ring.
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//               S buffers, then O += P_{j-1} V_{j-1} into the TMEM O
-//               accumulator, so the softmax of tile j overlaps the MMAs.
+//               S buffers and O += P_j V_j into the TMEM O accumulator, each
+//               issued as soon as its inputs are ready.
 //   warps 2..5  softmax: one thread per TMEM lane (query row).  Load S_j,
 //               mask the block's causal tail, keep a running max m and sum l
-//               in base 2, write P_j = 2^(s - m) to shared memory as bf16
-//               hi + lo parts (P V is issued twice, so the bf16 rounding of
-//               P does not reach the output), rescale O in TMEM only when the
-//               running max grows by more than 2^8, and finally read O,
-//               divide by l and write the bf16 output or an fp32 partial.
+//               in base 2, and write P_j = 2^(s - m) back over S_j as bf16
+//               hi + lo parts (the PV MMA takes P from TMEM and runs once per
+//               part, so the bf16 rounding of P does not reach the output);
+//               rescale O in TMEM only when the running max grows by more
+//               than 2^8; finally read O, divide by l and write the bf16
+//               output or an fp32 partial.
+//
+// The tile width is set by the MMA issue rate: QK^T costs 16 instructions
+// per tile whatever its width, so 64-token tiles halve the instructions per
+// KV byte of 32-token tiles.
 //
 // Every wait is bounded (about two seconds of clock); a wait that runs out
 // sets SPEC_STATUS_TIMEOUT in the status word (checked mode) and makes every
@@ -36,21 +41,18 @@
 namespace specv {
 namespace {
 
-constexpr int kT = 32;                        // tokens per tile
-constexpr int kStages = 3;
+constexpr int kT = 64;                        // tokens per tile
+constexpr int kStages = 2;
 constexpr int kThreads = 192;
 constexpr int kQBytes = 4 * 128 * 128;        // Q: 4 column blocks x 128 rows
 constexpr int kHalfBytes = 4 * kT * 128;      // K (or V) of one stage
 constexpr int kStageBytes = 2 * kHalfBytes;
-constexpr int kPBytes = 128 * 128;            // P hi (or lo): 128 rows x 128 B
 constexpr int kOffKV = kQBytes;
-constexpr int kOffPhi = kOffKV + kStages * kStageBytes;
-constexpr int kOffPlo = kOffPhi + kPBytes;
-constexpr int kOffPre = kOffPlo + kPBytes;
+constexpr int kOffPre = kOffKV + kStages * kStageBytes;
 constexpr int kPreBytes = ((kMaxBatch + 1) * 4 + 127) / 128 * 128;
 constexpr int kSmemBytes = kOffPre + kPreBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 256;               // S buffers: columns 256, 288
+constexpr uint32_t kColS = 256;               // S/P buffers: columns 256, 320
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr float kRescaleLog2 = 8.0f;          // rescale O when m grows > 2^8
 
@@ -61,7 +63,6 @@ struct Bars {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
-  uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t drain;
@@ -109,7 +110,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 // ---- warp 0: TMA loads of the piece's K/V tiles ----------------------------
-// Lane i owns box i of a tile (a run of min(page_size, 32) tokens of one
+// Lane i owns box i of a tile (a run of min(page_size, 64) tokens of one
 // page); its page id for the next tile is loaded while the current tile
 // waits for a free stage, so the page-table latency stays off the pipeline.
 __device__ __forceinline__ int box_page(const AttnParams& p, const Piece& pc,
@@ -179,16 +180,16 @@ __device__ __forceinline__ void issue_qk(const Ctx& cx, int gj, uint32_t tmem,
 
 __device__ __forceinline__ void issue_pv(const Ctx& cx, int gj, bool first,
                                          uint32_t tmem, uint8_t* smem) {
-  const int st = gj % kStages, h = gj & 1;
+  const int st = gj % kStages;
   const uint32_t vbase = tc::smem_u32(smem + kOffKV + st * kStageBytes) + kHalfBytes;
-  const uint32_t phi = tc::smem_u32(smem + kOffPhi) + h * 64;
-  const uint32_t plo = tc::smem_u32(smem + kOffPlo) + h * 64;
+  const uint32_t p_hi = tmem + kColS + (gj & 1) * kT;  // 32 columns: bf16 pairs
+  const uint32_t p_lo = p_hi + kT / 2;
 #pragma unroll
-  for (int kk = 0; kk < 2; ++kk) {
+  for (int kk = 0; kk < kT / 16; ++kk) {
     const uint64_t bd = tc::desc_sw128(vbase + kk * 2048, kT * 128, 1024);
-    tc::mma_bf16(tmem, tc::desc_sw128(phi + kk * 32, 16, 1024), bd, kIdescPV,
-                 (first && kk == 0) ? 0u : 1u);
-    tc::mma_bf16(tmem, tc::desc_sw128(plo + kk * 32, 16, 1024), bd, kIdescPV, 1u);
+    tc::mma_bf16_ta(tmem, p_hi + kk * 8, bd, kIdescPV,
+                    (first && kk == 0) ? 0u : 1u);
+    tc::mma_bf16_ta(tmem, p_lo + kk * 8, bd, kIdescPV, 1u);
   }
   tc::commit(tc::smem_u32(&cx.bars->kv_empty[st]));
   tc::commit(tc::smem_u32(&cx.bars->pv_done[gj & 1]));
@@ -204,7 +205,7 @@ __device__ void mma_piece(const Ctx& cx, const Piece& pc, int gj0, uint32_t tmem
       const int gj = gj0 + qk;
       if (tc::bar_try_wait(tc::smem_u32(&cx.bars->kv_full[gj % kStages]),
                            (gj / kStages) & 1) &&
-          (gj < 2 || tc::bar_try_wait(tc::smem_u32(&cx.bars->s_free[gj & 1]),
+          (gj < 2 || tc::bar_try_wait(tc::smem_u32(&cx.bars->pv_done[gj & 1]),
                                       ((gj >> 1) - 1) & 1))) {
         tc::fence_after();
         issue_qk(cx, gj, tmem, smem);
@@ -247,20 +248,17 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
   const int i = valid ? r / p.group : 0;
   const int lim = pc.len - p.q_len + i + 1;
   const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
-  uint8_t* phi = smem + kOffPhi + pos * 128;
-  uint8_t* plo = smem + kOffPlo + pos * 128;
   const float sl2 = p.scale_log2;
 
   float m = -INFINITY, l = 0.f;
   for (int jt = 0; jt < pc.n_tiles; ++jt) {
     const int gj = gj0 + jt;
+    const uint32_t sbuf = lane_base + kColS + (gj & 1) * kT;
     wait_bar(cx, &cx.bars->s_full[gj & 1], (gj >> 1) & 1);
     tc::fence_after();
     float s[kT];
-    tc::tmem_ld32(lane_base + kColS + (gj & 1) * kT, s);
-    tc::fence_before();
-    __syncwarp();
-    if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->s_free[gj & 1]));
+    tc::tmem_ld32(sbuf, s);
+    tc::tmem_ld32(sbuf + 32, s + 32);
 
     const int t0 = pc.tok_begin + jt * kT;
     if (t0 + kT > lim) {  // the causal tail of the block reaches this tile
@@ -272,7 +270,7 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
 #pragma unroll
     for (int k = 4; k < kT; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], s[k]);
     // scale > 0, so the max of the raw scores gives the max of the scaled
-    float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
     bool need = false;
     float alpha = 1.f;
     if (jt == 0) {
@@ -285,12 +283,10 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
         m = mn;
       }
     }
-    bool waited_prev = false;
     if (__any_sync(0xffffffffu, need)) {
       // O must be final for tile gj-1 before it is rescaled
       wait_bar(cx, &cx.bars->pv_done[(gj - 1) & 1], ((gj - 1) >> 1) & 1);
       tc::fence_after();
-      waited_prev = true;
 #pragma unroll 1
       for (int cb = 0; cb < 8; ++cb) {
         float o[32];
@@ -304,15 +300,20 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
     }
     const float mu = m == -INFINITY ? 0.f : m;
     float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t hi[kT / 2], lo[kT / 2];
 #pragma unroll
-    for (int k = 0; k < kT; ++k) {
-      s[k] = exp2f(fmaf(s[k], sl2, -mu));
-      sum4[k & 3] += s[k];
+    for (int k = 0; k < kT; k += 2) {
+      const float x0 = exp2f(fmaf(s[k], sl2, -mu));
+      const float x1 = exp2f(fmaf(s[k + 1], sl2, -mu));
+      sum4[k & 3] += x0;
+      sum4[(k & 3) + 1] += x1;
+      const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
+      const __nv_bfloat162 ll =
+          __floats2bfloat162_rn(x0 - __low2float(hh), x1 - __high2float(hh));
+      hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
+      lo[k >> 1] = *reinterpret_cast<const uint32_t*>(&ll);
     }
     l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-    // the P half this tile writes was last read by PV of tile gj-2
-    if (!waited_prev && gj >= 2)
-      wait_bar(cx, &cx.bars->pv_done[gj & 1], ((gj >> 1) - 1) & 1);
     // V rows past the piece's last token must be zero (0 * NaN poisons PV)
     if (t0 + kT > pc.tok_end) {
       const int st = gj % kStages;
@@ -325,28 +326,12 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
         *reinterpret_cast<uint4*>(v + cb * (kT * 128) + row * 128 + (ch << 4)) =
             make_uint4(0, 0, 0, 0);
       }
+      tc::fence_proxy_async_smem();
     }
-    // P_j = hi + lo, 32 tokens = 4 chunks of 8 in half (gj & 1) of the row
-    const int h = gj & 1;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float x0 = s[8 * k + 2 * e], x1 = s[8 * k + 2 * e + 1];
-        const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
-        const __nv_bfloat162 ll = __floats2bfloat162_rn(
-            x0 - __low2float(hh), x1 - __high2float(hh));
-        hi[e] = *reinterpret_cast<const uint32_t*>(&hh);
-        lo[e] = *reinterpret_cast<const uint32_t*>(&ll);
-      }
-      const int chunk = (4 * h + k) ^ (pos & 7);
-      *reinterpret_cast<uint4*>(phi + (chunk << 4)) =
-          make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(plo + (chunk << 4)) =
-          make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    tc::fence_proxy_async_smem();
+    // P_j over S_j: hi in the first 32 columns, lo in the next 32
+    tc::tmem_st32(sbuf, reinterpret_cast<const float*>(hi));
+    tc::tmem_st32(sbuf + kT / 2, reinterpret_cast<const float*>(lo));
+    tc::tmem_wait_st();
     tc::fence_before();
     __syncwarp();
     if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->p_full[gj & 1]));
@@ -451,7 +436,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       tc::bar_init(tc::smem_u32(&bars.s_full[s]), 1);
-      tc::bar_init(tc::smem_u32(&bars.s_free[s]), 4);
       tc::bar_init(tc::smem_u32(&bars.p_full[s]), 4);
       tc::bar_init(tc::smem_u32(&bars.pv_done[s]), 1);
     }
