@@ -41,19 +41,23 @@ UNIT = "steps/s"
 DEFAULT_WORKLOAD = "b8_q8_p32k"
 KERNEL_LAUNCHES_PER_STEP = 4   # split, merge, argmax partial, accept finalize
 
-# DRAM traffic per attention call measured by ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum of the split and merge kernels), keyed by workload,
-# valid only for the kernel sources whose hash is recorded with it.
-NCU_TRAFFIC = {}
+# DRAM traffic of one launch of the dominant kernel (the tcgen05 split-KV
+# attention kernel), dram__bytes_read.sum + dram__bytes_write.sum from one
+# ncu capture (profiles/verify_split_tc_*.md), keyed by workload and valid
+# only while the kernel's sources still hash to the recorded value.
+NCU_TRAFFIC = {
+    "b8_q8_p32k": {"source_hash": "e81d89c50fb61f96",
+                   "bytes_per_launch": 1077420000 + 4863232},
+}
+SPLIT_KERNEL_SOURCES = ("verify_attention_tc.cu", "common.cuh", "tc_ptx.cuh")
 
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_target_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
+    for fn in SPLIT_KERNEL_SOURCES:
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
