@@ -118,7 +118,9 @@ size_t spec_verify_workspace_size(const spec_attn_desc* desc);
  *   k_scales, v_scales  fp16 [num_pages, Hkv, page_size, D/64] for
  *             SPEC_KV_FP8_E4M3 (element c of a cached row is
  *             e4m3(byte_c) * scale[c/64]: "Qwen3.8-27B-FP8" page,
- *             "Implemented execution path"), 8-byte aligned; NULL for bf16
+ *             "Implemented execution path"), 16-byte aligned; NULL for
+ *             bf16.  FP8 KV is computed in fp16: dequantised K/V and Q must
+ *             lie within the fp16 range (|x| <= 65504); needs page_size >= 8
  *   page_table int32 [B, max_pages_per_seq]; only the first
  *             ceil(seq_lens[b]/page_size) entries of row b are read
  *   seq_lens  int32 [B]: cached tokens of each request INCLUDING the

@@ -142,10 +142,11 @@ cudaError_t launch_verify_merge(const AttnParams& p, cudaStream_t s);
 int verify_split_bf16_ctas_per_sm(int rows);
 cudaError_t launch_verify_split_tc(const AttnParams& p, const CUtensorMap& tm_k,
                                    const CUtensorMap& tm_v, cudaStream_t s);
-int verify_split_tc_ctas_per_sm();
+int verify_split_tc_ctas_per_sm(bool fp8);
 int verify_split_tc_box_rows(int page_size);
-// The tcgen05 kernel loads whole 8-row swizzle groups with TMA, so it needs
-// pages of at least 8 tokens; smaller pages take the mma.sync kernel.
+// The tcgen05 kernel loads whole 8-row swizzle groups (and, for FP8 KV,
+// 16-byte multiples of the scales) per page run, so it needs pages of at
+// least 8 tokens; smaller bf16 pages take the mma.sync kernel.
 constexpr int kTcMinPageSize = 8;
 
 struct AcceptParams {

@@ -32,8 +32,9 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_sms[kMaxDevices];
-int g_occ[kMaxDevices][10];  // split-kernel CTAs per SM: [w] mma.sync with w
-                             // compute warps, [9] the tcgen05 kernel
+int g_occ[kMaxDevices][11];  // split-kernel CTAs per SM: [w] mma.sync with w
+                             // compute warps, [9] tcgen05 bf16, [10] tcgen05
+                             // FP8
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool use_tc(const spec_attn_desc* d) {
@@ -89,11 +90,11 @@ int current_device(int* dev) {
 
 // Split-kernel grid for `rows` query rows per KV head on the current device:
 // every SM filled with as many CTAs as fit.
-int split_grid(int rows, bool tc, int* grid) {
+int split_grid(int rows, bool tc, bool fp8, int* grid) {
   int dev;
   int rc = current_device(&dev);
   if (rc) return rc;
-  const int w = tc ? 9 : (rows + 15) / 16;
+  const int w = tc ? (fp8 ? 10 : 9) : (rows + 15) / 16;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_sms[dev]) {
     int n = 0;
@@ -104,7 +105,7 @@ int split_grid(int rows, bool tc, int* grid) {
     g_sms[dev] = n;
   }
   if (!g_occ[dev][w]) {
-    int occ = tc ? specv::verify_split_tc_ctas_per_sm()
+    int occ = tc ? specv::verify_split_tc_ctas_per_sm(fp8)
                  : specv::verify_split_bf16_ctas_per_sm(rows);
     if (occ <= 0)
       return fail(SPEC_ERR_CUDA, "split kernel does not fit on an SM");
@@ -155,6 +156,9 @@ int check_desc(const spec_attn_desc* d) {
   if ((long long)d->num_pages * d->num_kv_heads * d->page_size >= (1LL << 31))
     return fail(SPEC_ERR_UNSUPPORTED,
                 "num_pages * num_kv_heads * page_size must be < 2^31");
+  if (d->kv_dtype == SPEC_KV_FP8_E4M3 && d->page_size < specv::kTcMinPageSize)
+    return fail(SPEC_ERR_UNSUPPORTED, "FP8 KV needs page_size >= %d",
+                specv::kTcMinPageSize);
   return SPEC_OK;
 }
 
@@ -165,7 +169,8 @@ struct Layout {
 
 int layout(const spec_attn_desc* d, Layout* L) {
   L->rows = d->q_len * (d->num_q_heads / d->num_kv_heads);
-  int rc = split_grid(L->rows, use_tc(d), &L->grid);
+  int rc = split_grid(L->rows, use_tc(d), d->kv_dtype == SPEC_KV_FP8_E4M3,
+                      &L->grid);
   if (rc) return rc;
   L->nslots = L->grid + d->batch * d->num_kv_heads;
   const size_t o_bytes =
@@ -221,12 +226,12 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
     return fail(SPEC_ERR_ALIGN, "q, k_pages, v_pages and out must be 16-byte aligned");
   if (!aligned(page_table, 4) || !aligned(seq_lens, 4))
     return fail(SPEC_ERR_ALIGN, "page_table and seq_lens must be 4-byte aligned");
-  if (desc->kv_dtype == SPEC_KV_FP8_E4M3) {
+  const bool fp8 = desc->kv_dtype == SPEC_KV_FP8_E4M3;
+  if (fp8) {
     if (!k_scales || !v_scales)
       return fail(SPEC_ERR_ARG, "FP8 KV needs k_scales and v_scales");
-    if (!aligned(k_scales, 8) || !aligned(v_scales, 8))
-      return fail(SPEC_ERR_ALIGN, "scales must be 8-byte aligned");
-    return fail(SPEC_ERR_UNSUPPORTED, "FP8 KV is not built yet");
+    if (!aligned(k_scales, 16) || !aligned(v_scales, 16))
+      return fail(SPEC_ERR_ALIGN, "scales must be 16-byte aligned");
   }
   Layout L;
   rc = layout(desc, &L);
@@ -245,8 +250,8 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k_pages = k_pages;
   p.v_pages = v_pages;
-  p.k_scales = static_cast<const __half*>(k_scales);
-  p.v_scales = static_cast<const __half*>(v_scales);
+  p.k_scales = fp8 ? static_cast<const __half*>(k_scales) : nullptr;
+  p.v_scales = fp8 ? static_cast<const __half*>(v_scales) : nullptr;
   p.page_table = page_table;
   p.seq_lens = seq_lens;
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -270,7 +275,9 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
   p.scale_log2 = scale * 1.4426950408889634f;
   const bool tc = use_tc(desc);
   CUtensorMap tm_k, tm_v;
-  if (tc) {
+  std::memset(&tm_k, 0, sizeof tm_k);  // unused by the FP8 variant
+  std::memset(&tm_v, 0, sizeof tm_v);
+  if (tc && !fp8) {
     const long long pool_rows =
         (long long)desc->num_pages * desc->num_kv_heads * desc->page_size;
     rc = make_pool_map(&tm_k, k_pages, pool_rows, p.box_rows);

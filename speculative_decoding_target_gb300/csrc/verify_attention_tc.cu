@@ -1,5 +1,6 @@
 // Split-KV paged GQA verify attention on the 5th-generation tensor cores
-// (tcgen05 MMA with TMEM accumulators, TMA tile loads), bf16 KV.
+// (tcgen05 MMA with TMEM operands and accumulators, TMA / bulk-copy loads),
+// for bf16 KV and for FP8-E4M3 KV with fp16 scales.
 //
 // One CTA per SM walks its contiguous run of 64-token units (the plan in
 // common.cuh).  For every (request b, KV head g) piece of the run, all
@@ -10,22 +11,35 @@
 // R = ceil(rows / 4), which spreads the rows over the four TMEM lane
 // quarters; the other lanes carry zero rows.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer (all 32 lanes): gathers each 64-token K and V
-//               tile of the piece page by page from the pool (one 2-D box of
-//               64 channels x min(page_size, 64) tokens per column block,
-//               lane i issuing box i) into a 2-stage ring.
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//               S buffers and O += P_j V_j into the TMEM O accumulator, each
-//               issued as soon as its inputs are ready.
+// Tensor memory (512 columns): O accumulator [0, 256), two S/P buffers of 64
+// columns [256, 384), the Q tile as an MMA A operand [384, 512) (256 16-bit
+// channels, two per column, even channel in the low half).
+//
+// Warp roles:
+//   warp 0      producer (all 32 lanes, lane i owns box i of a tile: a run of
+//               min(page_size, 64) tokens of one page; page ids prefetched
+//               one tile ahead).  bf16: 2-D TMA boxes of 64 channels with the
+//               128-byte swizzle straight into a 3-stage K/V ring.  FP8: 1-D
+//               bulk copies of the page runs of K/V bytes and their scales
+//               into a 2-stage staging ring.
+//   warp 1      MMA issuer (one thread): S_j = Q K_j^T (16 MMAs, N = 64) into
+//               an S buffer and O += P_j V_j (N = 256, V as an MN-major
+//               operand, P from TMEM) into O, each as soon as its inputs are
+//               ready.
 //   warps 2..5  softmax: one thread per TMEM lane (query row).  Load S_j,
 //               mask the block's causal tail, keep a running max m and sum l
-//               in base 2, and write P_j = 2^(s - m) back over S_j as bf16
-//               hi + lo parts (the PV MMA takes P from TMEM and runs once per
-//               part, so the bf16 rounding of P does not reach the output);
-//               rescale O in TMEM only when the running max grows by more
-//               than 2^8; finally read O, divide by l and write the bf16
-//               output or an fp32 partial.
+//               in base 2, write P_j = 2^(s - m) back over S_j; rescale O in
+//               TMEM only when m grows by more than 2^8; finally read O,
+//               divide by l and write the bf16 output or an fp32 partial.
+//               bf16 KV: P is stored as bf16 hi + lo parts and PV runs once
+//               per part (one bf16 P carries a 2^-9 relative error per
+//               weight, visible in the output when few keys are visible).
+//   warps 6..9  (FP8 only) dequant: element c of a cached row becomes
+//               fp16(e4m3(byte_c) * scale[c / 64]) in the swizzled K/V stage
+//               ("Qwen3.8-27B-FP8" page, "Implemented execution path": FP8
+//               E4M3 cache with per-token / per-KV-head FP16 scales over
+//               64-channel blocks).  The FP8 path computes in fp16 (Q, the
+//               dequantised K/V and P), which holds 11 significant bits.
 //
 // The tile width is set by the MMA issue rate: QK^T costs 16 instructions
 // per tile whatever its width, so 64-token tiles halve the instructions per
@@ -34,6 +48,8 @@
 // Every wait is bounded (about two seconds of clock); a wait that runs out
 // sets SPEC_STATUS_TIMEOUT in the status word (checked mode) and makes every
 // later wait of the CTA return at once, so the kernel always finishes.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "spec_verify.h"
 #include "tc_ptx.cuh"
@@ -42,26 +58,45 @@ namespace specv {
 namespace {
 
 constexpr int kT = 64;                        // tokens per tile
-constexpr int kStages = 2;
-constexpr int kThreads = 192;
-constexpr int kQBytes = 4 * 128 * 128;        // Q: 4 column blocks x 128 rows
-constexpr int kHalfBytes = 4 * kT * 128;      // K (or V) of one stage
+constexpr int kHalfBytes = 4 * kT * 128;      // K (or V) of one 16-bit stage
 constexpr int kStageBytes = 2 * kHalfBytes;
-constexpr int kOffKV = kQBytes;
-constexpr int kOffPre = kOffKV + kStages * kStageBytes;
 constexpr int kPreBytes = ((kMaxBatch + 1) * 4 + 127) / 128 * 128;
-constexpr int kSmemBytes = kOffPre + kPreBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;               // S/P buffers: columns 256, 320
+constexpr uint32_t kColQ = 384;               // Q: columns 384..511
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr float kRescaleLog2 = 8.0f;          // rescale O when m grows > 2^8
+// FP8 staging: K bytes, V bytes, K scales, V scales of one tile
+constexpr int kS8K = 0;
+constexpr int kS8V = kT * 256;
+constexpr int kS8KS = 2 * kT * 256;
+constexpr int kS8VS = kS8KS + kT * 8;
+constexpr int kS8Bytes = kS8VS + kT * 8;
 
-constexpr uint32_t kIdescQK = tc::idesc_bf16(128, kT, 0);
-constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 256, 1);
+template <bool kFp8>
+struct Cfg {
+  static constexpr int kStages = kFp8 ? 2 : 3;
+  static constexpr int kStages8 = kFp8 ? 2 : 0;
+  static constexpr int kThreads = kFp8 ? 320 : 192;
+  static constexpr int kOffKV = 0;
+  static constexpr int kOff8 = kOffKV + kStages * kStageBytes;
+  static constexpr int kOffPre = kOff8 + kStages8 * kS8Bytes;
+  static constexpr int kSmem = kOffPre + kPreBytes + 1024;  // + alignment
+  // kind::f16 with bf16 (1) or fp16 (0) inputs, fp32 accumulator
+  static constexpr uint32_t kAB = kFp8 ? 0u : 1u;
+  static constexpr uint32_t kIdescQK = (1u << 4) | (kAB << 7) | (kAB << 10) |
+                                       ((uint32_t)(kT >> 3) << 17) |
+                                       ((uint32_t)(128 >> 4) << 24);
+  static constexpr uint32_t kIdescPV = (1u << 4) | (kAB << 7) | (kAB << 10) |
+                                       (1u << 16) | ((uint32_t)(256 >> 3) << 17) |
+                                       ((uint32_t)(128 >> 4) << 24);
+};
 
 struct Bars {
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t kv_full[3];    // 16-bit stage holds tile j (TMA tx / dequant)
+  uint64_t kv_empty[3];   // PV of the stage's tile is done
+  uint64_t f8_full[2];    // FP8 staging landed (bulk-copy tx)
+  uint64_t f8_empty[2];   // dequant consumed the staging buffer
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
@@ -109,10 +144,16 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
       (reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
-// ---- warp 0: TMA loads of the piece's K/V tiles ----------------------------
-// Lane i owns box i of a tile (a run of min(page_size, 64) tokens of one
-// page); its page id for the next tile is loaded while the current tile
-// waits for a free stage, so the page-table latency stays off the pipeline.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src,
+                                          uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ---- warp 0: loads of the piece's K/V tiles ---------------------------------
 __device__ __forceinline__ int box_page(const AttnParams& p, const Piece& pc,
                                         int jt, int lane) {
   const int t = pc.tok_begin + jt * kT + lane * p.box_rows;
@@ -126,89 +167,184 @@ __device__ __forceinline__ int box_page(const AttnParams& p, const Piece& pc,
   return page;
 }
 
-__device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* kv,
+template <bool kFp8>
+__device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
                         const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
+  using C = Cfg<kFp8>;
   const AttnParams& p = *cx.p;
   const int lane = threadIdx.x & 31;
   const int rpb = p.box_rows;
   int page = box_page(p, pc, 0, lane);
   for (int jt = 0; jt < pc.n_tiles; ++jt) {
     const int next_page = box_page(p, pc, jt + 1, lane);
-    const int gj = gj0 + jt, st = gj % kStages;
-    if (gj >= kStages)
-      wait_bar(cx, &cx.bars->kv_empty[st], ((gj / kStages) - 1) & 1);
+    const int gj = gj0 + jt;
     const int t0 = pc.tok_begin + jt * kT;
     const int ntok = min(kT, pc.tok_end - t0);
     const int nbox = (ntok + rpb - 1) / rpb;
-    const uint32_t full = tc::smem_u32(&cx.bars->kv_full[st]);
-    if (lane == 0)
-      tc::bar_arrive_expect_tx(full, (uint32_t)(nbox * rpb * 128 * 4 * 2));
-    __syncwarp();
-    if (lane < nbox) {
-      const uint32_t kdst = tc::smem_u32(kv + st * kStageBytes);
-      const uint32_t vdst = kdst + kHalfBytes;
-      const int t = t0 + lane * rpb;
-      const int y = ((page * p.hkv + pc.g) << p.log2_ps) + (t & (p.page_size - 1));
+    const int t = t0 + lane * rpb;
+    // row of this box's first token in the [num_pages * Hkv * page_size] view
+    const long long row =
+        ((long long)(page * p.hkv + pc.g) << p.log2_ps) + (t & (p.page_size - 1));
+    if (!kFp8) {
+      const int st = gj % C::kStages;
+      if (gj >= C::kStages)
+        wait_bar(cx, &cx.bars->kv_empty[st], ((gj / C::kStages) - 1) & 1);
+      const uint32_t full = tc::smem_u32(&cx.bars->kv_full[st]);
+      if (lane == 0)
+        tc::bar_arrive_expect_tx(full, (uint32_t)(nbox * rpb * 128 * 4 * 2));
+      __syncwarp();
+      if (lane < nbox) {
+        const uint32_t kdst = tc::smem_u32(smem + C::kOffKV + st * kStageBytes);
+        const uint32_t vdst = kdst + kHalfBytes;
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        const uint32_t off = cb * (kT * 128) + lane * rpb * 128;
-        tc::tma_load_2d(kdst + off, tm_k, full, cb * 64, y);
-        tc::tma_load_2d(vdst + off, tm_v, full, cb * 64, y);
+        for (int cb = 0; cb < 4; ++cb) {
+          const uint32_t off = cb * (kT * 128) + lane * rpb * 128;
+          tc::tma_load_2d(kdst + off, tm_k, full, cb * 64, (int)row);
+          tc::tma_load_2d(vdst + off, tm_v, full, cb * 64, (int)row);
+        }
+      }
+    } else {
+      const int s8 = gj % C::kStages8;
+      if (gj >= C::kStages8)
+        wait_bar(cx, &cx.bars->f8_empty[s8], ((gj / C::kStages8) - 1) & 1);
+      const uint32_t full = tc::smem_u32(&cx.bars->f8_full[s8]);
+      if (lane == 0)
+        tc::bar_arrive_expect_tx(full, (uint32_t)(nbox * rpb * (2 * 256 + 2 * 8)));
+      __syncwarp();
+      if (lane < nbox) {
+        const uint32_t base = tc::smem_u32(smem + C::kOff8 + s8 * kS8Bytes);
+        const uint8_t* kb = static_cast<const uint8_t*>(p.k_pages);
+        const uint8_t* vb = static_cast<const uint8_t*>(p.v_pages);
+        const uint8_t* ksb = reinterpret_cast<const uint8_t*>(p.k_scales);
+        const uint8_t* vsb = reinterpret_cast<const uint8_t*>(p.v_scales);
+        const uint32_t o = lane * rpb;
+        bulk_copy(base + kS8K + o * 256, kb + row * 256, rpb * 256, full);
+        bulk_copy(base + kS8V + o * 256, vb + row * 256, rpb * 256, full);
+        bulk_copy(base + kS8KS + o * 8, ksb + row * 8, rpb * 8, full);
+        bulk_copy(base + kS8VS + o * 8, vsb + row * 8, rpb * 8, full);
       }
     }
     page = next_page;
   }
 }
 
+// ---- warps 6..9 (FP8): dequantise a staged tile into the fp16 K/V stage ------
+// Unit u of a tile = (token row, 64-channel block, 16-byte output chunk):
+// 8 E4M3 bytes -> 8 fp16 values times the row's block scale.  Rows past the
+// piece's last token are written as zeros (their bytes are not data).
+__device__ __forceinline__ uint4 dequant8(uint2 raw, __half2 sc) {
+  uint4 out;
+  uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+  const uint32_t w[2] = {raw.x, raw.y};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const __nv_fp8x2_storage_t pair =
+        static_cast<__nv_fp8x2_storage_t>((w[k >> 1] >> (16 * (k & 1))) & 0xFFFF);
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+    __half2 h = *reinterpret_cast<const __half2*>(&hr);
+    h = __hmul2(h, sc);
+    o[k] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return out;
+}
+
+__device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
+                              uint8_t* smem) {
+  using C = Cfg<true>;
+  const int tid = threadIdx.x - 192;  // 0..127
+  const int lane = threadIdx.x & 31;
+  for (int jt = 0; jt < pc.n_tiles; ++jt) {
+    const int gj = gj0 + jt;
+    const int s8 = gj % C::kStages8, st = gj % C::kStages;
+    const int t0 = pc.tok_begin + jt * kT;
+    const int nvalid = min(kT, pc.tok_end - t0);
+    wait_bar(cx, &cx.bars->f8_full[s8], (gj / C::kStages8) & 1);
+    if (gj >= C::kStages)
+      wait_bar(cx, &cx.bars->kv_empty[st], ((gj / C::kStages) - 1) & 1);
+    const uint8_t* s8p = smem + C::kOff8 + s8 * kS8Bytes;
+    uint8_t* dst = smem + C::kOffKV + st * kStageBytes;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {  // K then V
+      const uint8_t* src = s8p + (half ? kS8V : kS8K);
+      const __half* scl =
+          reinterpret_cast<const __half*>(s8p + (half ? kS8VS : kS8KS));
+      uint8_t* out = dst + half * kHalfBytes;
+#pragma unroll 4
+      for (int u = tid; u < kT * 32; u += 128) {
+        const int row = u >> 5, rem = u & 31, cb = rem >> 3, ch = rem & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < nvalid) {
+          const uint2 raw =
+              *reinterpret_cast<const uint2*>(src + row * 256 + cb * 64 + ch * 8);
+          const __half s = scl[row * 4 + cb];
+          v = dequant8(raw, __halves2half2(s, s));
+        }
+        *reinterpret_cast<uint4*>(out + cb * (kT * 128) + row * 128 +
+                                  ((ch ^ (row & 7)) << 4)) = v;
+      }
+    }
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tc::bar_arrive(tc::smem_u32(&cx.bars->kv_full[st]));
+      tc::bar_arrive(tc::smem_u32(&cx.bars->f8_empty[s8]));
+    }
+  }
+}
+
 // ---- warp 1, one thread: MMA issue -------------------------------------------
-// S_j = Q K_j^T and O += P_j V_j are issued as soon as their inputs are
-// ready, whichever comes first: a PV never waits behind the next tile's TMA.
+template <bool kFp8>
 __device__ __forceinline__ void issue_qk(const Ctx& cx, int gj, uint32_t tmem,
                                          uint8_t* smem) {
-  const int st = gj % kStages;
-  const uint32_t qbase = tc::smem_u32(smem);
-  const uint32_t kbase = tc::smem_u32(smem + kOffKV + st * kStageBytes);
+  using C = Cfg<kFp8>;
+  const int st = gj % C::kStages;
+  const uint32_t kbase = tc::smem_u32(smem + C::kOffKV + st * kStageBytes);
   const uint32_t d = tmem + kColS + (gj & 1) * kT;
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
-    const uint64_t ad = tc::desc_sw128(qbase + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
     const uint64_t bd = tc::desc_sw128(kbase + (k >> 2) * (kT * 128) + (k & 3) * 32, 16, 1024);
-    tc::mma_bf16(d, ad, bd, kIdescQK, k > 0 ? 1u : 0u);
+    tc::mma_bf16_ta(d, tmem + kColQ + k * 8, bd, C::kIdescQK, k > 0 ? 1u : 0u);
   }
   tc::commit(tc::smem_u32(&cx.bars->s_full[gj & 1]));
 }
 
+template <bool kFp8>
 __device__ __forceinline__ void issue_pv(const Ctx& cx, int gj, bool first,
                                          uint32_t tmem, uint8_t* smem) {
-  const int st = gj % kStages;
-  const uint32_t vbase = tc::smem_u32(smem + kOffKV + st * kStageBytes) + kHalfBytes;
-  const uint32_t p_hi = tmem + kColS + (gj & 1) * kT;  // 32 columns: bf16 pairs
+  using C = Cfg<kFp8>;
+  const int st = gj % C::kStages;
+  const uint32_t vbase =
+      tc::smem_u32(smem + C::kOffKV + st * kStageBytes) + kHalfBytes;
+  const uint32_t p_hi = tmem + kColS + (gj & 1) * kT;  // 32 columns: pairs
   const uint32_t p_lo = p_hi + kT / 2;
 #pragma unroll
   for (int kk = 0; kk < kT / 16; ++kk) {
     const uint64_t bd = tc::desc_sw128(vbase + kk * 2048, kT * 128, 1024);
-    tc::mma_bf16_ta(tmem, p_hi + kk * 8, bd, kIdescPV,
+    tc::mma_bf16_ta(tmem, p_hi + kk * 8, bd, C::kIdescPV,
                     (first && kk == 0) ? 0u : 1u);
-    tc::mma_bf16_ta(tmem, p_lo + kk * 8, bd, kIdescPV, 1u);
+    if (!kFp8) tc::mma_bf16_ta(tmem, p_lo + kk * 8, bd, C::kIdescPV, 1u);
   }
   tc::commit(tc::smem_u32(&cx.bars->kv_empty[st]));
   tc::commit(tc::smem_u32(&cx.bars->pv_done[gj & 1]));
 }
 
+template <bool kFp8>
 __device__ void mma_piece(const Ctx& cx, const Piece& pc, int gj0, uint32_t tmem,
                           uint8_t* smem) {
+  using C = Cfg<kFp8>;
   int qk = 0, pv = 0;
   long long last = clock64();
   while (pv < pc.n_tiles) {
     bool did = false;
     if (qk < pc.n_tiles) {
       const int gj = gj0 + qk;
-      if (tc::bar_try_wait(tc::smem_u32(&cx.bars->kv_full[gj % kStages]),
-                           (gj / kStages) & 1) &&
+      // the S/P buffer of tile gj is free once PV of tile gj-2 is done
+      if (tc::bar_try_wait(tc::smem_u32(&cx.bars->kv_full[gj % C::kStages]),
+                           (gj / C::kStages) & 1) &&
           (gj < 2 || tc::bar_try_wait(tc::smem_u32(&cx.bars->pv_done[gj & 1]),
                                       ((gj >> 1) - 1) & 1))) {
         tc::fence_after();
-        issue_qk(cx, gj, tmem, smem);
+        issue_qk<kFp8>(cx, gj, tmem, smem);
         ++qk;
         did = true;
       }
@@ -218,7 +354,7 @@ __device__ void mma_piece(const Ctx& cx, const Piece& pc, int gj0, uint32_t tmem
       if (tc::bar_try_wait(tc::smem_u32(&cx.bars->p_full[gj & 1]),
                            (gj >> 1) & 1)) {
         tc::fence_after();
-        issue_pv(cx, gj, pv == 0, tmem, smem);
+        issue_pv<kFp8>(cx, gj, pv == 0, tmem, smem);
         ++pv;
         did = true;
       }
@@ -235,13 +371,55 @@ __device__ void mma_piece(const Ctx& cx, const Piece& pc, int gj0, uint32_t tmem
   }
 }
 
-// ---- warps 2..5: softmax and epilogue ----------------------------------------
+// ---- warps 2..5: Q load, softmax and epilogue -------------------------------
+// Each softmax thread writes its TMEM lane of the Q operand: the query row it
+// owns (bf16, or converted to fp16 for FP8 KV), or zeros.
+template <bool kFp8>
+__device__ __forceinline__ void load_q_tmem(const AttnParams& p, const Piece& pc,
+                                            uint32_t tmem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w4 = warp & 3;
+  const int R = (p.rows + 3) >> 2;
+  const int r = w4 * R + lane;
+  const bool valid = lane < R && r < p.rows;
+  const int i = valid ? r / p.group : 0;
+  const int h = pc.g * p.group + (valid ? r - i * p.group : 0);
+  const uint4* src = reinterpret_cast<const uint4*>(
+      p.q + (((long long)pc.b * p.q_len + i) * p.hq + h) * kHeadDim);
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16) + kColQ;
+#pragma unroll 1
+  for (int cb = 0; cb < 4; ++cb) {  // 64 channels = 32 columns per step
+    uint32_t v[32];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint4 x = valid ? __ldg(src + cb * 8 + k) : make_uint4(0, 0, 0, 0);
+      if (kFp8) {  // bf16 pairs -> fp16 pairs
+        uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+          const __half2 h2 = __floats2half2_rn(__low2float(b2), __high2float(b2));
+          w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      }
+      v[4 * k] = x.x;
+      v[4 * k + 1] = x.y;
+      v[4 * k + 2] = x.z;
+      v[4 * k + 3] = x.w;
+    }
+    tc::tmem_st32(lane_base + cb * 32, reinterpret_cast<const float*>(v));
+  }
+  tc::tmem_wait_st();
+}
+
+template <bool kFp8>
 __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
                               uint32_t tmem, uint8_t* smem, const int* s_pre,
                               long long U, int P, int c) {
+  using C = Cfg<kFp8>;
   const AttnParams& p = *cx.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int w4 = warp & 3, pos = 32 * w4 + lane;
+  const int w4 = warp & 3;
   const int R = (p.rows + 3) >> 2;
   const int r = w4 * R + lane;
   const bool valid = lane < R && r < p.rows;
@@ -307,18 +485,24 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
       const float x1 = exp2f(fmaf(s[k + 1], sl2, -mu));
       sum4[k & 3] += x0;
       sum4[(k & 3) + 1] += x1;
-      const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
-      const __nv_bfloat162 ll =
-          __floats2bfloat162_rn(x0 - __low2float(hh), x1 - __high2float(hh));
-      hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
-      lo[k >> 1] = *reinterpret_cast<const uint32_t*>(&ll);
+      if (kFp8) {
+        const __half2 hh = __floats2half2_rn(x0, x1);
+        hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
+      } else {
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
+        const __nv_bfloat162 ll =
+            __floats2bfloat162_rn(x0 - __low2float(hh), x1 - __high2float(hh));
+        hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
+        lo[k >> 1] = *reinterpret_cast<const uint32_t*>(&ll);
+      }
     }
     l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-    // V rows past the piece's last token must be zero (0 * NaN poisons PV)
-    if (t0 + kT > pc.tok_end) {
-      const int st = gj % kStages;
-      wait_bar(cx, &cx.bars->kv_full[st], (gj / kStages) & 1);
-      uint8_t* v = smem + kOffKV + st * kStageBytes + kHalfBytes;
+    // bf16: V rows past the piece's last token must be zero (0 * NaN
+    // poisons PV); the FP8 dequant warps write those rows as zeros.
+    if (!kFp8 && t0 + kT > pc.tok_end) {
+      const int st = gj % C::kStages;
+      wait_bar(cx, &cx.bars->kv_full[st], (gj / C::kStages) & 1);
+      uint8_t* v = smem + C::kOffKV + st * kStageBytes + kHalfBytes;
       const int z0 = pc.tok_end - t0;
       const int n = (kT - z0) * 4 * 8;  // rows x column blocks x chunks
       for (int e = threadIdx.x - 64; e < n; e += 128) {
@@ -328,9 +512,9 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
       }
       tc::fence_proxy_async_smem();
     }
-    // P_j over S_j: hi in the first 32 columns, lo in the next 32
+    // P_j over S_j: hi in the first 32 columns, lo (bf16) in the next 32
     tc::tmem_st32(sbuf, reinterpret_cast<const float*>(hi));
-    tc::tmem_st32(sbuf + kT / 2, reinterpret_cast<const float*>(lo));
+    if (!kFp8) tc::tmem_st32(sbuf + kT / 2, reinterpret_cast<const float*>(lo));
     tc::tmem_wait_st();
     tc::fence_before();
     __syncwarp();
@@ -391,33 +575,15 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
   }
 }
 
-// Softmax threads write their Q row of piece (b, g) into the swizzled tile.
-__device__ __forceinline__ void load_q_row(const AttnParams& p, const Piece& pc,
-                                           uint8_t* q_s) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int w4 = warp & 3, pos = 32 * w4 + lane;
-  const int R = (p.rows + 3) >> 2;
-  const int r = w4 * R + lane;
-  if (!(lane < R && r < p.rows)) return;
-  const int i = r / p.group, h = pc.g * p.group + (r - i * p.group);
-  const uint4* src = reinterpret_cast<const uint4*>(
-      p.q + (((long long)pc.b * p.q_len + i) * p.hq + h) * kHeadDim);
-#pragma unroll 8
-  for (int cidx = 0; cidx < 32; ++cidx) {
-    const uint4 v = __ldg(src + cidx);
-    const int blk = cidx >> 3, ch = cidx & 7;
-    *reinterpret_cast<uint4*>(q_s + blk * 16384 + pos * 128 +
-                              ((ch ^ (pos & 7)) << 4)) = v;
-  }
-}
-
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kFp8>
+__global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     verify_split_tc_kernel(const AttnParams p,
                            const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v) {
+  using C = Cfg<kFp8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  int* s_pre = reinterpret_cast<int*>(smem + kOffPre);
+  int* s_pre = reinterpret_cast<int*>(smem + C::kOffPre);
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -430,9 +596,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (c >= P) return;  // uniform over the CTA, before any TMEM or barrier use
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      tc::bar_init(tc::smem_u32(&bars.kv_full[s]), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      // bf16: one arrival (the producer's expect_tx) plus the TMA bytes;
+      // FP8: one arrival per dequant warp
+      tc::bar_init(tc::smem_u32(&bars.kv_full[s]), kFp8 ? 4 : 1);
       tc::bar_init(tc::smem_u32(&bars.kv_empty[s]), 1);
+    }
+    for (int s = 0; s < C::kStages8; ++s) {
+      tc::bar_init(tc::smem_u32(&bars.f8_full[s]), 1);
+      tc::bar_init(tc::smem_u32(&bars.f8_empty[s]), 4);
     }
     for (int s = 0; s < 2; ++s) {
       tc::bar_init(tc::smem_u32(&bars.s_full[s]), 1);
@@ -444,15 +616,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::bar_fence_init();
   }
   if (warp == 1) tc::tmem_alloc(tc::smem_u32(&s_tmem), kTmemCols);
-  if (warp >= 2) {  // zero every Q row once; valid rows are rewritten per piece
-    const int pos = 32 * (warp & 3) + lane;
-#pragma unroll
-    for (int blk = 0; blk < 4; ++blk)
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(smem + blk * 16384 + pos * 128 + ch * 16) =
-            make_uint4(0, 0, 0, 0);
-  }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -478,23 +641,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     pc.tok_end = min(j1 * kUnit, pc.len);
     pc.n_tiles = (pc.tok_end - pc.tok_begin + kT - 1) / kT;
 
-    if (warp >= 2) {
-      load_q_row(p, pc, smem);
-      tc::fence_proxy_async_smem();
-    }
+    if (warp >= 2 && warp < 6) load_q_tmem<kFp8>(p, pc, tmem);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     if (warp == 0) {
-      // the whole warp: lanes issue the boxes of their pages
-      produce(cx, pc, gj0, smem + kOffKV, &tm_k, &tm_v);
+      // the whole warp: lanes issue the copies of their pages
+      produce<kFp8>(cx, pc, gj0, smem, &tm_k, &tm_v);
       last_loaded = gj0 + pc.n_tiles - 1;
       __syncwarp();
     } else if (warp == 1) {
-      if (lane == 0) mma_piece(cx, pc, gj0, tmem, smem);
+      if (lane == 0) mma_piece<kFp8>(cx, pc, gj0, tmem, smem);
       __syncwarp();
-    } else {
-      softmax_piece(cx, pc, gj0, tmem, smem, s_pre, U, P, c);
+    } else if (warp < 6) {
+      softmax_piece<kFp8>(cx, pc, gj0, tmem, smem, s_pre, U, P, c);
+    } else if (kFp8) {
+      dequant_piece(cx, pc, gj0, smem);
     }
     gj0 += pc.n_tiles;
     tc::fence_before();
@@ -502,10 +664,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after();
   }
 
-  // teardown: no TMA copy or MMA may still be in flight
+  // teardown: no copy or MMA may still be in flight
   if (warp == 0 && lane == 0) {
-    for (int gj = max(0, last_loaded - kStages + 1); gj <= last_loaded; ++gj)
-      wait_bar(cx, &bars.kv_full[gj % kStages], (gj / kStages) & 1, true);
+    const int S = kFp8 ? C::kStages8 : C::kStages;
+    for (int gj = max(0, last_loaded - S + 1); gj <= last_loaded; ++gj) {
+      if (kFp8)
+        wait_bar(cx, &bars.f8_full[gj % S], (gj / S) & 1, true);
+      else
+        wait_bar(cx, &bars.kv_full[gj % S], (gj / S) & 1, true);
+    }
   }
   if (warp == 1 && lane == 0) {
     tc::commit(tc::smem_u32(&bars.drain));
@@ -517,28 +684,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+template <bool kFp8>
+cudaError_t launch(const AttnParams& p, const CUtensorMap& tm_k,
+                   const CUtensorMap& tm_v, cudaStream_t s) {
+  using C = Cfg<kFp8>;
+  cudaError_t e = cudaFuncSetAttribute(verify_split_tc_kernel<kFp8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmem);
+  if (e != cudaSuccess) return e;
+  verify_split_tc_kernel<kFp8><<<p.grid, C::kThreads, C::kSmem, s>>>(p, tm_k, tm_v);
+  return cudaGetLastError();
+}
+
+template <bool kFp8>
+int ctas_per_sm() {
+  using C = Cfg<kFp8>;
+  if (cudaFuncSetAttribute(verify_split_tc_kernel<kFp8>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmem) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &n, verify_split_tc_kernel<kFp8>, C::kThreads, C::kSmem) !=
+      cudaSuccess)
+    return 0;
+  return n < 1 ? 0 : 1;  // TMEM: one 512-column allocation per SM
+}
+
 }  // namespace
 
 cudaError_t launch_verify_split_tc(const AttnParams& p, const CUtensorMap& tm_k,
                                    const CUtensorMap& tm_v, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(
-      verify_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      kSmemBytes);
-  if (e != cudaSuccess) return e;
-  verify_split_tc_kernel<<<p.grid, kThreads, kSmemBytes, s>>>(p, tm_k, tm_v);
-  return cudaGetLastError();
+  return p.k_scales ? launch<true>(p, tm_k, tm_v, s)
+                    : launch<false>(p, tm_k, tm_v, s);
 }
 
-int verify_split_tc_ctas_per_sm() {
-  if (cudaFuncSetAttribute(verify_split_tc_kernel,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess)
-    return 0;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &n, verify_split_tc_kernel, kThreads, kSmemBytes) != cudaSuccess)
-    return 0;
-  return n < 1 ? 0 : 1;  // TMEM: one 512-column allocation per SM
+int verify_split_tc_ctas_per_sm(bool fp8) {
+  return fp8 ? ctas_per_sm<true>() : ctas_per_sm<false>();
 }
 
 int verify_split_tc_box_rows(int page_size) { return page_size < kT ? page_size : kT; }

@@ -90,6 +90,10 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert _attn(lib, _desc(), scale=-0.5) == _native.SPEC_ERR_ARG
     fp8 = _desc(kv_dtype="fp8")
     assert _attn(lib, fp8) == _native.SPEC_ERR_ARG          # scales missing
+    assert _attn(lib, fp8, k_scales=ctypes.c_void_p(0x100008),
+                 v_scales=FAKE) == _native.SPEC_ERR_ALIGN  # 16 B needed
+    assert _attn(lib, _desc(kv_dtype="fp8", page_size=4), k_scales=FAKE,
+                 v_scales=FAKE) == _native.SPEC_ERR_UNSUPPORTED
 
 
 def test_empty_batch_is_a_noop(lib):

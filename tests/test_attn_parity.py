@@ -42,6 +42,36 @@ def test_grid_bf16(q_len, pi):
     _check_all(inp, f"q_len={q_len} prefix={prefix} ps={ps} B={B}")
 
 
+FP8_PREFIXES = [0, 17, 65, 321, 4096]
+
+
+@pytest.mark.parametrize("q_len", [1, 8, 16])
+@pytest.mark.parametrize("pi", range(len(FP8_PREFIXES)))
+def test_grid_fp8(q_len, pi):
+    prefix = FP8_PREFIXES[pi]
+    ps = 16 if pi % 2 == 0 else 64
+    B = 1 if pi % 3 == 0 else 3
+    inp = _case(B, q_len, prefix, ps, kv_dtype="fp8_e4m3",
+                seed=500 + 10 * q_len + pi)
+    _check_all(inp, f"fp8 q_len={q_len} prefix={prefix} ps={ps} B={B}")
+
+
+@pytest.mark.parametrize("ps", [8, 32, 128])
+def test_fp8_page_sizes_and_ragged(ps):
+    g = torch.Generator().manual_seed(ps)
+    prefixes = torch.randint(0, 2500, (9,), generator=g).tolist()
+    inp = _case(9, 8, prefixes, ps, kv_dtype="fp8_e4m3", seed=ps + 7)
+    _check_all(inp, f"fp8 page_size={ps} ragged")
+
+
+def test_fp8_rejects_small_pages():
+    import speculative_decoding_target_gb300 as sv
+    inp = _case(1, 8, 40, 4, kv_dtype="fp8_e4m3", seed=1)
+    with pytest.raises(sv.SpecError) as e:     # refused on the host
+        gpu_attention(inp)
+    assert "page_size" in str(e.value)
+
+
 @pytest.mark.parametrize("hq,hkv,q_len", [(8, 8, 8), (32, 4, 16), (4, 1, 16),
                                           (24, 4, 3), (12, 2, 5)])
 def test_gqa_shapes(hq, hkv, q_len):
@@ -117,19 +147,25 @@ def _sample_rows(w, n, seed):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", [n for n in wl.WORKLOAD_ORDER
-                                  if wl.WORKLOADS[n].kv_dtype == "bf16"])
+@pytest.mark.parametrize("name", wl.WORKLOAD_ORDER)
 def test_full_size_workloads_sampled_rows(name):
     w = wl.WORKLOADS[name]
+    fp8 = w.kv_dtype != "bf16"
     inp = wl.workload_inputs(w, device=DEV, with_accept=False)
     out = gpu_attention(inp)
     torch.cuda.synchronize()
     # property at any size: every output is a convex combination of V rows
-    vmax = inp["v_pages"].float().nan_to_num(0.0).abs().max().item()
+    if fp8:
+        v = inp["v_pages"].view(torch.float8_e4m3fn).float() * \
+            inp["v_scales"].float().repeat_interleave(64, dim=-1)
+    else:
+        v = inp["v_pages"].float()
+    vmax = v.nan_to_num(0.0).abs().max().item()
+    del v
     o = out.float()
     assert torch.isfinite(o).all()
-    assert o.abs().max().item() <= vmax * (1 + 2 ** -7)
+    assert o.abs().max().item() <= vmax * (1 + 2 ** -7) + (0.05 if fp8 else 0)
     n = 24 if w.batch * w.q_len * w.num_q_heads > 256 else 10 ** 9
     rows = _sample_rows(w, n, w.seed)
     ref = oracle_attention(inp, rows=np.asarray(rows, np.int64))
-    assert_attention_close(rows_of(out, rows), ref, False, name)
+    assert_attention_close(rows_of(out, rows), ref, fp8, name)
