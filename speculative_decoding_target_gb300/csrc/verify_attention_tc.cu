@@ -73,6 +73,9 @@ constexpr int kS8KS = 2 * kT * 256;
 constexpr int kS8VS = kS8KS + kT * 8;
 constexpr int kS8Bytes = kS8VS + kT * 8;
 
+// bf16: K/V stage s at s * kStageBytes (K) and + kHalfBytes (V), one
+// barrier pair per stage.  FP8: separate 2-slot K and V rings, so a K slot
+// is refilled as soon as its QK^T is done rather than after the PV.
 template <bool kFp8>
 struct Cfg {
   static constexpr int kStages = kFp8 ? 2 : 3;
@@ -81,6 +84,13 @@ struct Cfg {
   static constexpr int kOffKV = 0;
   static constexpr int kOff8 = kOffKV + kStages * kStageBytes;
   static constexpr int kOffPre = kOff8 + kStages8 * kS8Bytes;
+  __device__ static uint32_t k_off(int gj) {
+    return kFp8 ? (gj % kStages) * kHalfBytes : (gj % kStages) * kStageBytes;
+  }
+  __device__ static uint32_t v_off(int gj) {
+    return kFp8 ? kStages * kHalfBytes + (gj % kStages) * kHalfBytes
+                : (gj % kStages) * kStageBytes + kHalfBytes;
+  }
   static constexpr int kSmem = kOffPre + kPreBytes + 1024;  // + alignment
   // kind::f16 with bf16 (1) or fp16 (0) inputs, fp32 accumulator
   static constexpr uint32_t kAB = kFp8 ? 0u : 1u;
@@ -93,8 +103,10 @@ struct Cfg {
 };
 
 struct Bars {
-  uint64_t kv_full[3];    // 16-bit stage holds tile j (TMA tx / dequant)
-  uint64_t kv_empty[3];   // PV of the stage's tile is done
+  uint64_t kv_full[3];    // bf16: stage holds tile j (TMA tx); FP8: K slot
+  uint64_t kv_empty[3];   // bf16: PV of the stage's tile done; FP8: QK done
+  uint64_t v_full[2];     // FP8: V slot dequantised
+  uint64_t v_empty[2];    // FP8: PV of the V slot's tile done
   uint64_t f8_full[2];    // FP8 staging landed (bulk-copy tx)
   uint64_t f8_empty[2];   // dequant consumed the staging buffer
   uint64_t s_full[2];
@@ -228,24 +240,19 @@ __device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
   }
 }
 
-// ---- warps 6..9 (FP8): dequantise a staged tile into the fp16 K/V stage ------
-// Unit u of a tile = (token row, 64-channel block, 16-byte output chunk):
-// 8 E4M3 bytes -> 8 fp16 values times the row's block scale.  Rows past the
-// piece's last token are written as zeros (their bytes are not data).
-__device__ __forceinline__ uint4 dequant8(uint2 raw, __half2 sc) {
-  uint4 out;
-  uint32_t* o = reinterpret_cast<uint32_t*>(&out);
-  const uint32_t w[2] = {raw.x, raw.y};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const __nv_fp8x2_storage_t pair =
-        static_cast<__nv_fp8x2_storage_t>((w[k >> 1] >> (16 * (k & 1))) & 0xFFFF);
-    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-    __half2 h = *reinterpret_cast<const __half2*>(&hr);
-    h = __hmul2(h, sc);
-    o[k] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  return out;
+// ---- warps 6..9 (FP8): dequantise a staged tile into the fp16 K/V slots -----
+// Thread t converts 16-byte input chunks c16 = t & 15 of rows (t >> 4) + 8k
+// (k = 0..7), first of K, then of V: 16 E4M3 bytes = channels 16*c16 ..
+// 16*c16+15, one 64-channel block and one scale, two 16-byte output chunks.
+// A thread's rows agree modulo 8, so its swizzled output offsets and its
+// scale offsets are fixed strides of k, and all eight loads of a half are
+// issued before the first conversion.  Rows past the piece's last token are
+// written as zeros (their bytes are not data).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16, __half2 sc) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+      static_cast<__nv_fp8x2_storage_t>(pair16), __NV_E4M3);
+  const __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&hr), sc);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
@@ -253,42 +260,61 @@ __device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
   using C = Cfg<true>;
   const int tid = threadIdx.x - 192;  // 0..127
   const int lane = threadIdx.x & 31;
+  const int c16 = tid & 15, r0 = tid >> 4;  // rows r0 + 8k
+  const int cb = c16 >> 2, ch0 = (c16 & 3) * 2;
+  const int src_off = r0 * 256 + c16 * 16;
+  const int sc_off = r0 * 8 + cb * 2;
+  const int dst_off0 = cb * (kT * 128) + r0 * 128 + ((ch0 ^ (r0 & 7)) << 4);
+  const int dst_off1 = cb * (kT * 128) + r0 * 128 + (((ch0 + 1) ^ (r0 & 7)) << 4);
   for (int jt = 0; jt < pc.n_tiles; ++jt) {
     const int gj = gj0 + jt;
     const int s8 = gj % C::kStages8, st = gj % C::kStages;
     const int t0 = pc.tok_begin + jt * kT;
     const int nvalid = min(kT, pc.tok_end - t0);
     wait_bar(cx, &cx.bars->f8_full[s8], (gj / C::kStages8) & 1);
-    if (gj >= C::kStages)
-      wait_bar(cx, &cx.bars->kv_empty[st], ((gj / C::kStages) - 1) & 1);
     const uint8_t* s8p = smem + C::kOff8 + s8 * kS8Bytes;
-    uint8_t* dst = smem + C::kOffKV + st * kStageBytes;
-#pragma unroll 1
+#pragma unroll
     for (int half = 0; half < 2; ++half) {  // K then V
-      const uint8_t* src = s8p + (half ? kS8V : kS8K);
-      const __half* scl =
-          reinterpret_cast<const __half*>(s8p + (half ? kS8VS : kS8KS));
-      uint8_t* out = dst + half * kHalfBytes;
-#pragma unroll 4
-      for (int u = tid; u < kT * 32; u += 128) {
-        const int row = u >> 5, rem = u & 31, cb = rem >> 3, ch = rem & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < nvalid) {
-          const uint2 raw =
-              *reinterpret_cast<const uint2*>(src + row * 256 + cb * 64 + ch * 8);
-          const __half s = scl[row * 4 + cb];
-          v = dequant8(raw, __halves2half2(s, s));
-        }
-        *reinterpret_cast<uint4*>(out + cb * (kT * 128) + row * 128 +
-                                  ((ch ^ (row & 7)) << 4)) = v;
+      if (gj >= C::kStages)  // the slot's previous tile is done with it
+        wait_bar(cx, half ? &cx.bars->v_empty[st] : &cx.bars->kv_empty[st],
+                 ((gj / C::kStages) - 1) & 1);
+      const uint8_t* src = s8p + (half ? kS8V : kS8K) + src_off;
+      const uint8_t* scl = s8p + (half ? kS8VS : kS8KS) + sc_off;
+      uint8_t* out = smem + (half ? C::v_off(gj) : C::k_off(gj));
+      uint4 raw[8];
+      __half sc[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        raw[k] = *reinterpret_cast<const uint4*>(src + k * 8 * 256);
+        sc[k] = *reinterpret_cast<const __half*>(scl + k * 8 * 8);
       }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const __half2 s2 = __halves2half2(sc[k], sc[k]);
+        const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+        uint4 a, b;
+        a.x = e4m3x2_to_f16x2(w[0] & 0xFFFF, s2);
+        a.y = e4m3x2_to_f16x2(w[0] >> 16, s2);
+        a.z = e4m3x2_to_f16x2(w[1] & 0xFFFF, s2);
+        a.w = e4m3x2_to_f16x2(w[1] >> 16, s2);
+        b.x = e4m3x2_to_f16x2(w[2] & 0xFFFF, s2);
+        b.y = e4m3x2_to_f16x2(w[2] >> 16, s2);
+        b.z = e4m3x2_to_f16x2(w[3] & 0xFFFF, s2);
+        b.w = e4m3x2_to_f16x2(w[3] >> 16, s2);
+        if (r0 + 8 * k >= nvalid) {
+          a = make_uint4(0, 0, 0, 0);
+          b = a;
+        }
+        *reinterpret_cast<uint4*>(out + dst_off0 + k * 8 * 128) = a;
+        *reinterpret_cast<uint4*>(out + dst_off1 + k * 8 * 128) = b;
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0)
+        tc::bar_arrive(tc::smem_u32(half ? &cx.bars->v_full[st]
+                                         : &cx.bars->kv_full[st]));
     }
-    tc::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tc::bar_arrive(tc::smem_u32(&cx.bars->kv_full[st]));
-      tc::bar_arrive(tc::smem_u32(&cx.bars->f8_empty[s8]));
-    }
+    if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->f8_empty[s8]));
   }
 }
 
@@ -297,14 +323,14 @@ template <bool kFp8>
 __device__ __forceinline__ void issue_qk(const Ctx& cx, int gj, uint32_t tmem,
                                          uint8_t* smem) {
   using C = Cfg<kFp8>;
-  const int st = gj % C::kStages;
-  const uint32_t kbase = tc::smem_u32(smem + C::kOffKV + st * kStageBytes);
+  const uint32_t kbase = tc::smem_u32(smem + C::k_off(gj));
   const uint32_t d = tmem + kColS + (gj & 1) * kT;
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
     const uint64_t bd = tc::desc_sw128(kbase + (k >> 2) * (kT * 128) + (k & 3) * 32, 16, 1024);
     tc::mma_bf16_ta(d, tmem + kColQ + k * 8, bd, C::kIdescQK, k > 0 ? 1u : 0u);
   }
+  if (kFp8) tc::commit(tc::smem_u32(&cx.bars->kv_empty[gj % C::kStages]));
   tc::commit(tc::smem_u32(&cx.bars->s_full[gj & 1]));
 }
 
@@ -313,8 +339,7 @@ __device__ __forceinline__ void issue_pv(const Ctx& cx, int gj, bool first,
                                          uint32_t tmem, uint8_t* smem) {
   using C = Cfg<kFp8>;
   const int st = gj % C::kStages;
-  const uint32_t vbase =
-      tc::smem_u32(smem + C::kOffKV + st * kStageBytes) + kHalfBytes;
+  const uint32_t vbase = tc::smem_u32(smem + C::v_off(gj));
   const uint32_t p_hi = tmem + kColS + (gj & 1) * kT;  // 32 columns: pairs
   const uint32_t p_lo = p_hi + kT / 2;
 #pragma unroll
@@ -324,7 +349,7 @@ __device__ __forceinline__ void issue_pv(const Ctx& cx, int gj, bool first,
                     (first && kk == 0) ? 0u : 1u);
     if (!kFp8) tc::mma_bf16_ta(tmem, p_lo + kk * 8, bd, C::kIdescPV, 1u);
   }
-  tc::commit(tc::smem_u32(&cx.bars->kv_empty[st]));
+  tc::commit(tc::smem_u32(kFp8 ? &cx.bars->v_empty[st] : &cx.bars->kv_empty[st]));
   tc::commit(tc::smem_u32(&cx.bars->pv_done[gj & 1]));
 }
 
@@ -352,7 +377,9 @@ __device__ void mma_piece(const Ctx& cx, const Piece& pc, int gj0, uint32_t tmem
     if (pv < qk) {
       const int gj = gj0 + pv;
       if (tc::bar_try_wait(tc::smem_u32(&cx.bars->p_full[gj & 1]),
-                           (gj >> 1) & 1)) {
+                           (gj >> 1) & 1) &&
+          (!kFp8 || tc::bar_try_wait(tc::smem_u32(&cx.bars->v_full[gj % C::kStages]),
+                                     (gj / C::kStages) & 1))) {
         tc::fence_after();
         issue_pv<kFp8>(cx, gj, pv == 0, tmem, smem);
         ++pv;
@@ -502,7 +529,7 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
     if (!kFp8 && t0 + kT > pc.tok_end) {
       const int st = gj % C::kStages;
       wait_bar(cx, &cx.bars->kv_full[st], (gj / C::kStages) & 1);
-      uint8_t* v = smem + C::kOffKV + st * kStageBytes + kHalfBytes;
+      uint8_t* v = smem + C::v_off(gj);
       const int z0 = pc.tok_end - t0;
       const int n = (kT - z0) * 4 * 8;  // rows x column blocks x chunks
       for (int e = threadIdx.x - 64; e < n; e += 128) {
@@ -601,6 +628,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       // FP8: one arrival per dequant warp
       tc::bar_init(tc::smem_u32(&bars.kv_full[s]), kFp8 ? 4 : 1);
       tc::bar_init(tc::smem_u32(&bars.kv_empty[s]), 1);
+      if (kFp8) {
+        tc::bar_init(tc::smem_u32(&bars.v_full[s]), 4);
+        tc::bar_init(tc::smem_u32(&bars.v_empty[s]), 1);
+      }
     }
     for (int s = 0; s < C::kStages8; ++s) {
       tc::bar_init(tc::smem_u32(&bars.f8_full[s]), 1);
