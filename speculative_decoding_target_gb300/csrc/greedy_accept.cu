@@ -4,7 +4,7 @@
 // section 1.6.1 commit_lens = accept_len + 1).
 //
 // Kernel 1 streams the fp32 logits once: CTA (chunk, row) reduces 8192
-// entries with 16-byte streaming loads to a (value, index) pair.  Kernel 2,
+// entries with 16-byte streaming loads to a (maximum, first index) pair.  Kernel 2,
 // one CTA per request, reduces the chunk pairs of its q_len rows and walks
 // the drafts.  The reduction order is arbitrary, so the combine is a total
 // order that makes the result unique: NaN above every number (lower index
@@ -39,57 +39,93 @@ __device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
   }
 }
 
+// Maximum that propagates NaN (IEEE maxNum would drop it).
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ bool hits(float e, float M, bool nanM) {
+  return nanM ? e != e : e == M;
+}
+
+// One CTA per (8192-entry chunk, row).  Pass 1 takes the chunk's maximum
+// with one NaN-propagating max per logit; only threads that hold that
+// maximum then look for its first index among their own logits (in index
+// order), and the smallest such index wins.  The pair (maximum, first
+// index) is the same one the total order above selects.
 __global__ void __launch_bounds__(kAcceptThreads)
     argmax_partial_kernel(const AcceptParams p) {
+  constexpr int kVec = kAcceptChunk / 4 / kAcceptThreads;  // float4 per thread
+  __shared__ float s_m[kAcceptThreads / 32];
+  __shared__ int s_i[kAcceptThreads / 32];
   const int chunk = blockIdx.x, row = blockIdx.y;
   const float* x = p.logits + (long long)row * p.vocab;
   const int begin = chunk * kAcceptChunk;
   const int end = min(begin + kAcceptChunk, p.vocab);
-  float bv = -INFINITY;
-  int bi = INT_MAX;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  float4 v[kVec];
+  const int n4 = (end - begin) >> 2;
   if (p.vec4) {
-    // 8192 floats = 2048 float4 = 8 per thread, all loads issued first
     const float4* x4 = reinterpret_cast<const float4*>(x + begin);
-    const int n4 = (end - begin) >> 2;
-    float4 v[kAcceptChunk / 4 / kAcceptThreads];
 #pragma unroll
-    for (int k = 0; k < kAcceptChunk / 4 / kAcceptThreads; ++k) {
+    for (int k = 0; k < kVec; ++k) {
       const int j = threadIdx.x + k * kAcceptThreads;
       v[k] = j < n4 ? __ldcs(x4 + j)
                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
 #pragma unroll
-    for (int k = 0; k < kAcceptChunk / 4 / kAcceptThreads; ++k) {
-      const int j = threadIdx.x + k * kAcceptThreads;
-      if (j < n4) {
-        const int i0 = begin + 4 * j;
-        take(v[k].x, i0, bv, bi);
-        take(v[k].y, i0 + 1, bv, bi);
-        take(v[k].z, i0 + 2, bv, bi);
-        take(v[k].w, i0 + 3, bv, bi);
-      }
-    }
+    for (int k = 0; k < kVec; ++k)
+      m = max_nan(max_nan(max_nan(m, v[k].x), max_nan(v[k].y, v[k].z)), v[k].w);
   } else {
     for (int i = begin + threadIdx.x; i < end; i += kAcceptThreads)
-      take(__ldcs(x + i), i, bv, bi);
+      m = max_nan(m, __ldcs(x + i));
   }
-  warp_argmax(bv, bi);
-  __shared__ float s_v[kAcceptThreads / 32];
-  __shared__ int s_i[kAcceptThreads / 32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    s_v[warp] = bv;
-    s_i[warp] = bi;
-  }
+  // chunk maximum
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    M = max_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_m[warp] = M;
   __syncthreads();
-  if (warp == 0) {
-    bv = lane < kAcceptThreads / 32 ? s_v[lane] : -INFINITY;
-    bi = lane < kAcceptThreads / 32 ? s_i[lane] : INT_MAX;
-    warp_argmax(bv, bi);
-    if (lane == 0) {
-      p.part_val[(long long)row * p.chunks + chunk] = bv;
-      p.part_idx[(long long)row * p.chunks + chunk] = bi;
+  M = s_m[0];
+#pragma unroll
+  for (int w = 1; w < kAcceptThreads / 32; ++w) M = max_nan(M, s_m[w]);
+  const bool nanM = M != M;
+  // first index of the maximum among this thread's logits
+  int cand = INT_MAX;
+  if (hits(m, M, nanM)) {
+    if (p.vec4) {
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) {
+        const int j = threadIdx.x + k * kAcceptThreads;
+        const int i0 = begin + 4 * j;
+        if (j < n4 && cand == INT_MAX) {
+          if (hits(v[k].x, M, nanM)) cand = i0;
+          else if (hits(v[k].y, M, nanM)) cand = i0 + 1;
+          else if (hits(v[k].z, M, nanM)) cand = i0 + 2;
+          else if (hits(v[k].w, M, nanM)) cand = i0 + 3;
+        }
+      }
+    } else {
+      for (int i = begin + threadIdx.x; i < end; i += kAcceptThreads)
+        if (hits(x[i], M, nanM)) {
+          cand = i;
+          break;
+        }
     }
+  }
+  cand = __reduce_min_sync(0xffffffffu, cand);
+  if (lane == 0) s_i[warp] = cand;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int best = s_i[0];
+#pragma unroll
+    for (int w = 1; w < kAcceptThreads / 32; ++w) best = min(best, s_i[w]);
+    p.part_val[(long long)row * p.chunks + chunk] = M;
+    p.part_idx[(long long)row * p.chunks + chunk] = best;
   }
 }
 
