@@ -46,8 +46,14 @@ KERNEL_LAUNCHES_PER_STEP = 4   # split, merge, argmax partial, accept finalize
 # ncu capture (profiles/verify_split_tc_*.md), keyed by workload and valid
 # only while the kernel's sources still hash to the recorded value.
 NCU_TRAFFIC = {
-    "b8_q8_p32k": {"source_hash": "e81d89c50fb61f96",
-                   "bytes_per_launch": 1077420000 + 4863232},
+    "b8_q8_p32k": {"source_hash": "4b8f0bf7281f90a3",
+                   "bytes_per_launch": 1077400000 + 5169664},
+    # captured on a smaller FP8 case (8 x 16K tokens, 276.9 MB algorithmic:
+    # 279.34 MB read + 4.11 MB written) and scaled to a full launch by the
+    # algorithmic bytes, which the traffic follows
+    "b32_q8_p1k128k_fp8": {"source_hash": "4b8f0bf7281f90a3",
+                           "per_algorithmic_byte": (279340288 + 4107264)
+                           / (8 * 16392 * 4 * 528)},
 }
 SPLIT_KERNEL_SOURCES = ("verify_attention_tc.cu", "common.cuh", "tc_ptx.cuh")
 
@@ -275,7 +281,9 @@ def run_gpu(args, w: wl.VerifyWorkload):
     traffic = None
     rec = NCU_TRAFFIC.get(w.name)
     if rec and rec.get("source_hash") == src_hash:
-        traffic = rec["bytes_per_launch"]
+        traffic = rec.get("bytes_per_launch")
+        if traffic is None:
+            traffic = int(rec["per_algorithmic_byte"] * kv_b)
     result = {
         "metric": METRIC,
         "value": round(ws_n * args.steps / (elapsed_ms / 1e3), 3),

@@ -197,7 +197,7 @@ __device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
     // row of this box's first token in the [num_pages * Hkv * page_size] view
     const long long row =
         ((long long)(page * p.hkv + pc.g) << p.log2_ps) + (t & (p.page_size - 1));
-    if (!kFp8) {
+    if constexpr (!kFp8) {
       const int st = gj % C::kStages;
       if (gj >= C::kStages)
         wait_bar(cx, &cx.bars->kv_empty[st], ((gj / C::kStages) - 1) & 1);
