@@ -141,6 +141,25 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks of the default process group (the value
+    itself when there is no group).  Timing uses the slowest rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or \
+            dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, elapsed_ms: float) -> float:
+    """Steps of the whole job per second: every rank runs `steps` steps of
+    its own replica, and the job takes as long as its slowest rank."""
+    return world * steps / (elapsed_ms / 1e3)
+
+
 def algorithmic_bytes(w: wl.VerifyWorkload, seq_lens):
     kv = wl.kv_bytes(seq_lens, w.num_kv_heads, w.head_dim, w.kv_dtype)
     logits = w.batch * w.q_len * w.vocab * 4
@@ -212,11 +231,7 @@ def run_gpu(args, w: wl.VerifyWorkload):
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
     attn_ms = [a.elapsed_time(b) for a, b in evs]
-    if ws_n > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     # end to end through the public API with host buffers: every step copies
     # its inputs from pinned host memory and reads its results back
@@ -261,12 +276,8 @@ def run_gpu(args, w: wl.VerifyWorkload):
         torch.cuda.synchronize(dev)
         barrier()
         e_ms = e0.elapsed_time(e1)
-        if ws_n > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(ws_n * args.steps / (e_ms / 1e3), 3),
+        e_ms = max_over_ranks(e_ms, dev)
+        e2e = {"value": round(job_throughput(ws_n, args.steps, e_ms), 3),
                "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h),
                "note": "KV pool resident in HBM (it is the cache state); "
@@ -286,7 +297,7 @@ def run_gpu(args, w: wl.VerifyWorkload):
             traffic = int(rec["per_algorithmic_byte"] * kv_b)
     result = {
         "metric": METRIC,
-        "value": round(ws_n * args.steps / (elapsed_ms / 1e3), 3),
+        "value": round(job_throughput(ws_n, args.steps, elapsed_ms), 3),
         "unit": UNIT,
         "n_gpus": ws_n,
         "steps": args.steps,
