@@ -12,7 +12,9 @@ The arithmetic lives in ``spec_oracle.c`` (plain C, float64, OpenMP over
 output rows only); this module compiles it with gcc and wraps it with
 ctypes.  Every function cites the passage it follows in the C file.
 
-Pins (see ``tests/test_oracle.py``): torch float64 scaled-dot-product
+Pins (see ``tests/test_oracle.py`` and ``tests/test_oracle_append.py``):
+the E4M3 / fp16 encoders against torch's float8_e4m3fn and numpy's float16
+conversions, torch float64 scaled-dot-product
 attention on gathered dense K/V, torch's float8_e4m3fn and numpy's float16
 decoders on every bit pattern, closed forms (identical keys, dominant key,
 two-key sigmoid), the invariants the pages fix (q_len=1 equals decode, row i
@@ -75,6 +77,12 @@ def _load():
         getattr(lib, name).restype = None
     lib.oracle_decode_e4m3.argtypes = [P, i64, P]
     lib.oracle_decode_e4m3.restype = None
+    for name in ("oracle_encode_fp16", "oracle_encode_e4m3"):
+        getattr(lib, name).argtypes = [P, i64, P]
+        getattr(lib, name).restype = None
+    lib.oracle_kv_append.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
+                                     P, P, P, P, P, P, P, P, P, P]
+    lib.oracle_kv_append.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -113,6 +121,54 @@ def decode_e4m3(bytes_) -> np.ndarray:
     out = np.empty(x.size, np.float64)
     _load().oracle_decode_e4m3(_ptr(x), x.size, _ptr(out))
     return out
+
+
+def encode_fp16(x) -> np.ndarray:
+    """float32 values -> fp16 bits, round-to-nearest-even."""
+    a = _c(x, np.float32).ravel()
+    out = np.empty(a.size, np.uint16)
+    _load().oracle_encode_fp16(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def encode_e4m3(x) -> np.ndarray:
+    """float32 values -> E4M3 bytes, round-to-nearest-even, saturated."""
+    a = _c(x, np.float32).ravel()
+    out = np.empty(a.size, np.uint8)
+    _load().oracle_encode_e4m3(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def kv_append(k_new_bits, v_new_bits, k_pages, v_pages, page_table, seq_lens,
+              *, k_scales=None, v_scales=None):
+    """Block KV append on copies of the pool.
+
+    k_new_bits, v_new_bits: uint16 bf16 bits [B, q_len, Hkv, D]; pools as in
+    verify_attention (uint8 + fp16-bit scales for FP8).  Returns
+    (k_pages, v_pages, k_scales, v_scales, positions, cache_loc) with the
+    pool arrays updated.
+    """
+    kn = _c(k_new_bits, np.uint16)
+    vn = _c(v_new_bits, np.uint16)
+    B, q_len, hkv, d = kn.shape
+    fp8 = k_scales is not None
+    kp = np.array(k_pages, dtype=np.uint8 if fp8 else np.uint16, copy=True)
+    vp = np.array(v_pages, dtype=np.uint8 if fp8 else np.uint16, copy=True)
+    ks = np.array(k_scales, dtype=np.uint16, copy=True) if fp8 else None
+    vs = np.array(v_scales, dtype=np.uint16, copy=True) if fp8 else None
+    num_pages, hkv2, page_size, _ = kp.shape
+    assert hkv2 == hkv
+    pt = _c(page_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    pos = np.zeros((B, q_len), np.int32)
+    loc = np.zeros((B, q_len), np.int64)
+    rc = _load().oracle_kv_append(
+        B, q_len, hkv, d, page_size, num_pages, pt.shape[1], int(fp8),
+        _ptr(kn), _ptr(vn), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(pt),
+        _ptr(sl), _ptr(pos), _ptr(loc))
+    if rc != ORACLE_OK:
+        raise ValueError(f"oracle_kv_append failed with code {rc}")
+    return kp, vp, ks, vs, pos, loc
 
 
 def verify_attention(q_bits, k_pages, v_pages, page_table, seq_lens, *,

@@ -304,6 +304,139 @@ void oracle_lse_merge(int32_t n_parts, int32_t d, const double* lse,
   *lse_out = total;
 }
 
+/* ---- encoders and block KV append ---------------------------------------------
+ *
+ * Quantise-on-write of the FP8 cache ("Qwen3.8-27B-FP8" page, "Implemented
+ * execution path": E4M3 with per-token / per-KV-head FP16 scales over
+ * 64-channel blocks).  The pages fix the format, not the rounding rule;
+ * the rule taken here (and stated in the C header of the library) is
+ *   amax  = max |x| over the 64-channel block, x the bf16 input as float
+ *   scale = fp16 round-to-nearest-even of (float)(amax / 448), computed as
+ *           an IEEE single-precision division; 1 if that rounds to zero
+ *   byte  = E4M3 round-to-nearest-even of (float)(x / scale), saturated to
+ *           +-448.
+ * Both encoders round an exactly known value once, from the definitions
+ * of the formats: fp16 has 10 fraction bits, exponent bias 15, subnormal
+ * quantum 2^-24; E4M3 has 3 fraction bits, bias 7, subnormal quantum 2^-9,
+ * largest finite 448. */
+
+uint16_t oracle_fp16_from_double(double x) {
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x);
+  if (isnan(x)) return 0x7E00;
+  if (a == 0.0) return sign;
+  double q;                 /* quantum at |x| */
+  int e;
+  frexp(a, &e);             /* a = m * 2^e, m in [0.5, 1) */
+  if (e - 1 < -14) q = ldexp(1.0, -24);
+  else q = ldexp(1.0, e - 1 - 10);
+  double r = rint(a / q) * q;   /* round half to even (default mode) */
+  if (r >= 65520.0 || isinf(a)) return sign | 0x7C00;  /* overflow: inf */
+  if (r < ldexp(1.0, -14)) return sign | (uint16_t)(r / ldexp(1.0, -24));
+  frexp(r, &e);
+  int E = e - 1;
+  uint16_t mant = (uint16_t)((r / ldexp(1.0, E) - 1.0) * 1024.0);
+  return sign | (uint16_t)((E + 15) << 10) | mant;
+}
+
+uint8_t oracle_e4m3_from_double(double x) {
+  uint8_t sign = signbit(x) ? 0x80 : 0;
+  double a = fabs(x);
+  if (isnan(x)) return 0x7F;
+  if (a >= 448.0) return sign | 0x7E;          /* saturate (inf included) */
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e);
+  double q = (e - 1 < -6) ? ldexp(1.0, -9) : ldexp(1.0, e - 1 - 3);
+  double r = rint(a / q) * q;
+  if (r >= 448.0) return sign | 0x7E;
+  if (r < ldexp(1.0, -6)) return sign | (uint8_t)(r / ldexp(1.0, -9));
+  frexp(r, &e);
+  int E = e - 1;
+  uint8_t mant = (uint8_t)((r / ldexp(1.0, E) - 1.0) * 8.0);
+  return sign | (uint8_t)((E + 7) << 3) | mant;
+}
+
+void oracle_encode_fp16(const float* x, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_fp16_from_double(x[i]);
+}
+void oracle_encode_e4m3(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_from_double(x[i]);
+}
+
+/*
+ * Block KV append.  Block row i of request b is token
+ * t = seq_lens[b] - q_len + i; its K and V rows of KV head g go to page
+ * page_table[b, t / page_size], slot t % page_size ("DFlash to dLLM
+ * self-spec, part 1", section 1.3.2 "KV over-allocation" and section 1.3.3:
+ * block ids, positions and cache loc prepared in one kernel).
+ *   k_new, v_new: bf16 bits [B, q_len, hkv, d]
+ *   pools / scales: updated in place (scales only when kv_fp8)
+ *   positions [B, q_len]: t, or -1 when t < 0
+ *   cache_loc [B, q_len]: page * page_size + slot, or -1 when the token has
+ *   no slot (t < 0, t beyond the table, page id outside the pool); such
+ *   rows are not written.
+ */
+int oracle_kv_append(int32_t batch, int32_t q_len, int32_t hkv, int32_t d,
+                     int32_t page_size, int32_t num_pages, int32_t max_pages,
+                     int32_t kv_fp8, const uint16_t* k_new,
+                     const uint16_t* v_new, void* k_pages, void* v_pages,
+                     uint16_t* k_scales, uint16_t* v_scales,
+                     const int32_t* page_table, const int32_t* seq_lens,
+                     int32_t* positions, int64_t* cache_loc) {
+  if (batch < 0 || q_len < 1 || hkv < 1 || d < 1 || page_size < 1 ||
+      (kv_fp8 && d % 64))
+    return ORACLE_ERR_ARG;
+  const int64_t max_tokens = (int64_t)max_pages * page_size;
+  for (int b = 0; b < batch; ++b) {
+    for (int i = 0; i < q_len; ++i) {
+      const int64_t t = (int64_t)seq_lens[b] - q_len + i;
+      int64_t loc = -1;
+      int32_t page = -1;
+      if (t >= 0 && t < max_tokens) {
+        page = page_table[(int64_t)b * max_pages + t / page_size];
+        if (page >= 0 && page < num_pages)
+          loc = (int64_t)page * page_size + t % page_size;
+      }
+      positions[(int64_t)b * q_len + i] = t >= 0 ? (int32_t)t : -1;
+      cache_loc[(int64_t)b * q_len + i] = loc;
+      if (loc < 0) continue;
+      for (int g = 0; g < hkv; ++g) {
+        const int64_t row = ((int64_t)page * hkv + g) * page_size + t % page_size;
+        const int64_t src = (((int64_t)b * q_len + i) * hkv + g) * d;
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint16_t* in = kv ? v_new : k_new;
+          if (!kv_fp8) {
+            uint16_t* dst = (uint16_t*)(kv ? v_pages : k_pages);
+            for (int c = 0; c < d; ++c) dst[row * d + c] = in[src + c];
+            continue;
+          }
+          uint8_t* dst = (uint8_t*)(kv ? v_pages : k_pages);
+          uint16_t* sc = kv ? v_scales : k_scales;
+          for (int blk = 0; blk < d / 64; ++blk) {
+            float amax = 0.0f;
+            for (int c = 0; c < 64; ++c) {
+              float x = (float)oracle_bf16_to_double(in[src + blk * 64 + c]);
+              if (fabsf(x) > amax) amax = fabsf(x);
+            }
+            float q = amax / 448.0f;            /* IEEE single division */
+            uint16_t sbits = oracle_fp16_from_double((double)q);
+            if ((sbits & 0x7FFF) == 0) sbits = 0x3C00;   /* 1.0 */
+            float s = (float)oracle_fp16_to_double(sbits);
+            sc[row * (d / 64) + blk] = sbits;
+            for (int c = 0; c < 64; ++c) {
+              float x = (float)oracle_bf16_to_double(in[src + blk * 64 + c]);
+              float y = x / s;                    /* IEEE single division */
+              dst[row * d + blk * 64 + c] = oracle_e4m3_from_double((double)y);
+            }
+          }
+        }
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
 /* ---- greedy acceptance ------------------------------------------------------ */
 
 /* argmax with the lowest index on ties; NaN ranks above every number and
