@@ -224,6 +224,50 @@ int spec_verify_attention_noalloc(const spec_attn_desc* desc, const void* q,
                                   const int32_t* seq_lens, float scale,
                                   void* out, void* stream);
 
+/*
+ * Append each request's verify block to its paged KV cache.
+ *
+ * Block row i of request b is token t = seq_lens[b] - q_len + i (seq_lens
+ * includes the block, as for spec_verify_attention); its K and V rows of
+ * every KV head go to page page_table[b, t / page_size], slot
+ * t % page_size.  The pages' serving stacks reserve those slots ahead of
+ * the verify pass and hand the kernels the block's positions and cache
+ * locations ("DFlash to dLLM self-spec, part 1", section 1.3.2 "KV
+ * over-allocation", and section 1.3.3: one kernel producing block ids,
+ * positions and cache loc); this call writes the rows and those two index
+ * arrays in one launch.
+ *
+ * bf16 pool (desc->kv_dtype == SPEC_KV_BF16): the rows are copied.
+ * FP8 pool: each 64-channel block of a row is quantised on write ("Qwen3.8-
+ * 27B-FP8" page, "Implemented execution path": E4M3 cache with per-token /
+ * per-KV-head FP16 scales over 64-channel blocks), with this library's rule
+ * (the pages fix only the format):
+ *   amax  = max |x| over the block (x the bf16 input, as fp32)
+ *   scale = fp16_rn(amax / 448), the division in fp32 round-to-nearest;
+ *           1 if that rounds to zero
+ *   byte  = E4M3 of fp32 x / scale, round-to-nearest-even, saturated to
+ *           +-448 (inputs must be finite)
+ *
+ *   k_new, v_new  bf16 [B, q_len, Hkv, D], 16-byte aligned
+ *   k_pages, v_pages, k_scales, v_scales  the pool, as in
+ *                 spec_verify_attention (scales only for FP8)
+ *   page_table, seq_lens  as in spec_verify_attention
+ *   positions     optional int32 [B, q_len]: t (or -1 where t < 0)
+ *   cache_loc     optional int64 [B, q_len]: page * page_size + slot, the
+ *                 flat token slot in the pool (or -1 where the token has no
+ *                 slot: t < 0, t beyond the table, or a page id outside the
+ *                 pool; such rows are not written, and SPEC_FLAG_CHECKED
+ *                 reports a bad page id through spec_verify_status on
+ *                 `workspace`)
+ *   workspace     only used with SPEC_FLAG_CHECKED (its status word);
+ *                 NULL otherwise
+ */
+int spec_kv_append(const spec_attn_desc* desc, const void* k_new,
+                   const void* v_new, void* k_pages, void* v_pages,
+                   void* k_scales, void* v_scales, const int32_t* page_table,
+                   const int32_t* seq_lens, int32_t* positions,
+                   int64_t* cache_loc, void* workspace, void* stream);
+
 /* Message for the last nonzero return on this thread ("" if none). */
 const char* spec_last_error(void);
 

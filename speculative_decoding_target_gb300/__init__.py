@@ -6,13 +6,14 @@ this package does not load the library; the first call does, and raises if
 it is missing.
 """
 from ._native import (SpecError, accept_workspace_size, alloc_workspace,
-                      desc_for, greedy_accept, greedy_accept_into, load,
+                      desc_for, greedy_accept, greedy_accept_into, kv_append,
+                      load,
                       make_desc, verify_attention, verify_attention_into,
                       verify_status, verify_workspace_size)
 
 __all__ = [
     "SpecError", "accept_workspace_size", "alloc_workspace", "desc_for",
-    "greedy_accept", "greedy_accept_into", "load", "make_desc",
+    "greedy_accept", "greedy_accept_into", "kv_append", "load", "make_desc",
     "verify_attention", "verify_attention_into", "verify_status",
     "verify_workspace_size",
 ]

@@ -32,6 +32,7 @@ EXPORTED = (
     "spec_verify_workspace_size", "spec_verify_attention",
     "spec_verify_status", "spec_accept_workspace_size", "spec_greedy_accept",
     "spec_last_error", "spec_version", "spec_verify_attention_noalloc",
+    "spec_kv_append",
 )
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
@@ -75,6 +76,9 @@ def load(path: str = LIB_PATH):
     lib.spec_verify_attention_noalloc.argtypes = [
         ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P, ctypes.c_float, P, P]
     lib.spec_verify_attention_noalloc.restype = ctypes.c_int
+    lib.spec_kv_append.argtypes = [ctypes.POINTER(AttnDesc), P, P, P, P, P,
+                                   P, P, P, P, P, P, P]
+    lib.spec_kv_append.restype = ctypes.c_int
     lib.spec_verify_status.argtypes = [P, ctypes.POINTER(u32), i32, P]
     lib.spec_verify_status.restype = ctypes.c_int
     lib.spec_accept_workspace_size.argtypes = [i32, i32]
@@ -181,6 +185,26 @@ def verify_attention_noalloc(q, k_pages, v_pages, page_table, seq_lens, *,
         _ptr(k_scales), _ptr(v_scales), _ptr(page_table), _ptr(seq_lens),
         float(scale), _ptr(out), _stream(stream)))
     return out
+
+
+def kv_append(k_new, v_new, k_pages, v_pages, page_table, seq_lens, *,
+              k_scales=None, v_scales=None, positions=None, cache_loc=None,
+              checked: bool = False, workspace=None, stream=None):
+    """Append the verify block's K/V (bf16 [B, q_len, Hkv, D]) to the paged
+    pool in place (quantised on write for an FP8 pool); fills the optional
+    positions (int32 [B, q_len]) and cache_loc (int64 [B, q_len])."""
+    B, q_len, hkv, d = k_new.shape
+    num_pages, hkv2, ps, _ = k_pages.shape
+    desc = make_desc(batch=B, q_len=q_len, num_q_heads=hkv, num_kv_heads=hkv,
+                     head_dim=d, page_size=ps, num_pages=num_pages,
+                     max_pages_per_seq=page_table.shape[1],
+                     kv_dtype="fp8" if k_pages.dtype == torch.uint8 else "bf16",
+                     checked=checked)
+    _check(load().spec_kv_append(
+        ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(k_pages),
+        _ptr(v_pages), _ptr(k_scales), _ptr(v_scales), _ptr(page_table),
+        _ptr(seq_lens), _ptr(positions), _ptr(cache_loc), _ptr(workspace),
+        _stream(stream)))
 
 
 def verify_status(workspace: torch.Tensor, clear: bool = True,

@@ -318,6 +318,68 @@ int spec_verify_status(const void* workspace, uint32_t* status_out,
   return SPEC_OK;
 }
 
+int spec_kv_append(const spec_attn_desc* desc, const void* k_new,
+                   const void* v_new, void* k_pages, void* v_pages,
+                   void* k_scales, void* v_scales, const int32_t* page_table,
+                   const int32_t* seq_lens, int32_t* positions,
+                   int64_t* cache_loc, void* workspace, void* stream) {
+  g_err[0] = 0;
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (desc->batch == 0) return SPEC_OK;
+  if (!k_new || !v_new || !k_pages || !v_pages || !page_table || !seq_lens)
+    return fail(SPEC_ERR_ARG, "NULL tensor pointer");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pages, 16) ||
+      !aligned(v_pages, 16))
+    return fail(SPEC_ERR_ALIGN, "k_new, v_new and the pools must be 16-byte aligned");
+  if (!aligned(page_table, 4) || !aligned(seq_lens, 4) ||
+      (positions && !aligned(positions, 4)) ||
+      (cache_loc && !aligned(cache_loc, 8)))
+    return fail(SPEC_ERR_ALIGN, "index arrays are misaligned");
+  const bool fp8 = desc->kv_dtype == SPEC_KV_FP8_E4M3;
+  if (fp8 && (!k_scales || !v_scales))
+    return fail(SPEC_ERR_ARG, "FP8 KV needs k_scales and v_scales");
+  if (fp8 && (!aligned(k_scales, 16) || !aligned(v_scales, 16)))
+    return fail(SPEC_ERR_ALIGN, "scales must be 16-byte aligned");
+  const bool checked = desc->flags & SPEC_FLAG_CHECKED;
+  if (checked && !workspace)
+    return fail(SPEC_ERR_WORKSPACE, "SPEC_FLAG_CHECKED needs a workspace");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  specv::AppendParams p;
+  std::memset(&p, 0, sizeof p);
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.k_pages = k_pages;
+  p.v_pages = v_pages;
+  p.k_scales = fp8 ? static_cast<__half*>(k_scales) : nullptr;
+  p.v_scales = fp8 ? static_cast<__half*>(v_scales) : nullptr;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.positions = positions;
+  p.cache_loc = cache_loc;
+  p.batch = desc->batch;
+  p.q_len = desc->q_len;
+  p.hkv = desc->num_kv_heads;
+  p.page_size = desc->page_size;
+  p.log2_ps = 0;
+  while ((1 << p.log2_ps) < desc->page_size) ++p.log2_ps;
+  p.num_pages = desc->num_pages;
+  p.max_pages = desc->max_pages_per_seq;
+  p.max_tokens = (long long)desc->max_pages_per_seq * desc->page_size;
+  p.fp8 = fp8;
+  cudaError_t e;
+  if (checked) {
+    p.status = static_cast<uint32_t*>(workspace);
+    e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess)
+      return fail(SPEC_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
+  }
+  e = specv::launch_kv_append(p, s);
+  if (e != cudaSuccess)
+    return fail(SPEC_ERR_CUDA, "append kernel launch: %s", cudaGetErrorString(e));
+  return SPEC_OK;
+}
+
 size_t spec_accept_workspace_size(int32_t rows, int32_t vocab) {
   if (rows < 0 || vocab < 1) {
     fail(SPEC_ERR_ARG, "rows %d / vocab %d", rows, vocab);

@@ -129,3 +129,23 @@ def test_accept_workspace_size_formula(lib):
     assert n >= 64 * chunks * 8
     assert n <= 64 * chunks * 8 + 3 * 256
     assert lib.spec_accept_workspace_size(-1, 10) == 0
+
+
+def test_kv_append_argument_checks(lib):
+    def call(desc, k_new=FAKE, ks=None, vs=None, pos=None, loc=None, ws=None):
+        return lib.spec_kv_append(
+            ctypes.byref(desc) if desc is not None else None, k_new, FAKE,
+            FAKE, FAKE, ks, vs, FAKE, FAKE, pos, loc, ws, None)
+
+    assert call(None) == _native.SPEC_ERR_ARG
+    assert call(_desc(batch=0), k_new=None) == _native.SPEC_OK
+    assert call(_desc(), k_new=None) == _native.SPEC_ERR_ARG
+    assert call(_desc(), k_new=ctypes.c_void_p(0x100008)) == \
+        _native.SPEC_ERR_ALIGN
+    assert call(_desc(), loc=ctypes.c_void_p(0x100004)) == \
+        _native.SPEC_ERR_ALIGN
+    assert call(_desc(kv_dtype="fp8")) == _native.SPEC_ERR_ARG
+    assert call(_desc(kv_dtype="fp8"), ks=FAKE,
+                vs=ctypes.c_void_p(0x100002)) == _native.SPEC_ERR_ALIGN
+    assert call(_desc(checked=True)) == _native.SPEC_ERR_WORKSPACE
+    assert call(_desc(page_size=24)) == _native.SPEC_ERR_ARG
