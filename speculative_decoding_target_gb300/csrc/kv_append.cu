@@ -12,6 +12,7 @@
 // per-token / per-KV-head FP16 scales over 64-channel blocks).
 #include <cuda_fp8.h>
 
+#include "append.cuh"
 #include "common.cuh"
 #include "spec_verify.h"
 

@@ -8,6 +8,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "append.cuh"
 #include "common.cuh"
 #include "spec_verify.h"
 
