@@ -50,8 +50,10 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    # no contraction into fused multiply-adds: the float32 steps the
+    # oracle states (quantisation, the width EWMA) are rounded one by one
     cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
-           "-Wall", "-o", tmp, _SRC, "-lm"]
+           "-ffp-contract=off", "-Wall", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -66,11 +68,12 @@ def _load():
     i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
     lib.oracle_verify_attention.argtypes = [
         i32, i32, i32, i32, i32, i32, i32, i32, i32,
-        P, P, P, P, P, P, P, f64, P, i64, i64, i64, P, P, i32]
+        P, P, P, P, P, P, P, P, f64, P, i64, i64, i64, P, P, i32]
     lib.oracle_verify_attention.restype = ctypes.c_int
     lib.oracle_lse_merge.argtypes = [i32, i32, P, P, P, P]
     lib.oracle_lse_merge.restype = None
-    lib.oracle_greedy_accept.argtypes = [P, P, i32, i32, i64, P, P, P, P, i32]
+    lib.oracle_greedy_accept.argtypes = [P, P, P, i32, i32, i64, P, P, P, P,
+                                         P, P, i32]
     lib.oracle_greedy_accept.restype = ctypes.c_int
     for name in ("oracle_decode_bf16", "oracle_decode_fp16"):
         getattr(lib, name).argtypes = [P, i64, P]
@@ -81,8 +84,13 @@ def _load():
         getattr(lib, name).argtypes = [P, i64, P]
         getattr(lib, name).restype = None
     lib.oracle_kv_append.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
-                                     P, P, P, P, P, P, P, P, P, P]
+                                     P, P, P, P, P, P, P, P, P, P, P]
     lib.oracle_kv_append.restype = ctypes.c_int
+    f32 = ctypes.c_float
+    lib.oracle_prepare_next_block.argtypes = [
+        i32, i32, i32, f32, f32, i32, P, P, P, P, P, i32, P, i32, i32, i32,
+        P, P, P, P, P]
+    lib.oracle_prepare_next_block.restype = ctypes.c_int64
     _lib = lib
     return lib
 
@@ -140,8 +148,9 @@ def encode_e4m3(x) -> np.ndarray:
 
 
 def kv_append(k_new_bits, v_new_bits, k_pages, v_pages, page_table, seq_lens,
-              *, k_scales=None, v_scales=None):
-    """Block KV append on copies of the pool.
+              *, k_scales=None, v_scales=None, q_lens=None):
+    """Block KV append on copies of the pool (q_lens: optional int32 [B] rows
+    per request of a block padded to q_len).
 
     k_new_bits, v_new_bits: uint16 bf16 bits [B, q_len, Hkv, D]; pools as in
     verify_attention (uint8 + fp16-bit scales for FP8).  Returns
@@ -160,12 +169,13 @@ def kv_append(k_new_bits, v_new_bits, k_pages, v_pages, page_table, seq_lens,
     assert hkv2 == hkv
     pt = _c(page_table, np.int32)
     sl = _c(seq_lens, np.int32)
+    ql = None if q_lens is None else _c(q_lens, np.int32)
     pos = np.zeros((B, q_len), np.int32)
     loc = np.zeros((B, q_len), np.int64)
     rc = _load().oracle_kv_append(
         B, q_len, hkv, d, page_size, num_pages, pt.shape[1], int(fp8),
         _ptr(kn), _ptr(vn), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(pt),
-        _ptr(sl), _ptr(pos), _ptr(loc))
+        _ptr(sl), _ptr(ql), _ptr(pos), _ptr(loc))
     if rc != ORACLE_OK:
         raise ValueError(f"oracle_kv_append failed with code {rc}")
     return kp, vp, ks, vs, pos, loc
@@ -175,7 +185,7 @@ def verify_attention(q_bits, k_pages, v_pages, page_table, seq_lens, *,
                      num_kv_heads: int, scale: float, k_scales=None,
                      v_scales=None, rows=None, key_begin: int = 0,
                      key_end: int = -1, threads: int = 0,
-                     return_lse: bool = False):
+                     return_lse: bool = False, q_lens=None):
     """Verify attention in float64.
 
     q_bits:   uint16 bf16 bits [B, q_len, Hq, D]
@@ -184,6 +194,8 @@ def verify_attention(q_bits, k_pages, v_pages, page_table, seq_lens, *,
     k_scales, v_scales: uint16 fp16 bits [num_pages, Hkv, page_size, D/64]
     page_table: int32 [B, max_pages];  seq_lens: int32 [B] (block included)
     rows:     optional flat row ids (b*q_len + i)*Hq + h; default every row.
+    q_lens:   optional int32 [B] rows per request (block padded to q_len);
+              rows i >= q_lens[b] are zero.
     Returns out float64 [n_rows, D] (and lse [n_rows] if requested).
     """
     q = _c(q_bits, np.uint16)
@@ -199,6 +211,8 @@ def verify_attention(q_bits, k_pages, v_pages, page_table, seq_lens, *,
     pt = _c(page_table, np.int32)
     sl = _c(seq_lens, np.int32)
     assert pt.ndim == 2 and pt.shape[0] == B and sl.shape == (B,)
+    ql = None if q_lens is None else _c(q_lens, np.int32)
+    assert ql is None or ql.shape == (B,)
     r = None if rows is None else _c(rows, np.int64).ravel()
     n = B * q_len * hq if r is None else r.size
     out = np.zeros((n, d), np.float64)
@@ -206,7 +220,7 @@ def verify_attention(q_bits, k_pages, v_pages, page_table, seq_lens, *,
     rc = _load().oracle_verify_attention(
         B, q_len, hq, hkv, d, page_size, num_pages, pt.shape[1], int(fp8),
         _ptr(q), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(pt), _ptr(sl),
-        float(scale), _ptr(r), n, int(key_begin), int(key_end), _ptr(out),
+        _ptr(ql), float(scale), _ptr(r), n, int(key_begin), int(key_end), _ptr(out),
         _ptr(lse), int(threads or default_threads()))
     if rc != ORACLE_OK:
         raise ValueError(f"oracle_verify_attention failed with code {rc}")
@@ -225,11 +239,13 @@ def lse_merge(lse_parts, o_parts):
     return out, float(lse_out[0])
 
 
-def greedy_accept(logits, draft_ids, *, threads: int = 0):
-    """Greedy acceptance.  logits fp32 [B*q_len, V]; draft_ids int32 [B, q_len].
+def greedy_accept(logits, draft_ids, *, q_lens=None, seq_lens=None,
+                  threads: int = 0):
+    """Greedy acceptance.  logits fp32 [B*q_len, V]; draft_ids int32 [B, q_len];
+    q_lens optional int32 [B] rows per request; seq_lens optional int32 [B].
 
     Returns dict with accept_len [B], next_token [B], out_tokens [B, q_len],
-    argmax [B*q_len].
+    argmax [B*q_len] and, when seq_lens is given, new_seq_lens [B].
     """
     lg = _c(logits, np.float32)
     dr = _c(draft_ids, np.int32)
@@ -240,10 +256,57 @@ def greedy_accept(logits, draft_ids, *, threads: int = 0):
     nxt = np.zeros(B, np.int32)
     toks = np.zeros((B, q_len), np.int32)
     am = np.zeros(B * q_len, np.int32)
+    ql = None if q_lens is None else _c(q_lens, np.int32)
+    sl = None if seq_lens is None else _c(seq_lens, np.int32)
+    nsl = None if sl is None else np.zeros(B, np.int32)
     rc = _load().oracle_greedy_accept(
-        _ptr(lg), _ptr(dr), B, q_len, vocab, _ptr(acc), _ptr(nxt), _ptr(toks),
-        _ptr(am), int(threads or default_threads()))
+        _ptr(lg), _ptr(dr), _ptr(ql), B, q_len, vocab, _ptr(sl), _ptr(nsl),
+        _ptr(acc), _ptr(nxt), _ptr(toks), _ptr(am),
+        int(threads or default_threads()))
     if rc != ORACLE_OK:
         raise ValueError(f"oracle_greedy_accept failed with code {rc}")
-    return {"accept_len": acc, "next_token": nxt, "out_tokens": toks,
-            "argmax": am}
+    res = {"accept_len": acc, "next_token": nxt, "out_tokens": toks,
+           "argmax": am}
+    if nsl is not None:
+        res["new_seq_lens"] = nsl
+    return res
+
+
+WIDTH_POLICIES = {"fixed": 0, "ewma": 1, "doubling": 2}
+
+
+def prepare_next_block(policy: str, q_max: int, q_lens, accept_len,
+                       next_token, new_seq_lens, state, page_table, *,
+                       page_size: int, num_pages: int, mask_id: int = 0,
+                       min_width: int = 2, alpha: float = 0.5,
+                       offset: float = 1.5):
+    """Next verify width per request and the next block's layout.
+
+    state: float32 [B] policy state (EWMA value or K), updated on a copy.
+    Returns dict with next_q_lens, next_seq_lens [B]; block_ids, positions
+    [B, q_max] int32; cache_loc [B, q_max] int64; state [B]; missing (rows
+    without a reserved slot).
+    """
+    ql = _c(q_lens, np.int32)
+    B = ql.shape[0]
+    acc = _c(accept_len, np.int32)
+    nxt = _c(next_token, np.int32)
+    nsl = _c(new_seq_lens, np.int32)
+    st = np.array(state, dtype=np.float32, copy=True)
+    pt = _c(page_table, np.int32)
+    out = {"next_q_lens": np.zeros(B, np.int32),
+           "next_seq_lens": np.zeros(B, np.int32),
+           "block_ids": np.zeros((B, q_max), np.int32),
+           "positions": np.zeros((B, q_max), np.int32),
+           "cache_loc": np.zeros((B, q_max), np.int64)}
+    n = _load().oracle_prepare_next_block(
+        WIDTH_POLICIES[policy], q_max, min_width, float(alpha), float(offset),
+        B, _ptr(ql), _ptr(acc), _ptr(nxt), _ptr(nsl), _ptr(st), mask_id,
+        _ptr(pt), pt.shape[1], page_size, num_pages, _ptr(out["next_q_lens"]),
+        _ptr(out["next_seq_lens"]), _ptr(out["block_ids"]),
+        _ptr(out["positions"]), _ptr(out["cache_loc"]))
+    if n < 0:
+        raise ValueError(f"oracle_prepare_next_block failed with code {n}")
+    out["state"] = st
+    out["missing"] = int(n)
+    return out

@@ -49,6 +49,21 @@
  *     +0.  accept a = number of leading j = 1..k with draft[j] == t[j-1];
  *     next = t[a].
  *
+ *  5. Per-request verify width ("Qwen3.8-27B-FP8" page: adaptive MTP K and
+ *     the EWMA-driven DFlash2 verify width; "DFlash to dLLM self-spec,
+ *     part 1", section 1.7.2: the verify length becomes a per-request
+ *     scheduling decision).  Request b verifies q_b <= q_max rows in a block
+ *     padded to q_max; block row i < q_b is token seq_len - q_b + i, rows
+ *     i >= q_b do not exist (zero output, nothing appended or compared).
+ *
+ *  6. Commit and next-block preparation ("DFlash to dLLM self-spec,
+ *     part 1", section 1.3.3: one kernel computes accept, bonus and the new
+ *     sequence lengths, another the next block's ids, positions and cache
+ *     locations; section 1.3.2: the GPU-side lengths advance without a copy
+ *     to the host).  After accepting a drafts the cache holds the prefix,
+ *     the boundary and d1..da: new_seq_len = seq_len - q_b + a + 1.  The
+ *     bonus token opens the next block at position new_seq_len.
+ *
  * Parity of this oracle against any engine on the pages is unpinned: the
  * pages print no output for a concrete input tensor.  It is pinned instead
  * by tests against library routines (torch scaled-dot-product attention in
@@ -124,7 +139,15 @@ typedef struct {
   const uint16_t* v_scales;
   const int32_t* page_table; /* [batch, max_pages] */
   const int32_t* seq_lens;   /* [batch], block included */
+  const int32_t* q_lens;     /* [batch] rows per request, or NULL: q_len */
 } oracle_attn_problem;
+
+/* Rows of request b's block: q_lens[b] clamped to [0, q_max], or q_max. */
+static int32_t block_rows(const int32_t* q_lens, int b, int32_t q_max) {
+  if (!q_lens) return q_max;
+  int32_t v = q_lens[b];
+  return v < 0 ? 0 : (v > q_max ? q_max : v);
+}
 
 /* Element c of the cached K (or V) row of token t of request b, KV head g.
  * Returns 0 and writes the row, or ORACLE_ERR_PAGE for a page id outside the
@@ -160,7 +183,8 @@ static int attention_row(const oracle_attn_problem* p, int b, int i, int h,
   const int d = p->d;
   const int group = p->hq / p->hkv;
   const int g = h / group;
-  const int64_t causal = (int64_t)p->seq_lens[b] - p->q_len + i + 1;
+  const int32_t qb = block_rows(p->q_lens, b, p->q_len);
+  const int64_t causal = i < qb ? (int64_t)p->seq_lens[b] - qb + i + 1 : 0;
   int64_t lo = key_begin > 0 ? key_begin : 0;
   int64_t hi = causal;
   if (key_end >= 0 && key_end < hi) hi = key_end;
@@ -216,7 +240,8 @@ int oracle_verify_attention(int32_t batch, int32_t q_len, int32_t hq,
                             const void* k_pages, const void* v_pages,
                             const uint16_t* k_scales, const uint16_t* v_scales,
                             const int32_t* page_table, const int32_t* seq_lens,
-                            double scale, const int64_t* rows, int64_t n_rows,
+                            const int32_t* q_lens, double scale,
+                            const int64_t* rows, int64_t n_rows,
                             int64_t key_begin, int64_t key_end, double* out,
                             double* lse, int32_t nthreads) {
   if (batch < 0 || q_len < 1 || hq < 1 || hkv < 1 || hq % hkv || d < 1 ||
@@ -226,7 +251,7 @@ int oracle_verify_attention(int32_t batch, int32_t q_len, int32_t hq,
   oracle_attn_problem p = {batch,   q_len,     hq,       hkv,      d,
                            page_size, num_pages, max_pages, kv_fp8, q,
                            k_pages, v_pages,   k_scales, v_scales, page_table,
-                           seq_lens};
+                           seq_lens, q_lens};
   const int64_t total = (int64_t)batch * q_len * hq;
   if (!rows) n_rows = total;
   int64_t max_len = 0;
@@ -365,17 +390,17 @@ void oracle_encode_e4m3(const float* x, int64_t n, uint8_t* out) {
 }
 
 /*
- * Block KV append.  Block row i of request b is token
- * t = seq_lens[b] - q_len + i; its K and V rows of KV head g go to page
+ * Block KV append.  Block row i < q_b of request b (q_b = q_lens[b], or
+ * q_len when q_lens is NULL) is token t = seq_lens[b] - q_b + i; its K and V rows of KV head g go to page
  * page_table[b, t / page_size], slot t % page_size ("DFlash to dLLM
  * self-spec, part 1", section 1.3.2 "KV over-allocation" and section 1.3.3:
  * block ids, positions and cache loc prepared in one kernel).
  *   k_new, v_new: bf16 bits [B, q_len, hkv, d]
  *   pools / scales: updated in place (scales only when kv_fp8)
- *   positions [B, q_len]: t, or -1 when t < 0
+ *   positions [B, q_len]: t, or -1 when t < 0 or i >= q_b
  *   cache_loc [B, q_len]: page * page_size + slot, or -1 when the token has
- *   no slot (t < 0, t beyond the table, page id outside the pool); such
- *   rows are not written.
+ *   no slot (i >= q_b, t < 0, t beyond the table, page id outside the
+ *   pool); such rows are not written.
  */
 int oracle_kv_append(int32_t batch, int32_t q_len, int32_t hkv, int32_t d,
                      int32_t page_size, int32_t num_pages, int32_t max_pages,
@@ -383,16 +408,23 @@ int oracle_kv_append(int32_t batch, int32_t q_len, int32_t hkv, int32_t d,
                      const uint16_t* v_new, void* k_pages, void* v_pages,
                      uint16_t* k_scales, uint16_t* v_scales,
                      const int32_t* page_table, const int32_t* seq_lens,
-                     int32_t* positions, int64_t* cache_loc) {
+                     const int32_t* q_lens, int32_t* positions,
+                     int64_t* cache_loc) {
   if (batch < 0 || q_len < 1 || hkv < 1 || d < 1 || page_size < 1 ||
       (kv_fp8 && d % 64))
     return ORACLE_ERR_ARG;
   const int64_t max_tokens = (int64_t)max_pages * page_size;
   for (int b = 0; b < batch; ++b) {
+    const int32_t qb = block_rows(q_lens, b, q_len);
     for (int i = 0; i < q_len; ++i) {
-      const int64_t t = (int64_t)seq_lens[b] - q_len + i;
+      const int64_t t = (int64_t)seq_lens[b] - qb + i;
       int64_t loc = -1;
       int32_t page = -1;
+      if (i >= qb) {
+        positions[(int64_t)b * q_len + i] = -1;
+        cache_loc[(int64_t)b * q_len + i] = -1;
+        continue;
+      }
       if (t >= 0 && t < max_tokens) {
         page = page_table[(int64_t)b * max_pages + t / page_size];
         if (page >= 0 && page < num_pages)
@@ -461,14 +493,21 @@ static int64_t row_argmax(const float* x, int64_t n) {
  *         block position j.
  * draft_ids: [batch, q_len]; column 0 is the boundary token (not compared),
  *         columns 1..q_len-1 are the drafts d1..dk.
+ * q_lens: [batch] rows per request (NULL: q_len); only rows j < q_b and
+ *         drafts 1..q_b-1 take part.  A request with q_b = 0 is idle:
+ *         accept 0, next -1, nothing committed.
  * accept_len/next_token: [batch].  out_tokens [batch, q_len] (optional):
  *         d1..da, then next, then -1.  argmax_rows [batch * q_len] (optional).
+ * seq_lens -> new_seq_lens (both optional, [batch]): seq_len - q_b + a + 1,
+ *         the cache length once the boundary and d1..da are committed
+ *         (seq_len for an idle request).
  */
 int oracle_greedy_accept(const float* logits, const int32_t* draft_ids,
-                         int32_t batch, int32_t q_len, int64_t vocab,
-                         int32_t* accept_len, int32_t* next_token,
-                         int32_t* out_tokens, int32_t* argmax_rows,
-                         int32_t nthreads) {
+                         const int32_t* q_lens, int32_t batch, int32_t q_len,
+                         int64_t vocab, const int32_t* seq_lens,
+                         int32_t* new_seq_lens, int32_t* accept_len,
+                         int32_t* next_token, int32_t* out_tokens,
+                         int32_t* argmax_rows, int32_t nthreads) {
   if (batch < 0 || q_len < 1 || vocab < 1) return ORACLE_ERR_ARG;
   const int64_t rows = (int64_t)batch * q_len;
   int32_t* t = (int32_t*)malloc(sizeof(int32_t) * (size_t)(rows ? rows : 1));
@@ -482,18 +521,125 @@ int oracle_greedy_accept(const float* logits, const int32_t* draft_ids,
   for (int b = 0; b < batch; ++b) {
     const int32_t* dr = draft_ids + (int64_t)b * q_len;
     const int32_t* tb = t + (int64_t)b * q_len;
+    const int32_t qb = block_rows(q_lens, b, q_len);
+    int32_t* ot = out_tokens ? out_tokens + (int64_t)b * q_len : NULL;
+    if (ot)
+      for (int j = 0; j < q_len; ++j) ot[j] = -1;
+    if (qb == 0) {
+      accept_len[b] = 0;
+      next_token[b] = -1;
+      if (new_seq_lens) new_seq_lens[b] = seq_lens[b];
+      continue;
+    }
     int a = 0;
-    while (a + 1 < q_len && dr[a + 1] == tb[a]) ++a;
+    while (a + 1 < qb && dr[a + 1] == tb[a]) ++a;
     accept_len[b] = a;
     next_token[b] = tb[a];
-    if (out_tokens) {
-      int32_t* ot = out_tokens + (int64_t)b * q_len;
-      for (int j = 0; j < q_len; ++j) ot[j] = -1;
+    if (ot) {
       for (int j = 0; j < a; ++j) ot[j] = dr[j + 1];
       ot[a] = tb[a];
     }
+    if (new_seq_lens) new_seq_lens[b] = seq_lens[b] - qb + a + 1;
   }
   if (argmax_rows) memcpy(argmax_rows, t, sizeof(int32_t) * (size_t)rows);
   free(t);
   return ORACLE_OK;
+}
+
+/* ---- verify width policy and next-block preparation ------------------------ */
+
+#define ORACLE_WIDTH_FIXED 0
+#define ORACLE_WIDTH_EWMA 1
+#define ORACLE_WIDTH_DOUBLING 2
+
+/*
+ * After a verify step: choose each request's next width and lay out its next
+ * block.  For request b with q_b rows this step and a accepted drafts:
+ *
+ *   FIXED:    w = q_max.
+ *   EWMA      ("Qwen3.8-27B-FP8" page, DFlash2 adaptive width: an EWMA of
+ *             the accepted count, verify ewma + 1.5 rows, floor of two):
+ *             e <- (1 - alpha) * e + alpha * a, each operation rounded to
+ *             float32, no fused multiply-add; w = ceil(e + offset) clamped
+ *             to [min_width, q_max].  state[b] holds e.
+ *   DOUBLING  ("Qwen3.8-27B-FP8" page, adaptive MTP K: start at K = 1,
+ *             double after full acceptance, back off after rejection):
+ *             K <- 2K if a == q_b - 1 else K / 2 (integer halving), clamped
+ *             to [1, max(1, q_max - 1)]; w = min(K + 1, q_max).  state[b]
+ *             holds K.
+ *
+ * An idle request (q_b = 0) keeps its state and stays idle (w = 0).
+ * The next block of an active request starts at p = new_seq_lens[b]:
+ *   next_q_lens[b] = w, next_seq_lens[b] = p + w,
+ *   block_ids[b, :] = [next_token, mask_id x (w - 1), -1 ...],
+ *   positions[b, i] = p + i (i < w, else -1),
+ *   cache_loc[b, i] = page_table[b, (p+i)/ps] * ps + (p+i) % ps, or -1 when
+ *   i >= w or the slot is not reserved (past the table, page id outside the
+ *   pool).  Returns the number of rows i < w without a reserved slot.
+ */
+int64_t oracle_prepare_next_block(
+    int32_t policy, int32_t q_max, int32_t min_width, float alpha,
+    float offset, int32_t batch, const int32_t* q_lens,
+    const int32_t* accept_len, const int32_t* next_token,
+    const int32_t* new_seq_lens, float* state, int32_t mask_id,
+    const int32_t* page_table, int32_t max_pages, int32_t page_size,
+    int32_t num_pages, int32_t* next_q_lens, int32_t* next_seq_lens,
+    int32_t* block_ids, int32_t* positions, int64_t* cache_loc) {
+  if (batch < 0 || q_max < 1 || page_size < 1 || policy < 0 || policy > 2)
+    return ORACLE_ERR_ARG;
+  int64_t missing = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int32_t qb = block_rows(q_lens, b, q_max);
+    const int32_t a = accept_len[b];
+    int32_t w = 0;
+    if (qb > 0) {
+      if (policy == ORACLE_WIDTH_FIXED) {
+        w = q_max;
+      } else if (policy == ORACLE_WIDTH_EWMA) {
+        const float keep = 1.0f - alpha;
+        const float old_part = keep * state[b];
+        const float new_part = alpha * (float)a;
+        const float e = old_part + new_part;
+        state[b] = e;
+        const float wf = ceilf(e + offset);
+        if (!(wf < (float)q_max)) w = q_max;   /* also NaN */
+        else if (wf < (float)min_width) w = min_width;
+        else w = (int32_t)wf;
+        if (w > q_max) w = q_max;
+        if (w < 1) w = 1;
+      } else {
+        const int32_t kmax = q_max - 1 > 1 ? q_max - 1 : 1;
+        int32_t k = (int32_t)state[b];
+        k = a == qb - 1 ? 2 * k : k / 2;
+        if (k < 1) k = 1;
+        if (k > kmax) k = kmax;
+        state[b] = (float)k;
+        w = k + 1 < q_max ? k + 1 : q_max;
+      }
+    }
+    const int64_t pos0 = new_seq_lens[b];
+    next_q_lens[b] = w;
+    next_seq_lens[b] = (int32_t)(pos0 + w);
+    for (int i = 0; i < q_max; ++i) {
+      const int64_t o = (int64_t)b * q_max + i;
+      if (i >= w) {
+        block_ids[o] = -1;
+        positions[o] = -1;
+        cache_loc[o] = -1;
+        continue;
+      }
+      const int64_t t = pos0 + i;
+      block_ids[o] = i == 0 ? next_token[b] : mask_id;
+      positions[o] = (int32_t)t;
+      int64_t loc = -1;
+      if (t >= 0 && t / page_size < max_pages) {
+        const int32_t page = page_table[(int64_t)b * max_pages + t / page_size];
+        if (page >= 0 && page < num_pages)
+          loc = (int64_t)page * page_size + t % page_size;
+      }
+      cache_loc[o] = loc;
+      if (loc < 0) ++missing;
+    }
+  }
+  return missing;
 }
