@@ -51,6 +51,8 @@ extern "C" {
 #define SPEC_STATUS_BAD_PAGE 1u   /* a page id outside [0, num_pages) */
 #define SPEC_STATUS_TIMEOUT 2u    /* a kernel wait ran past its bound (a bug,
                                      not a data condition); output invalid */
+#define SPEC_STATUS_NO_SLOT 4u    /* spec_prepare_next_block: a next-block
+                                     row has no reserved cache slot */
 
 typedef enum {
   SPEC_KV_BF16 = 0,     /* K/V elements are bf16 */
@@ -74,12 +76,24 @@ typedef enum {
  *   max_pages_per_seq  columns of page_table
  *   kv_dtype         spec_kv_dtype
  *   flags            SPEC_FLAG_* bits
+ *   q_lens           optional DEVICE pointer, int32 [B], 4-byte aligned:
+ *                    the rows request b verifies this step, its block
+ *                    padded to q_len rows ("Qwen3.8-27B-FP8" page: adaptive
+ *                    MTP K and the EWMA-driven DFlash2 verify width; "DFlash
+ *                    to dLLM self-spec, part 1", section 1.7.2: the verify
+ *                    length as a per-request scheduling decision).  Values
+ *                    are clamped to [0, q_len].  Block row i < q_lens[b] is
+ *                    token seq_lens[b] - q_lens[b] + i; rows past q_lens[b]
+ *                    are never read, output zeros and are not appended.
+ *                    NULL: every request verifies q_len rows.  Read on the
+ *                    device, so it may change between graph replays.
  */
 typedef struct {
   int32_t batch, q_len, num_q_heads, num_kv_heads, head_dim;
   int32_t page_size, num_pages, max_pages_per_seq;
   int32_t kv_dtype;
   uint32_t flags;
+  const int32_t* q_lens;
 } spec_attn_desc;
 
 /*
@@ -106,7 +120,9 @@ size_t spec_verify_workspace_size(const spec_attn_desc* desc);
  * 1.1: verify is a short causal extend over the existing prefix KV).
  *
  *   out[b,i,h,:] = sum_t softmax_t(scale * <q[b,i,h,:], K[b,t,g,:]>) V[b,t,g,:]
- *   over t < seq_lens[b] - q_len + i + 1, g = h / (Hq/Hkv).
+ *   over t < seq_lens[b] - q_b + i + 1, g = h / (Hq/Hkv), for block rows
+ *   i < q_b (q_b = desc->q_lens[b] when given, else q_len); rows i >= q_b
+ *   output zeros.
  *
  * Token t of request b lives in page page_table[b, t / page_size], slot
  * t % page_size.  Pool layout [num_pages, Hkv, page_size, D] (a page holds a
@@ -192,6 +208,113 @@ int spec_greedy_accept(const float* logits, const int32_t* draft_ids,
                        size_t workspace_bytes, void* stream);
 
 /*
+ * Greedy acceptance with per-request block widths and the cache length
+ * after the commit, in the same two launches as spec_greedy_accept ("DFlash
+ * to dLLM self-spec, part 1", section 1.3.3: accept, bonus and new sequence
+ * lengths from one kernel; section 1.3.2: the GPU-side lengths advance
+ * without a copy to the host).
+ *
+ * Arguments as spec_greedy_accept, with q_len the padded block width, plus:
+ *   q_lens       optional int32 [batch]: rows request b verified, clamped
+ *                to [0, q_len] (NULL: q_len).  Only rows j < q_b are read
+ *                from `logits` (rows past it are skipped unread) and only
+ *                drafts 1..q_b-1 are compared, so accept_len <= q_b - 1.
+ *                A request with q_b = 0 is idle: accept_len 0, next_token
+ *                -1, out_tokens all -1, new_seq_len = seq_len.
+ *   seq_lens     optional int32 [batch]: cache lengths of this verify step,
+ *                block included (as for spec_verify_attention)
+ *   new_seq_lens optional int32 [batch], given together with seq_lens:
+ *                seq_len - q_b + accept_len + 1, the cache length once the
+ *                boundary token and d1..da are committed.  The bonus token
+ *                is not in the cache yet: it opens the next block at that
+ *                position.
+ * All pointers are device pointers; nothing is copied to the host.
+ */
+int spec_greedy_accept_commit(const float* logits, const int32_t* draft_ids,
+                              const int32_t* q_lens, int32_t batch,
+                              int32_t q_len, int32_t vocab,
+                              const int32_t* seq_lens, int32_t* new_seq_lens,
+                              int32_t* accept_len, int32_t* next_token,
+                              int32_t* out_tokens, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Verify width policies (spec_width_policy.policy). */
+#define SPEC_WIDTH_FIXED 0     /* always q_max rows */
+#define SPEC_WIDTH_EWMA 1      /* EWMA of the accepted count + offset */
+#define SPEC_WIDTH_DOUBLING 2  /* K doubles on full acceptance, else halves */
+
+/*
+ * How spec_prepare_next_block picks each request's next verify width w
+ * (rows, boundary included) from the accept count a of a block of q_b rows:
+ *
+ *   SPEC_WIDTH_FIXED     w = q_max.
+ *   SPEC_WIDTH_EWMA      ("Qwen3.8-27B-FP8" page: DFlash2 adaptive width
+ *                        tracks an EWMA of the accepted count and verifies
+ *                        ewma + 1.5 rows with a floor of two)
+ *                        e = (1 - alpha) * e + alpha * a, every operation
+ *                        rounded to float32 (no fused multiply-add);
+ *                        w = ceil(e + offset) clamped to [min_width, q_max].
+ *                        state[b] holds e; start it at q_max - 1 for a full
+ *                        first block.  Rounding up lets a fully accepted
+ *                        narrow block grow again.
+ *   SPEC_WIDTH_DOUBLING  ("Qwen3.8-27B-FP8" page: adaptive MTP starts at
+ *                        K = 1, doubles K after full acceptance and backs
+ *                        off after rejection)
+ *                        K = 2K if a == q_b - 1 else K / 2 (integer),
+ *                        clamped to [1, max(1, q_max - 1)]; w = min(K + 1,
+ *                        q_max).  state[b] holds K as a float; start it at 1.
+ */
+typedef struct {
+  int32_t policy;     /* SPEC_WIDTH_* */
+  int32_t q_max;      /* padded block width, 1..16 */
+  int32_t min_width;  /* EWMA floor, 1..q_max (2 on the page) */
+  int32_t mask_id;    /* token id written into the next block's draft rows */
+  float alpha;        /* EWMA weight of the newest accept count, in [0, 1] */
+  float offset;       /* EWMA rows beyond the average (1.5 on the page) */
+} spec_width_policy;
+
+/*
+ * After spec_greedy_accept_commit: the next verify width of every request
+ * and its next block's layout, on the device ("DFlash to dLLM self-spec,
+ * part 1", section 1.3.3: block ids, positions and cache loc from one
+ * kernel; section 1.3.2: slots reserved ahead by KV over-allocation).
+ *
+ *   pol          host pointer to the policy
+ *   q_lens       optional int32 [B]: rows verified this step (NULL: q_max)
+ *   accept_len, next_token, new_seq_lens  int32 [B], as produced by
+ *                spec_greedy_accept_commit
+ *   state        float [B], read and updated (EWMA value or K); may be NULL
+ *                for SPEC_WIDTH_FIXED
+ *   page_table   int32 [B, max_pages_per_seq]: the request's reserved pages
+ *   next_q_lens  int32 [B] out: w (0 for an idle request, q_b = 0)
+ *   next_seq_lens int32 [B] out: new_seq_len + w, the seq_lens of the next
+ *                verify step
+ *   block_ids    optional int32 [B, q_max] out: [next_token, mask_id x
+ *                (w - 1), -1 ...]
+ *   positions    optional int32 [B, q_max] out: new_seq_len + i for i < w,
+ *                else -1
+ *   cache_loc    optional int64 [B, q_max] out: page * page_size + slot of
+ *                position new_seq_len + i, or -1 for i >= w and for a slot
+ *                that is not reserved (past the table, page id outside the
+ *                pool)
+ *   status       optional device uint32: SPEC_STATUS_NO_SLOT is OR-ed in
+ *                when a row i < w has no reserved slot (never cleared here;
+ *                read it with spec_verify_status)
+ * int32 / float buffers 4-byte aligned, cache_loc 8-byte aligned.  Host
+ * checks return SPEC_ERR_ARG / SPEC_ERR_ALIGN before anything is enqueued.
+ */
+int spec_prepare_next_block(const spec_width_policy* pol, int32_t batch,
+                            const int32_t* q_lens, const int32_t* accept_len,
+                            const int32_t* next_token,
+                            const int32_t* new_seq_lens, float* state,
+                            const int32_t* page_table,
+                            int32_t max_pages_per_seq, int32_t page_size,
+                            int32_t num_pages, int32_t* next_q_lens,
+                            int32_t* next_seq_lens, int32_t* block_ids,
+                            int32_t* positions, int64_t* cache_loc,
+                            uint32_t* status, void* stream);
+
+/*
  * Verify attention without a caller workspace, for callers that cannot
  * allocate device memory (no cudaMalloc and no pool of their own: e.g. code
  * handed only the input and output buffers of an engine that owns all device
@@ -227,8 +350,9 @@ int spec_verify_attention_noalloc(const spec_attn_desc* desc, const void* q,
 /*
  * Append each request's verify block to its paged KV cache.
  *
- * Block row i of request b is token t = seq_lens[b] - q_len + i (seq_lens
- * includes the block, as for spec_verify_attention); its K and V rows of
+ * Block row i < q_b of request b is token t = seq_lens[b] - q_b + i
+ * (seq_lens includes the block, as for spec_verify_attention; q_b =
+ * desc->q_lens[b] when given, else q_len); its K and V rows of
  * every KV head go to page page_table[b, t / page_size], slot
  * t % page_size.  The pages' serving stacks reserve those slots ahead of
  * the verify pass and hand the kernels the block's positions and cache
@@ -252,10 +376,11 @@ int spec_verify_attention_noalloc(const spec_attn_desc* desc, const void* q,
  *   k_pages, v_pages, k_scales, v_scales  the pool, as in
  *                 spec_verify_attention (scales only for FP8)
  *   page_table, seq_lens  as in spec_verify_attention
- *   positions     optional int32 [B, q_len]: t (or -1 where t < 0)
+ *   positions     optional int32 [B, q_len]: t (or -1 where t < 0 or
+ *                 i >= q_b)
  *   cache_loc     optional int64 [B, q_len]: page * page_size + slot, the
  *                 flat token slot in the pool (or -1 where the token has no
- *                 slot: t < 0, t beyond the table, or a page id outside the
+ *                 slot: i >= q_b, t < 0, t beyond the table, or a page id outside the
  *                 pool; such rows are not written, and SPEC_FLAG_CHECKED
  *                 reports a bad page id through spec_verify_status on
  *                 `workspace`)

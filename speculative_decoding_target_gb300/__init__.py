@@ -6,14 +6,18 @@ this package does not load the library; the first call does, and raises if
 it is missing.
 """
 from ._native import (SpecError, accept_workspace_size, alloc_workspace,
-                      desc_for, greedy_accept, greedy_accept_into, kv_append,
-                      load,
-                      make_desc, verify_attention, verify_attention_into,
-                      verify_status, verify_workspace_size)
+                      desc_for, greedy_accept, greedy_accept_commit,
+                      greedy_accept_commit_into, greedy_accept_into,
+                      kv_append, load, make_desc, prepare_next_block,
+                      prepare_next_block_into, verify_attention,
+                      verify_attention_into, verify_status,
+                      verify_workspace_size, width_policy)
 
 __all__ = [
     "SpecError", "accept_workspace_size", "alloc_workspace", "desc_for",
-    "greedy_accept", "greedy_accept_into", "kv_append", "load", "make_desc",
-    "verify_attention", "verify_attention_into", "verify_status",
-    "verify_workspace_size",
+    "greedy_accept", "greedy_accept_commit", "greedy_accept_commit_into",
+    "greedy_accept_into", "kv_append", "load", "make_desc",
+    "prepare_next_block", "prepare_next_block_into", "verify_attention",
+    "verify_attention_into", "verify_status", "verify_workspace_size",
+    "width_policy",
 ]

@@ -27,12 +27,14 @@ SPEC_KV_FP8_E4M3 = 1
 SPEC_FLAG_CHECKED = 1
 SPEC_STATUS_BAD_PAGE = 1
 SPEC_STATUS_TIMEOUT = 2
+SPEC_STATUS_NO_SLOT = 4
+WIDTH_POLICIES = {"fixed": 0, "ewma": 1, "doubling": 2}
 
 EXPORTED = (
     "spec_verify_workspace_size", "spec_verify_attention",
     "spec_verify_status", "spec_accept_workspace_size", "spec_greedy_accept",
     "spec_last_error", "spec_version", "spec_verify_attention_noalloc",
-    "spec_kv_append",
+    "spec_kv_append", "spec_greedy_accept_commit", "spec_prepare_next_block",
 )
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
@@ -49,7 +51,14 @@ class AttnDesc(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("kv_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("q_lens", ctypes.c_void_p)]
+
+
+class WidthPolicy(ctypes.Structure):
+    _fields_ = [("policy", ctypes.c_int32), ("q_max", ctypes.c_int32),
+                ("min_width", ctypes.c_int32), ("mask_id", ctypes.c_int32),
+                ("alpha", ctypes.c_float), ("offset", ctypes.c_float)]
 
 
 _lib = None
@@ -85,6 +94,13 @@ def load(path: str = LIB_PATH):
     lib.spec_accept_workspace_size.restype = sz
     lib.spec_greedy_accept.argtypes = [P, P, i32, i32, i32, P, P, P, P, sz, P]
     lib.spec_greedy_accept.restype = ctypes.c_int
+    lib.spec_greedy_accept_commit.argtypes = [P, P, P, i32, i32, i32, P, P, P,
+                                              P, P, P, sz, P]
+    lib.spec_greedy_accept_commit.restype = ctypes.c_int
+    lib.spec_prepare_next_block.argtypes = [
+        ctypes.POINTER(WidthPolicy), i32, P, P, P, P, P, P, i32, i32, i32, P,
+        P, P, P, P, P, P]
+    lib.spec_prepare_next_block.restype = ctypes.c_int
     lib.spec_last_error.argtypes = []
     lib.spec_last_error.restype = ctypes.c_char_p
     lib.spec_version.argtypes = []
@@ -110,15 +126,18 @@ def _stream(stream) -> ctypes.c_void_p:
 
 def make_desc(*, batch, q_len, num_q_heads, num_kv_heads, head_dim,
               page_size, num_pages, max_pages_per_seq, kv_dtype="bf16",
-              checked=False) -> AttnDesc:
+              checked=False, q_lens: Optional[torch.Tensor] = None) -> AttnDesc:
+    """q_lens: optional int32 device tensor [B] of per-request block rows."""
     return AttnDesc(batch, q_len, num_q_heads, num_kv_heads, head_dim,
                     page_size, num_pages, max_pages_per_seq,
                     SPEC_KV_BF16 if kv_dtype == "bf16" else SPEC_KV_FP8_E4M3,
-                    SPEC_FLAG_CHECKED if checked else 0)
+                    SPEC_FLAG_CHECKED if checked else 0,
+                    None if q_lens is None else q_lens.data_ptr())
 
 
 def desc_for(q: torch.Tensor, k_pages: torch.Tensor,
-             page_table: torch.Tensor, checked: bool = False) -> AttnDesc:
+             page_table: torch.Tensor, checked: bool = False,
+             q_lens: Optional[torch.Tensor] = None) -> AttnDesc:
     B, q_len, hq, d = q.shape
     num_pages, hkv, ps, d2 = k_pages.shape
     assert d2 == d
@@ -126,7 +145,7 @@ def desc_for(q: torch.Tensor, k_pages: torch.Tensor,
                      head_dim=d, page_size=ps, num_pages=num_pages,
                      max_pages_per_seq=page_table.shape[1],
                      kv_dtype="fp8" if k_pages.dtype == torch.uint8 else "bf16",
-                     checked=checked)
+                     checked=checked, q_lens=q_lens)
 
 
 def verify_workspace_size(desc: AttnDesc) -> int:
@@ -159,9 +178,12 @@ def verify_attention(q, k_pages, v_pages, page_table, seq_lens, *,
                      scale: float, k_scales=None, v_scales=None,
                      out: Optional[torch.Tensor] = None,
                      workspace: Optional[torch.Tensor] = None,
-                     checked: bool = False, stream=None) -> torch.Tensor:
-    """Verify attention on device tensors; returns out bf16 [B, q_len, Hq, D]."""
-    desc = desc_for(q, k_pages, page_table, checked)
+                     checked: bool = False, q_lens=None,
+                     stream=None) -> torch.Tensor:
+    """Verify attention on device tensors; returns out bf16 [B, q_len, Hq, D]
+    (q_lens: optional int32 [B] rows per request of a block padded to
+    q_len)."""
+    desc = desc_for(q, k_pages, page_table, checked, q_lens)
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
@@ -174,10 +196,10 @@ def verify_attention(q, k_pages, v_pages, page_table, seq_lens, *,
 def verify_attention_noalloc(q, k_pages, v_pages, page_table, seq_lens, *,
                              scale: float, k_scales=None, v_scales=None,
                              out: Optional[torch.Tensor] = None,
-                             stream=None) -> torch.Tensor:
+                             q_lens=None, stream=None) -> torch.Tensor:
     """Verify attention with the library's fixed scratch instead of a
     workspace (for callers that cannot allocate device memory)."""
-    desc = desc_for(q, k_pages, page_table)
+    desc = desc_for(q, k_pages, page_table, q_lens=q_lens)
     if out is None:
         out = torch.empty_like(q)
     _check(load().spec_verify_attention_noalloc(
@@ -189,7 +211,8 @@ def verify_attention_noalloc(q, k_pages, v_pages, page_table, seq_lens, *,
 
 def kv_append(k_new, v_new, k_pages, v_pages, page_table, seq_lens, *,
               k_scales=None, v_scales=None, positions=None, cache_loc=None,
-              checked: bool = False, workspace=None, stream=None):
+              checked: bool = False, workspace=None, q_lens=None,
+              stream=None):
     """Append the verify block's K/V (bf16 [B, q_len, Hkv, D]) to the paged
     pool in place (quantised on write for an FP8 pool); fills the optional
     positions (int32 [B, q_len]) and cache_loc (int64 [B, q_len])."""
@@ -199,7 +222,7 @@ def kv_append(k_new, v_new, k_pages, v_pages, page_table, seq_lens, *,
                      head_dim=d, page_size=ps, num_pages=num_pages,
                      max_pages_per_seq=page_table.shape[1],
                      kv_dtype="fp8" if k_pages.dtype == torch.uint8 else "bf16",
-                     checked=checked)
+                     checked=checked, q_lens=q_lens)
     _check(load().spec_kv_append(
         ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(k_pages),
         _ptr(v_pages), _ptr(k_scales), _ptr(v_scales), _ptr(page_table),
@@ -222,6 +245,81 @@ def greedy_accept_into(logits, draft_ids, accept_len, next_token, out_tokens,
         _ptr(logits), _ptr(draft_ids), B, q_len, logits.shape[-1],
         _ptr(accept_len), _ptr(next_token), _ptr(out_tokens),
         _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def greedy_accept_commit_into(logits, draft_ids, q_lens, seq_lens,
+                              new_seq_lens, accept_len, next_token, out_tokens,
+                              workspace: torch.Tensor, stream=None) -> None:
+    B, q_len = draft_ids.shape
+    _check(load().spec_greedy_accept_commit(
+        _ptr(logits), _ptr(draft_ids), _ptr(q_lens), B, q_len,
+        logits.shape[-1], _ptr(seq_lens), _ptr(new_seq_lens),
+        _ptr(accept_len), _ptr(next_token), _ptr(out_tokens),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def greedy_accept_commit(logits, draft_ids, q_lens, seq_lens, *,
+                         workspace: Optional[torch.Tensor] = None,
+                         stream=None):
+    """Greedy accept with per-request widths and the committed cache length.
+    Returns (accept_len, next_token, out_tokens, new_seq_lens)."""
+    B, q_len = draft_ids.shape
+    dev = logits.device
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    toks = torch.empty((B, q_len), dtype=torch.int32, device=dev)
+    new = torch.empty(B, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(
+            accept_workspace_size(B * q_len, logits.shape[-1]), dev)
+    greedy_accept_commit_into(logits, draft_ids, q_lens, seq_lens, new, acc,
+                              nxt, toks, workspace, stream)
+    return acc, nxt, toks, new
+
+
+def width_policy(policy: str, q_max: int, *, min_width: int = 2,
+                 alpha: float = 0.5, offset: float = 1.5,
+                 mask_id: int = 0) -> WidthPolicy:
+    return WidthPolicy(WIDTH_POLICIES[policy], q_max, min_width, mask_id,
+                       alpha, offset)
+
+
+def prepare_next_block_into(pol: WidthPolicy, q_lens, accept_len, next_token,
+                            new_seq_lens, state, page_table, page_size: int,
+                            num_pages: int, next_q_lens, next_seq_lens,
+                            block_ids=None, positions=None, cache_loc=None,
+                            status=None, stream=None) -> None:
+    B = accept_len.shape[0]
+    _check(load().spec_prepare_next_block(
+        ctypes.byref(pol), B, _ptr(q_lens), _ptr(accept_len),
+        _ptr(next_token), _ptr(new_seq_lens), _ptr(state), _ptr(page_table),
+        page_table.shape[1], page_size, num_pages, _ptr(next_q_lens),
+        _ptr(next_seq_lens), _ptr(block_ids), _ptr(positions),
+        _ptr(cache_loc), _ptr(status), _stream(stream)))
+
+
+def prepare_next_block(pol: WidthPolicy, q_lens, accept_len, next_token,
+                       new_seq_lens, state, page_table, *, page_size: int,
+                       num_pages: int, status=None, stream=None):
+    """Next widths and next-block layout on the device (state updated in
+    place).  Returns dict of next_q_lens, next_seq_lens, block_ids,
+    positions, cache_loc."""
+    B = accept_len.shape[0]
+    dev = accept_len.device
+    out = {"next_q_lens": torch.empty(B, dtype=torch.int32, device=dev),
+           "next_seq_lens": torch.empty(B, dtype=torch.int32, device=dev),
+           "block_ids": torch.empty((B, pol.q_max), dtype=torch.int32,
+                                    device=dev),
+           "positions": torch.empty((B, pol.q_max), dtype=torch.int32,
+                                    device=dev),
+           "cache_loc": torch.empty((B, pol.q_max), dtype=torch.int64,
+                                    device=dev)}
+    prepare_next_block_into(pol, q_lens, accept_len, next_token, new_seq_lens,
+                            state, page_table, page_size, num_pages,
+                            out["next_q_lens"], out["next_seq_lens"],
+                            out["block_ids"], out["positions"],
+                            out["cache_loc"], status, stream)
+    return out
 
 
 def greedy_accept(logits: torch.Tensor, draft_ids: torch.Tensor, *,

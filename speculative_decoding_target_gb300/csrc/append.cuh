@@ -16,6 +16,7 @@ struct AppendParams {
   __half* v_scales;
   const int32_t* page_table;
   const int32_t* seq_lens;
+  const int32_t* q_lens;  // optional [B]: rows of each block (<= q_len)
   int32_t* positions;   // optional
   int64_t* cache_loc;   // optional
   uint32_t* status;     // checked mode only

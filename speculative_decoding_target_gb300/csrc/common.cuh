@@ -37,6 +37,7 @@ struct AttnParams {
   const __half* v_scales;
   const int32_t* page_table;
   const int32_t* seq_lens;
+  const int32_t* q_lens;  // optional [B]: rows of each block (<= q_len)
   __nv_bfloat16* out;
   float* part_o;      // [nslots, rows, 256]
   float* part_lse;    // [nslots, rows] (base 2)
@@ -51,6 +52,19 @@ struct AttnParams {
 
 __device__ __forceinline__ int clamp_len(int len, int cap) {
   return len < 0 ? 0 : (len > cap ? cap : len);
+}
+
+// Rows of request b's verify block: q_lens[b] clamped to [0, q_len], or
+// q_len.  Block row i < rows is token seq_len - rows + i; the rows past it
+// do not exist and get an empty causal window (zero output).
+__device__ __forceinline__ int block_rows(const AttnParams& p, int b) {
+  return p.q_lens ? clamp_len(p.q_lens[b], p.q_len) : p.q_len;
+}
+
+// Keys visible to block row i of a request with len cached tokens and qb
+// block rows.
+__device__ __forceinline__ int causal_limit(int len, int qb, int i) {
+  return i < qb ? len - qb + i + 1 : 0;
 }
 
 __device__ __forceinline__ int units_of(int len) {
@@ -152,6 +166,9 @@ constexpr int kTcMinPageSize = 8;
 struct AcceptParams {
   const float* logits;
   const int32_t* draft_ids;
+  const int32_t* q_lens;     // optional [B]: rows of each block (<= q_len)
+  const int32_t* seq_lens;   // optional [B], with new_seq_lens
+  int32_t* new_seq_lens;     // optional [B]: seq_len - q_b + a + 1
   int32_t* accept_len;
   int32_t* next_token;
   int32_t* out_tokens;

@@ -4,9 +4,10 @@
 // section 1.6.1 commit_lens = accept_len + 1).
 //
 // Kernel 1 streams the fp32 logits once: CTA (chunk, row) reduces 8192
-// entries with 16-byte streaming loads to a (maximum, first index) pair.  Kernel 2,
-// one CTA per request, reduces the chunk pairs of its q_len rows and walks
-// the drafts.  The reduction order is arbitrary, so the combine is a total
+// entries with 16-byte streaming loads to a (maximum, first index) pair;
+// rows past a request's block width are skipped unread.  Kernel 2, one CTA
+// per request, reduces the chunk pairs of its rows, walks the drafts and
+// publishes the committed cache length.  The reduction order is arbitrary, so the combine is a total
 // order that makes the result unique: NaN above every number (lower index
 // first among NaNs), then larger value, then lower index (so -0 == +0 ties
 // go to the lower index).
@@ -61,6 +62,10 @@ __global__ void __launch_bounds__(kAcceptThreads)
   __shared__ float s_m[kAcceptThreads / 32];
   __shared__ int s_i[kAcceptThreads / 32];
   const int chunk = blockIdx.x, row = blockIdx.y;
+  if (p.q_lens) {  // uniform per CTA: the row lies past its block
+    const int b = row / p.q_len;
+    if (row - b * p.q_len >= min(max(p.q_lens[b], 0), p.q_len)) return;
+  }
   const float* x = p.logits + (long long)row * p.vocab;
   const int begin = chunk * kAcceptChunk;
   const int end = min(begin + kAcceptChunk, p.vocab);
@@ -133,7 +138,8 @@ __global__ void accept_finalize_kernel(const AcceptParams p) {
   __shared__ int s_t[32];
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < p.q_len) {
+  const int qb = p.q_lens ? min(max(p.q_lens[b], 0), p.q_len) : p.q_len;
+  if (warp < qb) {
     const long long row = (long long)b * p.q_len + warp;
     float bv = -INFINITY;
     int bi = INT_MAX;
@@ -147,14 +153,19 @@ __global__ void accept_finalize_kernel(const AcceptParams p) {
   if (threadIdx.x == 0) {
     const int32_t* d = p.draft_ids + (long long)b * p.q_len;
     int a = 0;
-    while (a + 1 < p.q_len && d[a + 1] == s_t[a]) ++a;
+    while (a + 1 < qb && d[a + 1] == s_t[a]) ++a;
+    // an idle request (no rows) commits nothing
+    const int next = qb > 0 ? s_t[a] : -1;
     p.accept_len[b] = a;
-    p.next_token[b] = s_t[a];
+    p.next_token[b] = next;
     if (p.out_tokens) {
       int32_t* o = p.out_tokens + (long long)b * p.q_len;
       for (int j = 0; j < p.q_len; ++j)
-        o[j] = j < a ? d[j + 1] : (j == a ? s_t[a] : -1);
+        o[j] = j < a ? d[j + 1] : (j == a ? next : -1);
     }
+    // the cache keeps the prefix, the boundary and d1..da
+    if (p.new_seq_lens)
+      p.new_seq_lens[b] = qb > 0 ? p.seq_lens[b] - qb + a + 1 : p.seq_lens[b];
   }
 }
 

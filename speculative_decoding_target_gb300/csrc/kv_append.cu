@@ -29,10 +29,12 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int g = w % p.hkv;
   const int bi = w / p.hkv;
   const int i = bi % p.q_len, b = bi / p.q_len;
-  const long long t = (long long)p.seq_lens[b] - p.q_len + i;
+  int qb = p.q_len;
+  if (p.q_lens) qb = min(max(p.q_lens[b], 0), p.q_len);
+  const long long t = (long long)p.seq_lens[b] - qb + i;
   long long loc = -1;
   int page = 0;
-  if (t >= 0 && t < p.max_tokens) {
+  if (i < qb && t >= 0 && t < p.max_tokens) {
     page = p.page_table[(long long)b * p.max_pages + (t >> p.log2_ps)];
     if (page >= 0 && page < p.num_pages) {
       loc = (long long)page * p.page_size + (t & (p.page_size - 1));
@@ -41,7 +43,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
   }
   if (g == 0 && lane == 0) {
-    if (p.positions) p.positions[bi] = t >= 0 ? (int32_t)t : -1;
+    if (p.positions) p.positions[bi] = i < qb && t >= 0 ? (int32_t)t : -1;
     if (p.cache_loc) p.cache_loc[bi] = loc;
   }
   if (loc < 0) return;

@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 
 #include "append.cuh"
+#include "next_block.cuh"
 #include "common.cuh"
 #include "spec_verify.h"
 
@@ -154,6 +155,8 @@ int check_desc(const spec_attn_desc* d) {
     return fail(SPEC_ERR_ARG, "kv_dtype %d", d->kv_dtype);
   if (d->flags & ~SPEC_FLAG_CHECKED)
     return fail(SPEC_ERR_ARG, "unknown flags 0x%x", d->flags);
+  if (d->q_lens && !aligned(d->q_lens, 4))
+    return fail(SPEC_ERR_ALIGN, "q_lens must be 4-byte aligned");
   if ((long long)d->num_pages * d->num_kv_heads * d->page_size >= (1LL << 31))
     return fail(SPEC_ERR_UNSUPPORTED,
                 "num_pages * num_kv_heads * page_size must be < 2^31");
@@ -255,6 +258,7 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
   p.v_scales = fp8 ? static_cast<const __half*>(v_scales) : nullptr;
   p.page_table = page_table;
   p.seq_lens = seq_lens;
+  p.q_lens = desc->q_lens;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.part_o = reinterpret_cast<float*>(ws + L.o_off);
   p.part_lse = reinterpret_cast<float*>(ws + L.lse_off);
@@ -356,6 +360,7 @@ int spec_kv_append(const spec_attn_desc* desc, const void* k_new,
   p.v_scales = fp8 ? static_cast<__half*>(v_scales) : nullptr;
   p.page_table = page_table;
   p.seq_lens = seq_lens;
+  p.q_lens = desc->q_lens;
   p.positions = positions;
   p.cache_loc = cache_loc;
   p.batch = desc->batch;
@@ -381,6 +386,76 @@ int spec_kv_append(const spec_attn_desc* desc, const void* k_new,
   return SPEC_OK;
 }
 
+int spec_prepare_next_block(const spec_width_policy* pol, int32_t batch,
+                            const int32_t* q_lens, const int32_t* accept_len,
+                            const int32_t* next_token,
+                            const int32_t* new_seq_lens, float* state,
+                            const int32_t* page_table,
+                            int32_t max_pages_per_seq, int32_t page_size,
+                            int32_t num_pages, int32_t* next_q_lens,
+                            int32_t* next_seq_lens, int32_t* block_ids,
+                            int32_t* positions, int64_t* cache_loc,
+                            uint32_t* status, void* stream) {
+  g_err[0] = 0;
+  if (!pol) return fail(SPEC_ERR_ARG, "policy is NULL");
+  if (pol->policy < SPEC_WIDTH_FIXED || pol->policy > SPEC_WIDTH_DOUBLING)
+    return fail(SPEC_ERR_ARG, "unknown width policy %d", pol->policy);
+  if (pol->q_max < 1 || pol->q_max > 16)
+    return fail(SPEC_ERR_ARG, "q_max %d outside [1, 16]", pol->q_max);
+  if (pol->min_width < 1 || pol->min_width > pol->q_max)
+    return fail(SPEC_ERR_ARG, "min_width %d outside [1, q_max]", pol->min_width);
+  if (!(pol->alpha >= 0.f && pol->alpha <= 1.f) ||
+      !(pol->offset > -1e6f && pol->offset < 1e6f))
+    return fail(SPEC_ERR_ARG, "alpha must lie in [0, 1] and offset be finite");
+  if (batch < 0 || batch > (1 << 24))
+    return fail(SPEC_ERR_ARG, "batch %d outside [0, 2^24]", batch);
+  if (page_size < 1 || max_pages_per_seq < 1 || num_pages < 1)
+    return fail(SPEC_ERR_ARG, "page_size, max_pages_per_seq and num_pages must be >= 1");
+  if (batch == 0) return SPEC_OK;
+  if (!accept_len || !next_token || !new_seq_lens || !page_table ||
+      !next_q_lens || !next_seq_lens)
+    return fail(SPEC_ERR_ARG, "NULL tensor pointer");
+  if (pol->policy != SPEC_WIDTH_FIXED && !state)
+    return fail(SPEC_ERR_ARG, "this width policy needs its state array");
+  const void* a4[] = {q_lens, accept_len, next_token, new_seq_lens, state,
+                      page_table, next_q_lens, next_seq_lens, block_ids,
+                      positions, status};
+  for (const void* q : a4)
+    if (q && !aligned(q, 4))
+      return fail(SPEC_ERR_ALIGN, "int32 / float buffers must be 4-byte aligned");
+  if (cache_loc && !aligned(cache_loc, 8))
+    return fail(SPEC_ERR_ALIGN, "cache_loc must be 8-byte aligned");
+  specv::NextBlockParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q_lens = q_lens;
+  p.accept_len = accept_len;
+  p.next_token = next_token;
+  p.new_seq_lens = new_seq_lens;
+  p.state = state;
+  p.page_table = page_table;
+  p.next_q_lens = next_q_lens;
+  p.next_seq_lens = next_seq_lens;
+  p.block_ids = block_ids;
+  p.positions = positions;
+  p.cache_loc = cache_loc;
+  p.status = status;
+  p.batch = batch;
+  p.policy = pol->policy;
+  p.q_max = pol->q_max;
+  p.min_width = pol->min_width;
+  p.mask_id = pol->mask_id;
+  p.max_pages = max_pages_per_seq;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
+  p.alpha = pol->alpha;
+  p.offset = pol->offset;
+  cudaError_t e =
+      specv::launch_prepare_next_block(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(SPEC_ERR_CUDA, "prepare kernel launch: %s", cudaGetErrorString(e));
+  return SPEC_OK;
+}
+
 size_t spec_accept_workspace_size(int32_t rows, int32_t vocab) {
   if (rows < 0 || vocab < 1) {
     fail(SPEC_ERR_ARG, "rows %d / vocab %d", rows, vocab);
@@ -397,6 +472,19 @@ int spec_greedy_accept(const float* logits, const int32_t* draft_ids,
                        int32_t* accept_len, int32_t* next_token,
                        int32_t* out_tokens, void* workspace,
                        size_t workspace_bytes, void* stream) {
+  return spec_greedy_accept_commit(logits, draft_ids, nullptr, batch, q_len,
+                                   vocab, nullptr, nullptr, accept_len,
+                                   next_token, out_tokens, workspace,
+                                   workspace_bytes, stream);
+}
+
+int spec_greedy_accept_commit(const float* logits, const int32_t* draft_ids,
+                              const int32_t* q_lens, int32_t batch,
+                              int32_t q_len, int32_t vocab,
+                              const int32_t* seq_lens, int32_t* new_seq_lens,
+                              int32_t* accept_len, int32_t* next_token,
+                              int32_t* out_tokens, void* workspace,
+                              size_t workspace_bytes, void* stream) {
   g_err[0] = 0;
   if (batch < 0) return fail(SPEC_ERR_ARG, "batch %d < 0", batch);
   if (q_len < 1 || q_len > 16)
@@ -408,8 +496,12 @@ int spec_greedy_accept(const float* logits, const int32_t* draft_ids,
   if (!logits || !draft_ids || !accept_len || !next_token)
     return fail(SPEC_ERR_ARG, "NULL tensor pointer");
   if (!aligned(logits, 4) || !aligned(draft_ids, 4) || !aligned(accept_len, 4) ||
-      !aligned(next_token, 4) || (out_tokens && !aligned(out_tokens, 4)))
+      !aligned(next_token, 4) || (out_tokens && !aligned(out_tokens, 4)) ||
+      (q_lens && !aligned(q_lens, 4)) || (seq_lens && !aligned(seq_lens, 4)) ||
+      (new_seq_lens && !aligned(new_seq_lens, 4)))
     return fail(SPEC_ERR_ALIGN, "logits and int32 buffers must be 4-byte aligned");
+  if (!seq_lens != !new_seq_lens)
+    return fail(SPEC_ERR_ARG, "seq_lens and new_seq_lens go together");
   if (!workspace) return fail(SPEC_ERR_WORKSPACE, "workspace is NULL");
   if (!aligned(workspace, 16))
     return fail(SPEC_ERR_ALIGN, "workspace must be 16-byte aligned");
@@ -421,6 +513,9 @@ int spec_greedy_accept(const float* logits, const int32_t* draft_ids,
   specv::AcceptParams p;
   p.logits = logits;
   p.draft_ids = draft_ids;
+  p.q_lens = q_lens;
+  p.seq_lens = seq_lens;
+  p.new_seq_lens = new_seq_lens;
   p.accept_len = accept_len;
   p.next_token = next_token;
   p.out_tokens = out_tokens;

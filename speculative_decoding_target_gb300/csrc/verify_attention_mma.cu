@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
     u = s0 + j1;
 
     const int len = clamp_len(p.seq_lens[b], p.max_tokens);
+    const int qb = block_rows(p, b);
     const int tok_begin = j0 * kUnit;
     const int tok_end = min(j1 * kUnit, len);
     const int n_tiles = (tok_end - tok_begin + kTile - 1) / kTile;
@@ -165,9 +166,10 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
     // Q rows r = i * group + j of KV head g: q[b, i, g * group + j, :]
     for (int idx = tid; idx < C::kQRows * 32; idx += C::kThreads) {
       const int r = idx >> 5, cc = idx & 31;
-      const bool valid = r < p.rows;
-      const int i = valid ? r / p.group : 0;
-      const int h = g * p.group + (valid ? r - i * p.group : 0);
+      const bool in_tile = r < p.rows;
+      const int i = in_tile ? r / p.group : 0;
+      const int h = g * p.group + (in_tile ? r - i * p.group : 0);
+      const bool valid = in_tile && i < qb;   // zero-fill rows past the block
       const __nv_bfloat16* src =
           p.q + ((((long long)b * p.q_len + i) * p.hq + h) * kHeadDim + cc * 8);
       cp_async16(smem_addr(q_s + swz(r, cc)), valid ? src : p.q, valid);
@@ -181,8 +183,10 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
       o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     const int r0 = warp * 16 + g4, r1 = r0 + 8;
-    const int lim0 = len - p.q_len + r0 / p.group + 1;
-    const int lim1 = len - p.q_len + r1 / p.group + 1;
+    const int lim0 = causal_limit(len, qb, r0 / p.group);
+    const int lim1 = causal_limit(len, qb, r1 / p.group);
+    // smallest limit over the piece's rows: 0 once a row lies past the block
+    const int lim_min = qb < p.q_len ? 0 : len - qb + 1;
 
     for (int it = 0; it < n_tiles; ++it) {
       const int t0 = tok_begin + it * kTile;
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
           }
         }
         // scale to base 2, causal / length mask on the block tail
-        const bool need_mask = t0 + kTile > len - p.q_len + 1;
+        const bool need_mask = t0 + kTile > lim_min;
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int n = 0; n < kTile / 8; ++n) {

@@ -408,9 +408,11 @@ __device__ __forceinline__ void load_q_tmem(const AttnParams& p, const Piece& pc
   const int w4 = warp & 3;
   const int R = (p.rows + 3) >> 2;
   const int r = w4 * R + lane;
-  const bool valid = lane < R && r < p.rows;
-  const int i = valid ? r / p.group : 0;
-  const int h = pc.g * p.group + (valid ? r - i * p.group : 0);
+  const bool in_tile = lane < R && r < p.rows;
+  const int i = in_tile ? r / p.group : 0;
+  const int h = pc.g * p.group + (in_tile ? r - i * p.group : 0);
+  // rows past the request's block are never read (they may hold anything)
+  const bool valid = in_tile && i < block_rows(p, pc.b);
   const uint4* src = reinterpret_cast<const uint4*>(
       p.q + (((long long)pc.b * p.q_len + i) * p.hq + h) * kHeadDim);
   const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16) + kColQ;
@@ -451,7 +453,7 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
   const int r = w4 * R + lane;
   const bool valid = lane < R && r < p.rows;
   const int i = valid ? r / p.group : 0;
-  const int lim = pc.len - p.q_len + i + 1;
+  const int lim = causal_limit(pc.len, block_rows(p, pc.b), i);
   const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
   const float sl2 = p.scale_log2;
 

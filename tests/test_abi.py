@@ -149,3 +149,52 @@ def test_kv_append_argument_checks(lib):
                 vs=ctypes.c_void_p(0x100002)) == _native.SPEC_ERR_ALIGN
     assert call(_desc(checked=True)) == _native.SPEC_ERR_WORKSPACE
     assert call(_desc(page_size=24)) == _native.SPEC_ERR_ARG
+
+
+def test_accept_commit_argument_checks(lib):
+    f = lib.spec_greedy_accept_commit
+
+    def call(q_lens=None, seq_lens=None, new=None):
+        return f(FAKE, FAKE, q_lens, 2, 8, 1000, seq_lens, new, FAKE, FAKE,
+                 None, FAKE, 1 << 20, None)
+
+    assert call(seq_lens=FAKE) == _native.SPEC_ERR_ARG      # needs new too
+    assert call(new=FAKE) == _native.SPEC_ERR_ARG
+    assert call(q_lens=ctypes.c_void_p(0x100002)) == _native.SPEC_ERR_ALIGN
+    assert call(seq_lens=FAKE, new=ctypes.c_void_p(0x100001)) == \
+        _native.SPEC_ERR_ALIGN
+
+
+def test_desc_q_lens_must_be_aligned(lib):
+    d = _desc()
+    d.q_lens = 0x100002
+    assert _attn(lib, d) == _native.SPEC_ERR_ALIGN
+
+
+def test_prepare_next_block_argument_checks(lib):
+    f = lib.spec_prepare_next_block
+
+    def call(pol, batch=3, state=FAKE, cache_loc=FAKE, next_q=FAKE):
+        return f(ctypes.byref(pol) if pol is not None else None, batch, None,
+                 FAKE, FAKE, FAKE, state, FAKE, 4, 16, 64, next_q, FAKE, FAKE,
+                 FAKE, cache_loc, None, None)
+
+    ok = _native.width_policy("ewma", 8)
+    assert call(None) == _native.SPEC_ERR_ARG
+    assert call(_native.width_policy("fixed", 17)) == _native.SPEC_ERR_ARG
+    assert call(_native.width_policy("ewma", 8, min_width=9)) == \
+        _native.SPEC_ERR_ARG
+    assert call(_native.width_policy("ewma", 8, alpha=1.5)) == \
+        _native.SPEC_ERR_ARG
+    assert call(_native.width_policy("ewma", 8, offset=float("nan"))) == \
+        _native.SPEC_ERR_ARG
+    bad = _native.width_policy("fixed", 8)
+    bad.policy = 3
+    assert call(bad) == _native.SPEC_ERR_ARG
+    assert call(ok, state=None) == _native.SPEC_ERR_ARG
+    assert call(_native.width_policy("fixed", 8), batch=0, state=None,
+                next_q=None) == _native.SPEC_OK
+    assert call(ok, next_q=None) == _native.SPEC_ERR_ARG
+    assert call(ok, cache_loc=ctypes.c_void_p(0x100004)) == \
+        _native.SPEC_ERR_ALIGN
+    assert call(ok, batch=-1) == _native.SPEC_ERR_ARG
