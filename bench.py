@@ -46,15 +46,16 @@ KERNEL_LAUNCHES_PER_STEP = 4   # split, merge, argmax partial, accept finalize
 # ncu capture (profiles/verify_split_tc_*.md), keyed by workload and valid
 # only while the kernel's sources still hash to the recorded value.
 NCU_TRAFFIC = {
-    "b8_q8_p32k": {"source_hash": "4b8f0bf7281f90a3",
-                   "bytes_per_launch": 1077400000 + 5169664},
-    # captured on a smaller FP8 case (8 x 16K tokens, 276.9 MB algorithmic:
-    # 279.34 MB read + 4.11 MB written) and scaled to a full launch by the
-    # algorithmic bytes, which the traffic follows
-    "b32_q8_p1k128k_fp8": {"source_hash": "4b8f0bf7281f90a3",
-                           "per_algorithmic_byte": (279340288 + 4107264)
+    "b8_q8_p32k": {"source_hash": "0c0e4b240d4c3b89",
+                   "bytes_per_launch": 1077458688 + 5071104},
+    # captured on the smaller FP8 case b8_q8_p16k_fp8 (276.96 MB
+    # algorithmic: 279.34 MB read + 4.73 MB written) and scaled to a full
+    # launch by the algorithmic bytes, which the traffic follows
+    "b32_q8_p1k128k_fp8": {"source_hash": "0c0e4b240d4c3b89",
+                           "per_algorithmic_byte": (279336448 + 4729600)
                            / (8 * 16392 * 4 * 528)},
 }
+NCU_TRAFFIC["b8_q8_p16k_fp8"] = NCU_TRAFFIC["b32_q8_p1k128k_fp8"]
 SPLIT_KERNEL_SOURCES = ("verify_attention_tc.cu", "common.cuh", "tc_ptx.cuh")
 
 
@@ -370,6 +371,9 @@ def run_gpu(args, w: wl.VerifyWorkload):
     if not args.no_append:
         result["kv_append"] = measure_kv_append(w, dev, args.steps,
                                                 args.warmup)
+    if not args.no_ragged:
+        result["ragged"] = measure_ragged(w, inp, dev, args.steps,
+                                          args.warmup, attn_avg_s)
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         host_inp = {k: (v.cpu() if torch.is_tensor(v) else v)
                     for k, v in inp.items()}
@@ -451,6 +455,87 @@ def measure_kv_append(w: wl.VerifyWorkload, dev, iters: int, warmup: int):
                     f"graph, replayed {reps} times; the block (<1% of L2) "
                     "stays warm in L2, so the figure is launch and latency "
                     "bound, not HBM bound"}
+
+
+# ------------------------------------------------ per-request verify widths --
+
+def measure_ragged(w: wl.VerifyWorkload, inp, dev, steps: int, warmup: int,
+                   full_attn_s: float):
+    """One verify step with per-request widths q_b ~ U[1, q_len] (seeded):
+    attention over the padded block, accept with commit lengths (only the
+    q_b logits rows of each request are read), and the next block's
+    preparation under the EWMA width policy.  Timed per part with CUDA
+    events over `steps` steps on the workload's resident inputs."""
+    import speculative_decoding_target_gb300 as sv
+    from speculative_decoding_target_gb300 import _native
+    g = torch.Generator().manual_seed(w.seed + 21)
+    ql_h = torch.randint(1, w.q_len + 1, (w.batch,), generator=g)
+    ql = ql_h.to(torch.int32).to(dev)
+    desc = sv.desc_for(inp["q"], inp["k_pages"], inp["page_table"],
+                       q_lens=ql)
+    attn_ws = sv.alloc_workspace(sv.verify_workspace_size(desc), dev)
+    acc_ws = sv.alloc_workspace(
+        sv.accept_workspace_size(w.batch * w.q_len, w.vocab), dev)
+    out = torch.empty_like(inp["q"])
+    i32 = dict(dtype=torch.int32, device=dev)
+    acc, nxt, new = (torch.empty(w.batch, **i32) for _ in range(3))
+    toks = torch.empty((w.batch, w.q_len), **i32)
+    pol = sv.width_policy("ewma", w.q_len)
+    state0 = torch.full((w.batch,), w.q_len - 1.0, device=dev)
+    state = state0.clone()
+    nq, nsl = torch.empty(w.batch, **i32), torch.empty(w.batch, **i32)
+    bids, pos = (torch.empty((w.batch, w.q_len), **i32) for _ in range(2))
+    loc = torch.empty((w.batch, w.q_len), dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    num_pages = inp["k_pages"].shape[0]
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        _native.verify_attention_into(
+            desc, inp["q"], inp["k_pages"], inp["v_pages"], inp["k_scales"],
+            inp["v_scales"], inp["page_table"], inp["seq_lens"], inp["scale"],
+            out, attn_ws, stream)
+        if ev:
+            ev[1].record(stream)
+        sv.greedy_accept_commit_into(inp["logits"], inp["draft_ids"], ql,
+                                     inp["seq_lens"], new, acc, nxt, toks,
+                                     acc_ws, stream)
+        if ev:
+            ev[2].record(stream)
+        sv.prepare_next_block_into(pol, ql, acc, nxt, new, state,
+                                   inp["page_table"], w.page_size, num_pages,
+                                   nq, nsl, bids, pos, loc, None, stream)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+           for _ in range(steps)]
+    for k in range(steps):
+        step(evs[k])
+    torch.cuda.synchronize(dev)
+    part = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+            for j in range(3)]
+    total = statistics.mean(e[0].elapsed_time(e[3]) for e in evs)
+    rows = int(ql_h.sum())
+    return {
+        "value": round(1e3 / total, 3), "unit": UNIT,
+        "widths": "q_b ~ U[1, q_len], seeded, the same every step; the "
+                  "EWMA policy prepares the next block",
+        "mean_width": round(rows / w.batch, 3),
+        "attention_ms": round(part[0], 5),
+        "attention_full_width_ms": round(full_attn_s * 1e3, 5),
+        "accept_commit_ms": round(part[1], 5),
+        "logits_bytes_read": rows * w.vocab * 4,
+        "prepare_ms": round(part[2], 5),
+        "gpu_launches": 5 * steps,
+        "note": "attention streams the same KV whatever the widths (rows "
+                "are free in the 128-row MMA tile); accept reads only the "
+                "q_b logits rows of each request",
+    }
 
 
 # ----------------------------------------------------------- CPU baseline --
@@ -551,19 +636,21 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=wl.WORKLOAD_ORDER)
+                    choices=list(wl.ALL_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="replay each C-ABI call from a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append", action="store_true",
                     help="skip the block KV append timing")
+    ap.add_argument("--no-ragged", action="store_true",
+                    help="skip the per-request width (ragged) step timing")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--ref-rows", type=int, default=48)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = wl.WORKLOADS[args.workload]
+    w = wl.ALL_WORKLOADS[args.workload]
     if args.impl == "reference":
         res, rank = run_reference(args, w)
     else:

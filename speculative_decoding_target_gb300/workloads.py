@@ -85,6 +85,15 @@ WORKLOADS = {
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
+# Smaller cases of the same kernels for profiler captures that replay a
+# launch many times: inputs still larger than L2, a few hundred MB on the
+# device.  Not bench lines.
+PROFILE_WORKLOADS = {
+    "b8_q8_p16k_fp8": VerifyWorkload("b8_q8_p16k_fp8", 8, 8, 16384, None, 64,
+                                     "fp8_e4m3", 0.5, 6),
+}
+ALL_WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
+
 
 def prefix_lengths(w: VerifyWorkload) -> List[int]:
     if w.prefix is not None:
