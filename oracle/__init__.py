@@ -91,6 +91,9 @@ def _load():
         i32, i32, i32, f32, f32, i32, P, P, P, P, P, i32, P, i32, i32, i32,
         P, P, P, P, P]
     lib.oracle_prepare_next_block.restype = ctypes.c_int64
+    lib.oracle_stochastic_accept.argtypes = [P, P, P, P, i32, i32, i64, P, P,
+                                             P, P, P, P, P, P, P, i32]
+    lib.oracle_stochastic_accept.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -310,3 +313,44 @@ def prepare_next_block(policy: str, q_max: int, q_lens, accept_len,
     out["state"] = st
     out["missing"] = int(n)
     return out
+
+
+def stochastic_accept(logits, draft_ids, temperature, u_accept, u_sample, *,
+                      draft_probs=None, q_lens=None, seq_lens=None,
+                      threads: int = 0):
+    """Rejection-sampling verify in float64.
+
+    logits fp32 [B*q_len, V]; draft_ids int32 [B, q_len]; temperature fp32
+    [B] (> 0); u_accept fp32 [B, q_len-1] and u_sample fp32 [B] uniforms in
+    [0, 1); draft_probs fp32 [B, q_len-1, V] or None (greedy drafts).
+    Returns dict with accept_len, next_token, out_tokens, margin and, when
+    seq_lens is given, new_seq_lens.
+    """
+    lg = _c(logits, np.float32)
+    dr = _c(draft_ids, np.int32)
+    B, q_len = dr.shape
+    vocab = lg.shape[1]
+    assert lg.shape[0] == B * q_len
+    dp = None if draft_probs is None else _c(draft_probs, np.float32)
+    assert dp is None or dp.shape == (B, q_len - 1, vocab)
+    ql = None if q_lens is None else _c(q_lens, np.int32)
+    tt = _c(temperature, np.float32).reshape(B)
+    ua = _c(u_accept, np.float32).reshape(B, max(q_len - 1, 0))
+    us = _c(u_sample, np.float32).reshape(B)
+    sl = None if seq_lens is None else _c(seq_lens, np.int32)
+    nsl = None if sl is None else np.zeros(B, np.int32)
+    acc = np.zeros(B, np.int32)
+    nxt = np.zeros(B, np.int32)
+    toks = np.zeros((B, q_len), np.int32)
+    mg = np.zeros(B, np.float64)
+    rc = _load().oracle_stochastic_accept(
+        _ptr(lg), _ptr(dr), _ptr(dp), _ptr(ql), B, q_len, vocab, _ptr(tt),
+        _ptr(ua), _ptr(us), _ptr(sl), _ptr(nsl), _ptr(acc), _ptr(nxt),
+        _ptr(toks), _ptr(mg), int(threads or default_threads()))
+    if rc != ORACLE_OK:
+        raise ValueError(f"oracle_stochastic_accept failed with code {rc}")
+    res = {"accept_len": acc, "next_token": nxt, "out_tokens": toks,
+           "margin": mg}
+    if nsl is not None:
+        res["new_seq_lens"] = nsl
+    return res

@@ -64,6 +64,19 @@
  *     the boundary and d1..da: new_seq_len = seq_len - q_b + a + 1.  The
  *     bonus token opens the next block at position new_seq_len.
  *
+ *  7. Stochastic verify ("MTP and DFlash2 at long context on XPU", Part II:
+ *     sampling needs rejection sampling against target and draft
+ *     probabilities; the rule is the speculative sampling of Leviathan et
+ *     al. 2023, "Fast Inference from Transformers via Speculative Decoding",
+ *     and Chen et al. 2023).  p_j = softmax(logits[b, j] / T_b) is the
+ *     target's distribution for the token after block position j; q_j is
+ *     the drafter's distribution that proposed d_j (one-hot at d_j for a
+ *     greedy drafter).  Draft j is accepted iff u_j * q_j(d_j) <
+ *     p_{j-1}(d_j); at the first rejection the next token is drawn from the
+ *     normalised residual max(0, p_{j-1} - q_j); when every draft is
+ *     accepted it is drawn from p_{q_b-1}.  A draw from weights w with the
+ *     uniform u is the smallest v whose running sum exceeds u * sum(w).
+ *
  * Parity of this oracle against any engine on the pages is unpinned: the
  * pages print no output for a concrete input tensor.  It is pinned instead
  * by tests against library routines (torch scaled-dot-product attention in
@@ -642,4 +655,165 @@ int64_t oracle_prepare_next_block(
     }
   }
   return missing;
+}
+
+/* ---- stochastic verify (rejection sampling) ------------------------------- */
+
+/* Row softmax statistics at temperature t: m = max_v x_v, z = sum_v
+ * exp((x_v - m) / t).  p(v) = exp((x_v - m) / t) / z. */
+static void softmax_stats(const float* x, int64_t n, double t, double* m,
+                          double* z) {
+  double mx = -INFINITY;
+  for (int64_t v = 0; v < n; ++v)
+    if ((double)x[v] > mx) mx = (double)x[v];
+  double s = 0.0;
+  for (int64_t v = 0; v < n; ++v) s += exp(((double)x[v] - mx) / t);
+  *m = mx;
+  *z = s;
+}
+
+/*
+ * logits       fp32 [batch * q_len, vocab]
+ * draft_ids    int32 [batch, q_len] (column 0 the boundary token)
+ * draft_probs  fp32 [batch, q_len - 1, vocab]: row j-1 is q_j, the
+ *              distribution draft j was drawn from; NULL for greedy drafts
+ * q_lens       optional [batch] rows per request (as greedy accept)
+ * temperature  fp32 [batch], > 0
+ * u_accept     fp32 [batch, q_len - 1] uniforms in [0, 1) for the accept
+ *              tests; u_sample fp32 [batch] the uniform of the final draw
+ * seq_lens / new_seq_lens, accept_len, next_token, out_tokens: as greedy
+ * margin        optional fp64 [batch] out: the smallest distance of any
+ *              decision this request took from its threshold, relative to
+ *              the quantities compared (|u q - p| / max(p, q) for a test;
+ *              distance of u * W from the chosen interval's ends / W for
+ *              the draw).  A request with a small margin may legitimately
+ *              come out differently under another rounding.
+ */
+int oracle_stochastic_accept(const float* logits, const int32_t* draft_ids,
+                             const float* draft_probs, const int32_t* q_lens,
+                             int32_t batch, int32_t q_len, int64_t vocab,
+                             const float* temperature, const float* u_accept,
+                             const float* u_sample, const int32_t* seq_lens,
+                             int32_t* new_seq_lens, int32_t* accept_len,
+                             int32_t* next_token, int32_t* out_tokens,
+                             double* margin, int32_t nthreads) {
+  if (batch < 0 || q_len < 1 || vocab < 1) return ORACLE_ERR_ARG;
+  int err = ORACLE_OK;
+#ifdef _OPENMP
+  if (nthreads < 1) nthreads = omp_get_max_threads();
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1)
+#endif
+  for (int b = 0; b < batch; ++b) {
+    const int32_t qb = block_rows(q_lens, b, q_len);
+    const int32_t* dr = draft_ids + (int64_t)b * q_len;
+    int32_t* ot = out_tokens ? out_tokens + (int64_t)b * q_len : NULL;
+    if (ot)
+      for (int j = 0; j < q_len; ++j) ot[j] = -1;
+    double mg = INFINITY;
+    if (qb == 0) {
+      accept_len[b] = 0;
+      next_token[b] = -1;
+      if (new_seq_lens) new_seq_lens[b] = seq_lens[b];
+      if (margin) margin[b] = mg;
+      continue;
+    }
+    const double t = (double)temperature[b];
+    if (!(t > 0.0)) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+      err = ORACLE_ERR_ARG;
+      continue;
+    }
+    int a = 0;
+    int rejected = 0;
+    double m = 0.0, z = 0.0;
+    for (int j = 1; j < qb; ++j) {
+      const float* row = logits + ((int64_t)b * q_len + j - 1) * vocab;
+      softmax_stats(row, vocab, t, &m, &z);
+      const int32_t d = dr[j];
+      const double p = (d >= 0 && d < vocab)
+                           ? exp(((double)row[d] - m) / t) / z : 0.0;
+      double q = 1.0;
+      if (draft_probs && d >= 0 && d < vocab)
+        q = (double)draft_probs[((int64_t)b * (q_len - 1) + j - 1) * vocab + d];
+      const double u = (double)u_accept[(int64_t)b * (q_len - 1) + j - 1];
+      const double scale = p > q ? p : q;
+      if (scale > 0.0) {
+        const double dist = fabs(u * q - p) / scale;
+        if (dist < mg) mg = dist;
+      }
+      if (u * q < p) {
+        ++a;
+      } else {
+        rejected = 1;
+        break;
+      }
+    }
+    /* the final draw: from row a, minus q_{a+1} after a rejection */
+    const float* row = logits + ((int64_t)b * q_len + a) * vocab;
+    softmax_stats(row, vocab, t, &m, &z);
+    const float* qrow = NULL;
+    if (rejected && draft_probs)
+      qrow = draft_probs + ((int64_t)b * (q_len - 1) + a) * vocab;
+    const int32_t drej = rejected ? dr[a + 1] : -1;
+    double total = 0.0;
+    for (int64_t v = 0; v < vocab; ++v) {
+      double w = exp(((double)row[v] - m) / t) / z;
+      if (rejected) {
+        const double qv = qrow ? (double)qrow[v] : (v == drej ? 1.0 : 0.0);
+        w = w > qv ? w - qv : 0.0;
+      }
+      total += w;
+    }
+    int use_residual = rejected && total > 0.0;
+    if (rejected && !use_residual) { /* p == q: fall back to p itself */
+      total = 0.0;
+      for (int64_t v = 0; v < vocab; ++v) total += exp(((double)row[v] - m) / t) / z;
+    }
+    const double target = (double)u_sample[b] * total;
+    double cum = 0.0, prev = 0.0;
+    int64_t pick = -1;
+    for (int64_t v = 0; v < vocab; ++v) {
+      double w = exp(((double)row[v] - m) / t) / z;
+      if (use_residual) {
+        const double qv = qrow ? (double)qrow[v] : (v == drej ? 1.0 : 0.0);
+        w = w > qv ? w - qv : 0.0;
+      }
+      prev = cum;
+      cum += w;
+      if (cum > target) {
+        pick = v;
+        break;
+      }
+    }
+    if (pick < 0) { /* rounding left u * W at the very end: last nonzero */
+      for (int64_t v = vocab - 1; v >= 0; --v) {
+        double w = exp(((double)row[v] - m) / t) / z;
+        if (use_residual) {
+          const double qv = qrow ? (double)qrow[v] : (v == drej ? 1.0 : 0.0);
+          w = w > qv ? w - qv : 0.0;
+        }
+        if (w > 0.0) {
+          pick = v;
+          break;
+        }
+      }
+      prev = cum = target;
+    }
+    if (total > 0.0) {
+      const double lo = (target - prev) / total, hi = (cum - target) / total;
+      const double dist = lo < hi ? lo : hi;
+      if (dist < mg) mg = dist;
+    }
+    accept_len[b] = a;
+    next_token[b] = (int32_t)pick;
+    if (ot) {
+      for (int j = 0; j < a; ++j) ot[j] = dr[j + 1];
+      ot[a] = (int32_t)pick;
+    }
+    if (new_seq_lens) new_seq_lens[b] = seq_lens[b] - qb + a + 1;
+    if (margin) margin[b] = mg;
+  }
+  return err;
 }
