@@ -238,6 +238,68 @@ int spec_greedy_accept_commit(const float* logits, const int32_t* draft_ids,
                               int32_t* out_tokens, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/*
+ * Bytes of workspace spec_stochastic_accept needs (per row and 8192-entry
+ * vocabulary chunk: the chunk's maximum and exponential sum; per request
+ * and chunk: a draw weight).  Returns 0 on bad sizes.
+ */
+size_t spec_stochastic_workspace_size(int32_t batch, int32_t q_len,
+                                      int32_t vocab);
+
+/*
+ * Stochastic verify: acceptance by rejection sampling against target and
+ * draft probabilities ("MTP and DFlash2 at long context on XPU", Part II:
+ * sampling requires rejection sampling against target and draft
+ * probabilities; the rule is speculative sampling, Leviathan et al. 2023,
+ * "Fast Inference from Transformers via Speculative Decoding", and Chen et
+ * al. 2023).
+ *
+ * p_j = softmax(logits[b, j] / temperature[b]) is the target's distribution
+ * for the token after block position j; q_j the distribution draft j was
+ * drawn from.  For j = 1 .. q_b-1 in order, draft j is accepted iff
+ *     u_accept[b, j-1] * q_j(d_j) < p_{j-1}(d_j);
+ * at the first rejection the next token is drawn from the normalised
+ * residual max(0, p_{j-1} - q_j) (from p_{j-1} itself when that residual is
+ * zero everywhere); when every draft is accepted it is drawn from
+ * p_{q_b-1}.  A draw from weights w with the uniform u = u_sample[b] is the
+ * smallest token v with w(v) > 0 whose running sum w(0) + .. + w(v)
+ * exceeds u * sum(w).  The committed tokens then follow the target's
+ * distribution whatever the drafts.
+ *
+ * Arithmetic is float32 (the probabilities through exp2 of the scaled
+ * logit differences, the sums over 8192-token chunks); a decision whose
+ * two sides lie within float32 rounding of each other may come out
+ * differently from an exact evaluation.
+ *
+ *   logits       fp32 [batch * q_len, vocab], finite or -inf, at least one
+ *                finite entry per row that is read
+ *   draft_ids    int32 [batch, q_len], column 0 the boundary token
+ *   draft_probs  optional fp32 [batch, q_len - 1, vocab]: row j-1 is q_j
+ *                (non-negative); NULL means greedy drafts (q_j one-hot at
+ *                d_j)
+ *   q_lens       optional int32 [batch] rows per request, as in
+ *                spec_greedy_accept_commit (rows past q_b are not read)
+ *   temperature  fp32 [batch], > 0 (a request whose temperature is not
+ *                > 0 is treated as idle)
+ *   u_accept     fp32 [batch, q_len - 1] uniforms in [0, 1) (may be NULL
+ *                when q_len == 1); u_sample fp32 [batch] uniforms in [0, 1)
+ *   seq_lens / new_seq_lens, accept_len, next_token, out_tokens  as in
+ *                spec_greedy_accept_commit
+ *   workspace    >= spec_stochastic_workspace_size(batch, q_len, vocab)
+ *                bytes, 16-byte aligned; contents need no initialisation
+ * All pointers are device pointers, 4-byte aligned; three launches on
+ * `stream`, nothing copied to the host.
+ */
+int spec_stochastic_accept(const float* logits, const int32_t* draft_ids,
+                           const float* draft_probs, const int32_t* q_lens,
+                           int32_t batch, int32_t q_len, int32_t vocab,
+                           const float* temperature, const float* u_accept,
+                           const float* u_sample, const int32_t* seq_lens,
+                           int32_t* new_seq_lens, int32_t* accept_len,
+                           int32_t* next_token, int32_t* out_tokens,
+                           void* workspace, size_t workspace_bytes,
+                           void* stream);
+
 /* Verify width policies (spec_width_policy.policy). */
 #define SPEC_WIDTH_FIXED 0     /* always q_max rows */
 #define SPEC_WIDTH_EWMA 1      /* EWMA of the accepted count + offset */

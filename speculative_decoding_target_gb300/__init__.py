@@ -9,7 +9,9 @@ from ._native import (SpecError, accept_workspace_size, alloc_workspace,
                       desc_for, greedy_accept, greedy_accept_commit,
                       greedy_accept_commit_into, greedy_accept_into,
                       kv_append, load, make_desc, prepare_next_block,
-                      prepare_next_block_into, verify_attention,
+                      prepare_next_block_into, stochastic_accept,
+                      stochastic_accept_into, stochastic_workspace_size,
+                      verify_attention,
                       verify_attention_into, verify_status,
                       verify_workspace_size, width_policy)
 
@@ -17,7 +19,8 @@ __all__ = [
     "SpecError", "accept_workspace_size", "alloc_workspace", "desc_for",
     "greedy_accept", "greedy_accept_commit", "greedy_accept_commit_into",
     "greedy_accept_into", "kv_append", "load", "make_desc",
-    "prepare_next_block", "prepare_next_block_into", "verify_attention",
+    "prepare_next_block", "prepare_next_block_into", "stochastic_accept",
+    "stochastic_accept_into", "stochastic_workspace_size", "verify_attention",
     "verify_attention_into", "verify_status", "verify_workspace_size",
     "width_policy",
 ]

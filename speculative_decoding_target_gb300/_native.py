@@ -35,6 +35,7 @@ EXPORTED = (
     "spec_verify_status", "spec_accept_workspace_size", "spec_greedy_accept",
     "spec_last_error", "spec_version", "spec_verify_attention_noalloc",
     "spec_kv_append", "spec_greedy_accept_commit", "spec_prepare_next_block",
+    "spec_stochastic_workspace_size", "spec_stochastic_accept",
 )
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
@@ -101,6 +102,11 @@ def load(path: str = LIB_PATH):
         ctypes.POINTER(WidthPolicy), i32, P, P, P, P, P, P, i32, i32, i32, P,
         P, P, P, P, P, P]
     lib.spec_prepare_next_block.restype = ctypes.c_int
+    lib.spec_stochastic_workspace_size.argtypes = [i32, i32, i32]
+    lib.spec_stochastic_workspace_size.restype = sz
+    lib.spec_stochastic_accept.argtypes = [P, P, P, P, i32, i32, i32, P, P, P,
+                                           P, P, P, P, P, P, sz, P]
+    lib.spec_stochastic_accept.restype = ctypes.c_int
     lib.spec_last_error.argtypes = []
     lib.spec_last_error.restype = ctypes.c_char_p
     lib.spec_version.argtypes = []
@@ -320,6 +326,43 @@ def prepare_next_block(pol: WidthPolicy, q_lens, accept_len, next_token,
                             out["block_ids"], out["positions"],
                             out["cache_loc"], status, stream)
     return out
+
+
+def stochastic_workspace_size(batch: int, q_len: int, vocab: int) -> int:
+    return int(load().spec_stochastic_workspace_size(batch, q_len, vocab))
+
+
+def stochastic_accept_into(logits, draft_ids, draft_probs, q_lens,
+                           temperature, u_accept, u_sample, seq_lens,
+                           new_seq_lens, accept_len, next_token, out_tokens,
+                           workspace: torch.Tensor, stream=None) -> None:
+    B, q_len = draft_ids.shape
+    _check(load().spec_stochastic_accept(
+        _ptr(logits), _ptr(draft_ids), _ptr(draft_probs), _ptr(q_lens), B,
+        q_len, logits.shape[-1], _ptr(temperature), _ptr(u_accept),
+        _ptr(u_sample), _ptr(seq_lens), _ptr(new_seq_lens), _ptr(accept_len),
+        _ptr(next_token), _ptr(out_tokens), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+
+
+def stochastic_accept(logits, draft_ids, temperature, u_accept, u_sample, *,
+                      draft_probs=None, q_lens=None, seq_lens=None,
+                      workspace: Optional[torch.Tensor] = None, stream=None):
+    """Rejection-sampling verify.  Returns (accept_len, next_token,
+    out_tokens, new_seq_lens or None)."""
+    B, q_len = draft_ids.shape
+    dev = logits.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    acc, nxt = torch.empty(B, **i32), torch.empty(B, **i32)
+    toks = torch.empty((B, q_len), **i32)
+    new = torch.empty(B, **i32) if seq_lens is not None else None
+    if workspace is None:
+        workspace = alloc_workspace(
+            stochastic_workspace_size(B, q_len, logits.shape[-1]), dev)
+    stochastic_accept_into(logits, draft_ids, draft_probs, q_lens,
+                           temperature, u_accept, u_sample, seq_lens, new,
+                           acc, nxt, toks, workspace, stream)
+    return acc, nxt, toks, new
 
 
 def greedy_accept(logits: torch.Tensor, draft_ids: torch.Tensor, *,

@@ -10,6 +10,7 @@
 
 #include "append.cuh"
 #include "next_block.cuh"
+#include "stochastic.cuh"
 #include "common.cuh"
 #include "spec_verify.h"
 
@@ -453,6 +454,86 @@ int spec_prepare_next_block(const spec_width_policy* pol, int32_t batch,
       specv::launch_prepare_next_block(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return fail(SPEC_ERR_CUDA, "prepare kernel launch: %s", cudaGetErrorString(e));
+  return SPEC_OK;
+}
+
+size_t spec_stochastic_workspace_size(int32_t batch, int32_t q_len,
+                                      int32_t vocab) {
+  if (batch < 0 || q_len < 1 || q_len > 16 || vocab < 1) {
+    fail(SPEC_ERR_ARG, "batch %d / q_len %d / vocab %d", batch, q_len, vocab);
+    return 0;
+  }
+  const size_t chunks = (vocab + specv::kSampleChunk - 1) / specv::kSampleChunk;
+  const size_t rows = (size_t)batch * q_len;
+  return 2 * round_up(rows * chunks * sizeof(float), 256) +
+         round_up((size_t)batch * chunks * sizeof(float), 256);
+}
+
+int spec_stochastic_accept(const float* logits, const int32_t* draft_ids,
+                           const float* draft_probs, const int32_t* q_lens,
+                           int32_t batch, int32_t q_len, int32_t vocab,
+                           const float* temperature, const float* u_accept,
+                           const float* u_sample, const int32_t* seq_lens,
+                           int32_t* new_seq_lens, int32_t* accept_len,
+                           int32_t* next_token, int32_t* out_tokens,
+                           void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  g_err[0] = 0;
+  if (batch < 0) return fail(SPEC_ERR_ARG, "batch %d < 0", batch);
+  if (q_len < 1 || q_len > 16)
+    return fail(SPEC_ERR_ARG, "q_len %d outside [1, 16]", q_len);
+  if (vocab < 1) return fail(SPEC_ERR_ARG, "vocab %d < 1", vocab);
+  if ((long long)batch * q_len > 65535)
+    return fail(SPEC_ERR_ARG, "batch * q_len exceeds 65535");
+  if (batch == 0) return SPEC_OK;
+  if (!logits || !draft_ids || !temperature || !u_sample || !accept_len ||
+      !next_token || (q_len > 1 && !u_accept))
+    return fail(SPEC_ERR_ARG, "NULL tensor pointer");
+  if (!seq_lens != !new_seq_lens)
+    return fail(SPEC_ERR_ARG, "seq_lens and new_seq_lens go together");
+  const void* a4[] = {logits, draft_ids, draft_probs, q_lens, temperature,
+                      u_accept, u_sample, seq_lens, new_seq_lens, accept_len,
+                      next_token, out_tokens};
+  for (const void* q : a4)
+    if (q && !aligned(q, 4))
+      return fail(SPEC_ERR_ALIGN, "tensors must be 4-byte aligned");
+  if (!workspace) return fail(SPEC_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 16))
+    return fail(SPEC_ERR_ALIGN, "workspace must be 16-byte aligned");
+  const size_t need = spec_stochastic_workspace_size(batch, q_len, vocab);
+  if (workspace_bytes < need)
+    return fail(SPEC_ERR_WORKSPACE, "workspace %zu bytes < %zu needed",
+                workspace_bytes, need);
+  specv::StochasticParams p;
+  std::memset(&p, 0, sizeof p);
+  p.logits = logits;
+  p.draft_ids = draft_ids;
+  p.draft_probs = draft_probs;
+  p.q_lens = q_lens;
+  p.temperature = temperature;
+  p.u_accept = u_accept;
+  p.u_sample = u_sample;
+  p.seq_lens = seq_lens;
+  p.new_seq_lens = new_seq_lens;
+  p.accept_len = accept_len;
+  p.next_token = next_token;
+  p.out_tokens = out_tokens;
+  p.batch = batch;
+  p.q_len = q_len;
+  p.vocab = vocab;
+  p.chunks = (vocab + specv::kSampleChunk - 1) / specv::kSampleChunk;
+  p.vec4 = (vocab % 4 == 0) && aligned(logits, 16);
+  const size_t rows = (size_t)batch * q_len;
+  const size_t part = round_up(rows * p.chunks * sizeof(float), 256);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.part_max = reinterpret_cast<float*>(ws);
+  p.part_sum = reinterpret_cast<float*>(ws + part);
+  p.chunk_w = reinterpret_cast<float*>(ws + 2 * part);
+  cudaError_t e =
+      specv::launch_stochastic_accept(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(SPEC_ERR_CUDA, "stochastic accept launch: %s",
+                cudaGetErrorString(e));
   return SPEC_OK;
 }
 

@@ -198,3 +198,24 @@ def test_prepare_next_block_argument_checks(lib):
     assert call(ok, cache_loc=ctypes.c_void_p(0x100004)) == \
         _native.SPEC_ERR_ALIGN
     assert call(ok, batch=-1) == _native.SPEC_ERR_ARG
+
+
+def test_stochastic_accept_argument_checks(lib):
+    f = lib.spec_stochastic_accept
+
+    def call(q_len=8, u_accept=FAKE, seq=None, new=None, temp=FAKE,
+             ws_bytes=1 << 24, ws=FAKE, probs=None):
+        return f(FAKE, FAKE, probs, None, 2, q_len, 1000, temp, u_accept,
+                 FAKE, seq, new, FAKE, FAKE, None, ws, ws_bytes, None)
+
+    assert call(q_len=0) == _native.SPEC_ERR_ARG
+    assert call(q_len=17) == _native.SPEC_ERR_ARG
+    assert call(u_accept=None) == _native.SPEC_ERR_ARG
+    assert call(temp=None) == _native.SPEC_ERR_ARG
+    assert call(seq=FAKE) == _native.SPEC_ERR_ARG
+    assert call(probs=ctypes.c_void_p(0x100002)) == _native.SPEC_ERR_ALIGN
+    assert call(ws=None) == _native.SPEC_ERR_WORKSPACE
+    need = lib.spec_stochastic_workspace_size(2, 8, 1000)
+    assert need > 0
+    assert call(ws_bytes=need - 1) == _native.SPEC_ERR_WORKSPACE
+    assert lib.spec_stochastic_workspace_size(2, 0, 1000) == 0
