@@ -374,6 +374,9 @@ def run_gpu(args, w: wl.VerifyWorkload):
     if not args.no_ragged:
         result["ragged"] = measure_ragged(w, inp, dev, args.steps,
                                           args.warmup, attn_avg_s)
+    if not args.no_stochastic:
+        result["stochastic"] = measure_stochastic(w, inp, dev, args.steps,
+                                                  args.warmup, peak)
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         host_inp = {k: (v.cpu() if torch.is_tensor(v) else v)
                     for k, v in inp.items()}
@@ -538,6 +541,60 @@ def measure_ragged(w: wl.VerifyWorkload, inp, dev, steps: int, warmup: int,
     }
 
 
+# ------------------------------------------------------ stochastic verify --
+
+def measure_stochastic(w: wl.VerifyWorkload, inp, dev, steps: int,
+                       warmup: int, peak: float):
+    """Rejection-sampling accept on the workload's logits: greedy drafts
+    (no draft probabilities) and drafts with full draft distributions
+    (B x (q_len - 1) x V fp32, the residual row read at a rejection).
+    Temperature 1, seeded uniforms; CUDA events per call."""
+    import speculative_decoding_target_gb300 as sv
+    B, q, V = w.batch, w.q_len, w.vocab
+    g = torch.Generator(device=dev).manual_seed(w.seed + 31)
+    temp = torch.ones(B, device=dev)
+    ua = torch.rand((B, max(q - 1, 1)), generator=g, device=dev)
+    us = torch.rand(B, generator=g, device=dev)
+    probs = torch.softmax(torch.randn((B, max(q - 1, 1), V), generator=g,
+                                      device=dev), dim=-1)
+    ws = sv.alloc_workspace(sv.stochastic_workspace_size(B, q, V), dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    acc, nxt = torch.empty(B, **i32), torch.empty(B, **i32)
+    toks = torch.empty((B, q), **i32)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for name, dp in (("greedy_drafts", None), ("draft_probs", probs)):
+        def call():
+            sv.stochastic_accept_into(inp["logits"], inp["draft_ids"], dp,
+                                      None, temp, ua, us, None, None, acc,
+                                      nxt, toks, ws, stream)
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        out[name + "_ms"] = round(ms, 5)
+    logit_bytes = B * q * V * 4
+    out.update({
+        "logits_bytes": logit_bytes,
+        "logits_gbs_greedy_drafts": round(
+            logit_bytes / (out["greedy_drafts_ms"] * 1e-3) / 1e9, 1),
+        "frac_of_peak_greedy_drafts": round(
+            logit_bytes / (out["greedy_drafts_ms"] * 1e-3) / 1e9 / peak, 4),
+        "gpu_launches": 3 * 2 * steps,
+        "note": "three launches per call: one streaming pass over the logits "
+                "(softmax statistics), per-chunk draw weights, the draw; "
+                "temperature 1, seeded uniforms",
+    })
+    return out
+
+
 # ----------------------------------------------------------- CPU baseline --
 
 def _oracle_step_estimate(w, host_inp, n_rows: int, n_acc_rows: int, rng):
@@ -645,6 +702,8 @@ def main():
                     help="skip the block KV append timing")
     ap.add_argument("--no-ragged", action="store_true",
                     help="skip the per-request width (ragged) step timing")
+    ap.add_argument("--no-stochastic", action="store_true",
+                    help="skip the rejection-sampling accept timing")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--ref-rows", type=int, default=48)
     args = ap.parse_args()

@@ -272,7 +272,7 @@ size_t spec_stochastic_workspace_size(int32_t batch, int32_t q_len,
  * differently from an exact evaluation.
  *
  *   logits       fp32 [batch * q_len, vocab], finite or -inf, at least one
- *                finite entry per row that is read
+ *                finite entry per row that is read; vocab <= 1,048,576
  *   draft_ids    int32 [batch, q_len], column 0 the boundary token
  *   draft_probs  optional fp32 [batch, q_len - 1, vocab]: row j-1 is q_j
  *                (non-negative); NULL means greedy drafts (q_j one-hot at

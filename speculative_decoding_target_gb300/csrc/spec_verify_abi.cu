@@ -482,7 +482,9 @@ int spec_stochastic_accept(const float* logits, const int32_t* draft_ids,
   if (batch < 0) return fail(SPEC_ERR_ARG, "batch %d < 0", batch);
   if (q_len < 1 || q_len > 16)
     return fail(SPEC_ERR_ARG, "q_len %d outside [1, 16]", q_len);
-  if (vocab < 1) return fail(SPEC_ERR_ARG, "vocab %d < 1", vocab);
+  if (vocab < 1 || vocab > specv::kMaxSampleChunks * specv::kSampleChunk)
+    return fail(SPEC_ERR_ARG, "vocab %d outside [1, %d]", vocab,
+                specv::kMaxSampleChunks * specv::kSampleChunk);
   if ((long long)batch * q_len > 65535)
     return fail(SPEC_ERR_ARG, "batch * q_len exceeds 65535");
   if (batch == 0) return SPEC_OK;

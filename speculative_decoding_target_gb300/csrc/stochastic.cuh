@@ -28,6 +28,7 @@ struct StochasticParams {
 
 constexpr int kSampleChunk = 8192;   // logits per CTA of the streaming pass
 constexpr int kSampleThreads = 256;
+constexpr int kMaxSampleChunks = 128;  // vocab <= 128 * 8192
 
 cudaError_t launch_stochastic_accept(const StochasticParams& p,
                                      cudaStream_t s);

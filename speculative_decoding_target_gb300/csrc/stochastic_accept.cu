@@ -12,10 +12,10 @@
 //   1. softmax_partial_kernel, CTA (chunk, row): the chunk's maximum M and
 //      sum exp2((x - M) k), k = log2(e) / T, in one streaming pass over the
 //      logits (rows past a request's width are skipped unread);
-//   2. residual_chunk_kernel, CTA (chunk, request): the accept walk (cheap,
-//      repeated by every CTA of the request), then the chunk's total draw
-//      weight;
-//   3. sample_finalize_kernel, one CTA per request: the walk again, the
+//   2. residual_chunk_kernel, CTA (chunk, request): the accept tests (one
+//      warp per block row, all rows side by side; repeated by every CTA of
+//      the request), then the chunk's total draw weight;
+//   3. sample_finalize_kernel, one CTA per request: the tests again, the
 //      chunk that holds u * W, and a block scan of that chunk alone.
 // Every float step that decides an integer goes through the same device
 // functions in kernels 2 and 3 with explicitly rounded operations, so both
@@ -102,32 +102,41 @@ __global__ void __launch_bounds__(kSampleThreads)
 }
 
 struct RowStats {
-  float m, z, k;
+  float m, z, k, inv_z;   // inv_z = 1/z rounded once: p(v) = e(v) * inv_z
 };
 
 // (max, normaliser) of a row from its chunk partials; one warp, fixed
-// order, identical on every lane and in every kernel.
+// order, identical on every lane and in every kernel.  Lane l holds chunks
+// l, l + 32, ... (at most kMaxSampleChunks / 32 of them), loaded in one go.
 __device__ RowStats row_stats(const StochasticParams& p, int row, float k) {
+  constexpr int kPerLane = kMaxSampleChunks / 32;
   const int lane = threadIdx.x & 31;
   const float* pm = p.part_max + (long long)row * p.chunks;
   const float* ps = p.part_sum + (long long)row * p.chunks;
-  float m = -INFINITY;
-  for (int c = lane; c < p.chunks; c += 32) m = fmaxf(m, pm[c]);
+  float cm[kPerLane], cs[kPerLane];
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int c = lane + 32 * i;
+    cm[i] = c < p.chunks ? pm[c] : -INFINITY;
+    cs[i] = c < p.chunks ? ps[c] : 0.f;
+  }
+  float m = cm[0];
+#pragma unroll
+  for (int i = 1; i < kPerLane; ++i) m = fmaxf(m, cm[i]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float z = 0.f;
-  for (int c = lane; c < p.chunks; c += 32) {
-    const float sc = ps[c];
-    if (sc > 0.f)
-      z = __fadd_rn(z, __fmul_rn(sc, exp2f(__fmul_rn(__fsub_rn(pm[c], m), k))));
-  }
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i)
+    if (cs[i] > 0.f)
+      z = __fadd_rn(z, __fmul_rn(cs[i], exp2f(__fmul_rn(__fsub_rn(cm[i], m), k))));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) z = __fadd_rn(z, __shfl_xor_sync(0xffffffffu, z, o));
-  return {m, z, k};
+  return {m, z, k, __frcp_rn(z)};
 }
 
 __device__ __forceinline__ float prob(const RowStats& r, float x) {
-  return __fdiv_rn(exp2f(__fmul_rn(__fsub_rn(x, r.m), r.k)), r.z);
+  return __fmul_rn(exp2f(__fmul_rn(__fsub_rn(x, r.m), r.k)), r.inv_z);
 }
 
 struct Walk {
@@ -135,73 +144,118 @@ struct Walk {
   RowStats fin;   // statistics of the row the next token is drawn from
 };
 
-// The accept tests, run by one full warp (every lane gets the result).
-__device__ Walk walk(const StochasticParams& p, int b) {
-  Walk w;
-  w.qb = rows_of(p, b);
-  w.a = 0;
-  w.rejected = 0;
-  w.drej = -1;
-  if (w.qb == 0 || !(p.temperature[b] > 0.f)) {
-    w.qb = 0;
-    return w;
-  }
-  const float k = k_of(p, b);
-  const int32_t* dr = p.draft_ids + (long long)b * p.q_len;
+struct WalkSmem {
+  RowStats stats[16];
+  int ok[16];
+  Walk walk;
+};
+
+// The accept tests of request b, run by the whole CTA: warp w takes rows
+// w, w + warps, ... (their statistics and the test of the draft each row
+// scores), then thread 0 counts the leading accepted drafts.  Every test is
+// independent of the others, so they run side by side; the result is the
+// same in every kernel that calls this.  Ends with the CTA synchronised and
+// the walk in sm->walk.
+__device__ void decide(const StochasticParams& p, int b, WalkSmem* sm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  const bool live = p.temperature[b] > 0.f;
+  const int qb = live ? rows_of(p, b) : 0;
   const long long row0 = (long long)b * p.q_len;
-  for (int j = 1; j < w.qb; ++j) {
-    const RowStats r = row_stats(p, (int)(row0 + j - 1), k);
-    const int d = dr[j];
-    float pd = 0.f, qd = 1.f;
-    if (d >= 0 && d < p.vocab) {
-      pd = prob(r, p.logits[(row0 + j - 1) * p.vocab + d]);
-      if (p.draft_probs)
-        qd = p.draft_probs[((long long)b * (p.q_len - 1) + j - 1) * p.vocab + d];
-    }
-    const float u = p.u_accept[(long long)b * (p.q_len - 1) + j - 1];
-    if (__fmul_rn(u, qd) < pd) {
-      ++w.a;
-    } else {
-      w.rejected = 1;
-      w.drej = d;
-      break;
+  const int32_t* dr = p.draft_ids + row0;
+  if (qb > 0) {
+    const float k = k_of(p, b);
+    for (int j = warp; j < qb; j += nw) {
+      // the inputs of the test are independent of the statistics: load first
+      float x = 0.f, qd = 1.f, u = 0.f;
+      int d = -1;
+      if (j + 1 < qb) {
+        d = dr[j + 1];
+        u = p.u_accept[(long long)b * (p.q_len - 1) + j];
+        if (d >= 0 && d < p.vocab) {
+          x = p.logits[(row0 + j) * p.vocab + d];
+          if (p.draft_probs)
+            qd = p.draft_probs[((long long)b * (p.q_len - 1) + j) * p.vocab + d];
+        }
+      }
+      const RowStats r = row_stats(p, (int)(row0 + j), k);
+      int ok = 1;
+      if (j + 1 < qb) {
+        const float pd = (d >= 0 && d < p.vocab) ? prob(r, x) : 0.f;
+        ok = __fmul_rn(u, qd) < pd;   // accept draft j + 1
+      }
+      if (lane == 0) {
+        sm->stats[j] = r;
+        sm->ok[j] = ok;
+      }
     }
   }
-  w.fin = row_stats(p, (int)(row0 + w.a), k);
-  return w;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Walk w;
+    w.qb = qb;
+    w.a = 0;
+    w.rejected = 0;
+    w.drej = -1;
+    if (qb > 0) {
+      while (w.a + 1 < qb && sm->ok[w.a]) ++w.a;
+      w.rejected = w.a + 1 < qb;
+      if (w.rejected) w.drej = dr[w.a + 1];
+      w.fin = sm->stats[w.a];
+    }
+    sm->walk = w;
+  }
+  __syncthreads();
 }
 
-// Draw weight of token v of the final row: p, or max(0, p - q) after a
-// rejection (q one-hot at the rejected draft for a greedy drafter).
-__device__ __forceinline__ float weight(const StochasticParams& p, int b,
-                                        const Walk& w, bool residual,
-                                        float x, int v) {
-  const float pv = prob(w.fin, x);
-  if (!residual) return pv;
-  const float qv = p.draft_probs
-      ? p.draft_probs[((long long)b * (p.q_len - 1) + w.a) * p.vocab + v]
-      : (v == w.drej ? 1.f : 0.f);
-  return pv > qv ? __fsub_rn(pv, qv) : 0.f;
+// Sum of the kMaxSampleChunks chunk weights in s_cw, by one warp in a fixed
+// order (lane l adds chunks 4l..4l+3, then a butterfly): the same on every
+// lane.
+__device__ __forceinline__ float chunk_total(const float* s_cw, int lane) {
+  constexpr int kPerLane = kMaxSampleChunks / 32;
+  float part = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) part = __fadd_rn(part, s_cw[lane * kPerLane + i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
+  return part;
 }
+
+// Draw weight of a token of the final row, written out where it is used:
+// p, or max(0, p - q) after a rejection (q one-hot at the rejected draft for
+// a greedy drafter).  Both kernels evaluate the same expression.
 
 __global__ void __launch_bounds__(kSampleThreads)
     residual_chunk_kernel(const StochasticParams p) {
   __shared__ float red[kSampleThreads / 32];
-  __shared__ Walk s_walk;
+  __shared__ WalkSmem sm;
   const int chunk = blockIdx.x, b = blockIdx.y;
-  if (threadIdx.x < 32) {
-    const Walk w = walk(p, b);
-    if (threadIdx.x == 0) s_walk = w;
-  }
-  __syncthreads();
-  const Walk w = s_walk;
+  decide(p, b, &sm);
+  const Walk w = sm.walk;
   if (w.qb == 0 || !w.rejected) return;  // only a rejection needs W_c
-  const float* x = p.logits + ((long long)b * p.q_len + w.a) * p.vocab;
+  constexpr int kPer = kSampleChunk / kSampleThreads;
+  const long long frow = (long long)b * p.q_len + w.a;
+  const float* x = p.logits + frow * p.vocab;
+  const float* qrow = p.draft_probs
+      ? p.draft_probs + ((long long)b * (p.q_len - 1) + w.a) * p.vocab
+      : nullptr;
   const int begin = chunk * kSampleChunk;
-  const int end = min(begin + kSampleChunk, p.vocab);
+  // every load of the chunk is issued before any is used
+  float xv[kPer], qv[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const int v = begin + threadIdx.x + e * kSampleThreads;
+    xv[e] = v < p.vocab ? x[v] : -INFINITY;
+    qv[e] = qrow ? (v < p.vocab ? qrow[v] : 0.f)
+                 : (v == w.drej ? 1.f : 0.f);
+  }
   float s = 0.f;
-  for (int v = begin + threadIdx.x; v < end; v += kSampleThreads)
-    s = __fadd_rn(s, weight(p, b, w, true, x[v], v));
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const float pv = prob(w.fin, xv[e]);
+    s = __fadd_rn(s, pv > qv[e] ? __fsub_rn(pv, qv[e]) : 0.f);
+  }
   const float W = block_sum(s, red);
   if (threadIdx.x == 0) p.chunk_w[(long long)b * p.chunks + chunk] = W;
 }
@@ -209,18 +263,18 @@ __global__ void __launch_bounds__(kSampleThreads)
 __global__ void __launch_bounds__(kSampleThreads)
     sample_finalize_kernel(const StochasticParams p) {
   constexpr int kPer = kSampleChunk / kSampleThreads;  // 32 per thread
-  __shared__ float red[kSampleThreads / 32];
-  __shared__ float s_scan[kSampleThreads];
-  __shared__ Walk s_walk;
-  __shared__ int s_chunk, s_pick, s_residual;
+  constexpr int kWarps = kSampleThreads / 32;
+  __shared__ WalkSmem sm;
+  __shared__ float s_cw[kMaxSampleChunks];
+  __shared__ float s_w[kSampleThreads * (kPer + 1)];
+  __shared__ float s_warp[kWarps];
+  __shared__ int s_found[kWarps], s_last[kWarps];
+  __shared__ int s_chunk, s_residual;
   __shared__ float s_base, s_target;
   const int b = blockIdx.x;
-  if (threadIdx.x < 32) {
-    const Walk w = walk(p, b);
-    if (threadIdx.x == 0) s_walk = w;
-  }
-  __syncthreads();
-  const Walk w = s_walk;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  decide(p, b, &sm);
+  const Walk w = sm.walk;
   if (w.qb == 0) {
     if (threadIdx.x == 0) {
       p.accept_len[b] = 0;
@@ -233,109 +287,150 @@ __global__ void __launch_bounds__(kSampleThreads)
     return;
   }
   const long long frow = (long long)b * p.q_len + w.a;
-  if (threadIdx.x == 0) {
-    // chunk weights: the residual's, else p's (from the row statistics);
-    // a residual that sums to zero (p == q) falls back to p
-    float W = 0.f;
-    if (w.rejected)
-      for (int c = 0; c < p.chunks; ++c)
-        W = __fadd_rn(W, p.chunk_w[(long long)b * p.chunks + c]);
-    const int residual = w.rejected && W > 0.f;
-    const float* pm = p.part_max + frow * p.chunks;
-    const float* ps = p.part_sum + frow * p.chunks;
-    auto cw = [&](int c) {
-      if (residual) return p.chunk_w[(long long)b * p.chunks + c];
-      const float sc = ps[c];
-      return sc > 0.f ? __fdiv_rn(__fmul_rn(sc, exp2f(__fmul_rn(
-                                     __fsub_rn(pm[c], w.fin.m), w.fin.k))),
-                                  w.fin.z)
-                      : 0.f;
-    };
+  // chunk weights in shared memory: the residual's (from kernel 2), else
+  // p's from the row statistics; a zero residual (p == q) falls back to p
+  const float* pm = p.part_max + frow * p.chunks;
+  const float* ps = p.part_sum + frow * p.chunks;
+  for (int c = threadIdx.x; c < kMaxSampleChunks; c += kSampleThreads)
+    s_cw[c] = w.rejected && c < p.chunks ? p.chunk_w[(long long)b * p.chunks + c]
+                                          : 0.f;
+  __syncthreads();
+  if (warp == 0) {
+    float W = chunk_total(s_cw, lane);
+    bool residual = w.rejected && W > 0.f;
     if (!residual) {
-      W = 0.f;
-      for (int c = 0; c < p.chunks; ++c) W = __fadd_rn(W, cw(c));
+      for (int c = lane; c < kMaxSampleChunks; c += 32) {
+        float v = 0.f;
+        if (c < p.chunks && ps[c] > 0.f)
+          v = __fmul_rn(__fmul_rn(ps[c], exp2f(__fmul_rn(__fsub_rn(pm[c], w.fin.m),
+                                                         w.fin.k))),
+                        w.fin.inv_z);
+        s_cw[c] = v;
+      }
+      __syncwarp();
+      W = chunk_total(s_cw, lane);
     }
+    // the first chunk whose running sum exceeds u * W: lane l scans chunks
+    // 4l .. 4l+3 after an exclusive warp scan of the lanes' sums
     const float target = __fmul_rn(p.u_sample[b], W);
-    float run = 0.f;
-    int cs = -1;
-    for (int c = 0; c < p.chunks; ++c) {
-      const float nx = __fadd_rn(run, cw(c));
-      if (nx > target) {
-        cs = c;
-        break;
+    constexpr int kPerLane = kMaxSampleChunks / 32;
+    float cw[kPerLane], part = 0.f;
+#pragma unroll
+    for (int i2 = 0; i2 < kPerLane; ++i2) {
+      cw[i2] = s_cw[lane * kPerLane + i2];
+      part = __fadd_rn(part, cw[i2]);
+    }
+    float inc = part;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc = __fadd_rn(inc, y);
+    }
+    float run = __fsub_rn(inc, part), base = 0.f;
+    int cs = INT_MAX;
+#pragma unroll
+    for (int i2 = 0; i2 < kPerLane; ++i2) {
+      const float nx = __fadd_rn(run, cw[i2]);
+      if (cs == INT_MAX && cw[i2] > 0.f && nx > target) {
+        cs = lane * kPerLane + i2;
+        base = run;
       }
       run = nx;
     }
-    if (cs < 0) {  // rounding put u * W at the very end: last nonzero chunk
-      for (int c = p.chunks - 1; c >= 0; --c)
-        if (cw(c) > 0.f) {
-          cs = c;
-          break;
-        }
-      run = -INFINITY;  // any index of that chunk qualifies; take the last
+    const int first = __reduce_min_sync(0xffffffffu, cs);
+    int last = -1;
+#pragma unroll
+    for (int i2 = 0; i2 < kPerLane; ++i2)
+      if (cw[i2] > 0.f) last = lane * kPerLane + i2;
+    last = __reduce_max_sync(0xffffffffu, last);
+    if (lane == 0) {
+      s_residual = residual;
+      s_target = target;
+      if (first != INT_MAX) {
+        s_chunk = first;
+      } else {  // rounding put u * W at the very end: last nonzero chunk
+        s_chunk = last >= 0 ? last : 0;
+        s_base = -INFINITY;  // any index of that chunk qualifies: the last
+      }
     }
-    s_chunk = cs;
-    s_base = run;
-    s_target = target;
-    s_residual = residual;
-    s_pick = INT_MAX;
+    if (first != INT_MAX && cs == first) s_base = base;
   }
   __syncthreads();
   const int cs = s_chunk;
   const bool residual = s_residual;
   const float* x = p.logits + frow * p.vocab;
+  const float* qrow = residual && p.draft_probs
+      ? p.draft_probs + ((long long)b * (p.q_len - 1) + w.a) * p.vocab
+      : nullptr;
   const int begin = cs * kSampleChunk;
-  // thread t scans the kPer consecutive tokens begin + t*kPer ...
-  const int v0 = begin + threadIdx.x * kPer;
-  float wv[kPer];
-  float tot = 0.f;
+  // stage the chunk's weights in shared memory with coalesced loads, then
+  // let thread t scan tokens begin + t*kPer ... (rows padded by one float
+  // so the column reads hit 32 different banks)
+  {
+    float xv[kPer], qv[kPer];  // every load issued before any is used
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    const int v = v0 + e;
-    wv[e] = v < p.vocab ? weight(p, b, w, residual, x[v], v) : 0.f;
-    tot = __fadd_rn(tot, wv[e]);
-  }
-  // exclusive scan of the thread totals (sequential over warps, fixed order)
-  s_scan[threadIdx.x] = tot;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float run = 0.f;
-    for (int t = 0; t < kSampleThreads; ++t) {
-      const float c = s_scan[t];
-      s_scan[t] = run;
-      run = __fadd_rn(run, c);
+    for (int e = 0; e < kPer; ++e) {
+      const int v = begin + e * kSampleThreads + threadIdx.x;
+      xv[e] = v < p.vocab ? x[v] : -INFINITY;
+      qv[e] = qrow ? (v < p.vocab ? qrow[v] : 0.f)
+                   : (residual && v == w.drej ? 1.f : 0.f);
+    }
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int i2 = e * kSampleThreads + threadIdx.x;
+      const float pv = prob(w.fin, xv[e]);
+      s_w[(i2 / kPer) * (kPer + 1) + i2 % kPer] =
+          !residual ? pv : (pv > qv[e] ? __fsub_rn(pv, qv[e]) : 0.f);
     }
   }
   __syncthreads();
+  const int v0 = begin + threadIdx.x * kPer;
+  const float* mine = s_w + threadIdx.x * (kPer + 1);
+  float tot = 0.f;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) tot = __fadd_rn(tot, mine[e]);
+  // exclusive prefix of the thread totals: warp shuffle scan, then the warp
+  // totals in order (a fixed pattern, so the same sums every time)
+  float inc = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc = __fadd_rn(inc, y);
+  }
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  float wbase = 0.f;
+  for (int i2 = 0; i2 < warp; ++i2) wbase = __fadd_rn(wbase, s_warp[i2]);
+  const float excl = __fadd_rn(wbase, __fsub_rn(inc, tot));
   int found = INT_MAX, last_nz = -1;
   if (s_base == -INFINITY) {  // fallback: the chunk's last nonzero weight
 #pragma unroll
     for (int e = 0; e < kPer; ++e)
-      if (wv[e] > 0.f) last_nz = v0 + e;
+      if (mine[e] > 0.f) last_nz = v0 + e;
   } else {
-    float run = __fadd_rn(s_base, s_scan[threadIdx.x]);
+    float run = __fadd_rn(s_base, excl);
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
-      run = __fadd_rn(run, wv[e]);
-      if (found == INT_MAX && wv[e] > 0.f && run > s_target) found = v0 + e;
-      if (wv[e] > 0.f) last_nz = v0 + e;
+      run = __fadd_rn(run, mine[e]);
+      if (found == INT_MAX && mine[e] > 0.f && run > s_target) found = v0 + e;
+      if (mine[e] > 0.f) last_nz = v0 + e;
     }
   }
   found = __reduce_min_sync(0xffffffffu, found);
   last_nz = __reduce_max_sync(0xffffffffu, last_nz);
-  if ((threadIdx.x & 31) == 0) {
-    atomicMin(&s_pick, found);
-    reinterpret_cast<int*>(red)[threadIdx.x >> 5] = last_nz;
+  if (lane == 0) {
+    s_found[warp] = found;
+    s_last[warp] = last_nz;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int pick = s_pick;
-    if (pick == INT_MAX) {  // rounding between the two sums: last nonzero
-      for (int i = 0; i < kSampleThreads / 32; ++i)
-        pick = pick == INT_MAX ? reinterpret_cast<int*>(red)[i]
-                               : max(pick, reinterpret_cast<int*>(red)[i]);
-      if (pick < 0) pick = begin;
+    int pick = INT_MAX, last = -1;
+    for (int i2 = 0; i2 < kWarps; ++i2) {
+      pick = min(pick, s_found[i2]);
+      last = max(last, s_last[i2]);
     }
+    if (pick == INT_MAX)  // rounding between the two sums: last nonzero
+      pick = last >= 0 ? last : begin;
     const int32_t* dr = p.draft_ids + (long long)b * p.q_len;
     p.accept_len[b] = w.a;
     p.next_token[b] = pick;
