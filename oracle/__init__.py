@@ -94,6 +94,10 @@ def _load():
     lib.oracle_stochastic_accept.argtypes = [P, P, P, P, i32, i32, i64, P, P,
                                              P, P, P, P, P, P, P, i32]
     lib.oracle_stochastic_accept.restype = ctypes.c_int
+    lib.oracle_dflash2_select.argtypes = [P, P, P, P, P, P, i32, i32, i64,
+                                          i32, i32, i32, i32, P, P, P, P, P,
+                                          i32]
+    lib.oracle_dflash2_select.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -354,3 +358,43 @@ def stochastic_accept(logits, draft_ids, temperature, u_accept, u_sample, *,
     if nsl is not None:
         res["new_seq_lens"] = nsl
     return res
+
+
+SELECT_MODES = {"greedy": 0, "map": 1}
+
+
+def dflash2_select(cand_logits, boundary, hidden_bits, w_h_bits, code_a_bits,
+                   code_b_bits, *, top: int = 16, mode: str = "greedy",
+                   threads: int = 0):
+    """DFlash2 candidate selection in float64.
+
+    cand_logits fp32 [B, P-1, V]; boundary int32 [B]; hidden_bits bf16 bits
+    [B, P-1, D]; w_h_bits [R, D]; code_a_bits, code_b_bits [V, R].
+    Returns dict: cand_ids [B, P-1, K], cand_logit [B, P-1, K], trans
+    [B, P-1, K, K], draft_ids [B, P], margin [B].
+    """
+    cl = _c(cand_logits, np.float32)
+    B, P1, V = cl.shape
+    bd = _c(boundary, np.int32).reshape(B)
+    hb = _c(hidden_bits, np.uint16)
+    D = hb.shape[2]
+    assert hb.shape == (B, P1, D)
+    wh = _c(w_h_bits, np.uint16)
+    R = wh.shape[0]
+    assert wh.shape == (R, D)
+    ca = _c(code_a_bits, np.uint16)
+    cb = _c(code_b_bits, np.uint16)
+    assert ca.shape == (V, R) and cb.shape == (V, R)
+    out = {"cand_ids": np.zeros((B, P1, top), np.int32),
+           "cand_logit": np.zeros((B, P1, top), np.float64),
+           "trans": np.zeros((B, P1, top, top), np.float64),
+           "draft_ids": np.zeros((B, P1 + 1), np.int32),
+           "margin": np.zeros(B, np.float64)}
+    rc = _load().oracle_dflash2_select(
+        _ptr(cl), _ptr(bd), _ptr(hb), _ptr(wh), _ptr(ca), _ptr(cb), B,
+        P1 + 1, V, top, R, D, SELECT_MODES[mode], _ptr(out["cand_ids"]),
+        _ptr(out["cand_logit"]), _ptr(out["trans"]), _ptr(out["draft_ids"]),
+        _ptr(out["margin"]), int(threads or default_threads()))
+    if rc != ORACLE_OK:
+        raise ValueError(f"oracle_dflash2_select failed with code {rc}")
+    return out

@@ -77,6 +77,21 @@
  *     accepted it is drawn from p_{q_b-1}.  A draw from weights w with the
  *     uniform u is the smallest v whose running sum exceeds u * sum(w).
  *
+ *  8. DFlash2 candidate selector ("MTP and DFlash2 at long context on XPU",
+ *     "The part that makes DFlash2 different" and "Selector and recurrent
+ *     math"; "Qwen3.8-27B-FP8" page: selector_rank = 256, selector_top_k =
+ *     16, and an exact MAP over the chain as an option).  Each draft
+ *     position t = 1 .. P-1 keeps the K best tokens of its candidate logits
+ *     (larger logit first, lower token id on ties).  A transition from
+ *     candidate a at t-1 (the boundary token at t = 0) to candidate b at t
+ *     scores S_t(a, b) = U_t(b) + sum_r A[a, r] H_t[r] B[b, r], with U_t(b)
+ *     the candidate's logit, A and B the predecessor and successor
+ *     codebooks (rows indexed by token id, rank R) and H_t = W_H h_t the
+ *     projection of the draft hidden state at t.  The greedy walk starts at
+ *     the boundary and takes at each position the best successor of the
+ *     token already chosen (lowest candidate rank on ties); the MAP walk
+ *     maximises the sum of S_t along the chain.
+ *
  * Parity of this oracle against any engine on the pages is unpinned: the
  * pages print no output for a concrete input tensor.  It is pinned instead
  * by tests against library routines (torch scaled-dot-product attention in
@@ -814,6 +829,185 @@ int oracle_stochastic_accept(const float* logits, const int32_t* draft_ids,
     }
     if (new_seq_lens) new_seq_lens[b] = seq_lens[b] - qb + a + 1;
     if (margin) margin[b] = mg;
+  }
+  return err;
+}
+
+/* ---- DFlash2 candidate selector -------------------------------------------- */
+
+#define ORACLE_SELECT_GREEDY 0
+#define ORACLE_SELECT_MAP 1
+
+/* The k best entries of x[0..n) in order: larger value first, lower index on
+ * ties.  Insertion into a sorted list of k. */
+static void top_k(const float* x, int64_t n, int k, int32_t* ids, float* vals) {
+  int have = 0;
+  for (int64_t v = 0; v < n; ++v) {
+    const float xv = x[v];
+    if (have == k && !(xv > vals[k - 1])) continue; /* ties keep the lower id */
+    int pos = have < k ? have : k - 1;
+    while (pos > 0 && xv > vals[pos - 1]) {
+      vals[pos] = vals[pos - 1];
+      ids[pos] = ids[pos - 1];
+      --pos;
+    }
+    vals[pos] = xv;
+    ids[pos] = (int32_t)v;
+    if (have < k) ++have;
+  }
+  for (int i = have; i < k; ++i) {
+    ids[i] = -1;
+    vals[i] = -INFINITY;
+  }
+}
+
+/*
+ * cand_logits  fp32 [B, P-1, V]: row t-1 scores draft position t
+ * boundary     int32 [B]: the verified token at position 0
+ * hidden       bf16 bits [B, P-1, D]: draft hidden state of position t
+ * w_h          bf16 bits [R, D]: the projection H = W_H h
+ * code_a, code_b  bf16 bits [V, R]: predecessor / successor codebooks
+ * mode         ORACLE_SELECT_GREEDY or ORACLE_SELECT_MAP
+ * cand_ids     int32 [B, P-1, K] out; cand_logit fp32-as-double [B, P-1, K]
+ * trans        fp64 [B, P-1, K, K] out: trans[b, t-1, a, c] = S_t(a, c)
+ *              with a the predecessor's rank (t = 1: only a = 0, the
+ *              boundary; rows a >= 1 are -inf)
+ * draft_ids    int32 [B, P] out: [boundary, c_1, .., c_{P-1}]
+ * margin       fp64 [B] out (optional): the smallest gap between the best
+ *              and the runner-up score over every max this request took
+ */
+int oracle_dflash2_select(const float* cand_logits, const int32_t* boundary,
+                          const uint16_t* hidden, const uint16_t* w_h,
+                          const uint16_t* code_a, const uint16_t* code_b,
+                          int32_t batch, int32_t positions, int64_t vocab,
+                          int32_t top, int32_t rank, int32_t dim, int32_t mode,
+                          int32_t* cand_ids, double* cand_logit, double* trans,
+                          int32_t* draft_ids, double* margin,
+                          int32_t nthreads) {
+  if (batch < 0 || positions < 2 || positions > 16 || top < 1 || top > 16 ||
+      rank < 1 || dim < 1 || vocab < top || (mode != 0 && mode != 1))
+    return ORACLE_ERR_ARG;
+  const int P1 = positions - 1, K = top;
+  int err = ORACLE_OK;
+#ifdef _OPENMP
+  if (nthreads < 1) nthreads = omp_get_max_threads();
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1)
+#endif
+  for (int b = 0; b < batch; ++b) {
+    double* hh = (double*)malloc(sizeof(double) * (size_t)rank);
+    if (!hh) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+      err = ORACLE_ERR_NOMEM;
+      continue;
+    }
+    double mg = INFINITY;
+    int32_t* ci = cand_ids + (int64_t)b * P1 * K;
+    double* cl = cand_logit + (int64_t)b * P1 * K;
+    double* tr = trans + (int64_t)b * P1 * K * K;
+    for (int t = 1; t <= P1; ++t) {
+      /* candidates of position t */
+      int32_t ids[16];
+      float vals[16];
+      top_k(cand_logits + ((int64_t)b * P1 + t - 1) * vocab, vocab, K, ids, vals);
+      for (int i = 0; i < K; ++i) {
+        ci[(t - 1) * K + i] = ids[i];
+        cl[(t - 1) * K + i] = (double)vals[i];
+      }
+      /* H_t = W_H h_t */
+      const uint16_t* h = hidden + ((int64_t)b * P1 + t - 1) * dim;
+      for (int r = 0; r < rank; ++r) {
+        double acc = 0.0;
+        for (int d = 0; d < dim; ++d)
+          acc += oracle_bf16_to_double(w_h[(int64_t)r * dim + d]) *
+                 oracle_bf16_to_double(h[d]);
+        hh[r] = acc;
+      }
+      /* S_t(a, c) for every predecessor rank a and successor rank c */
+      const int n_pred = t == 1 ? 1 : K;
+      for (int a = 0; a < K; ++a) {
+        for (int c = 0; c < K; ++c) {
+          double s = -INFINITY;
+          if (a < n_pred) {
+            const int32_t ta = t == 1 ? boundary[b] : ci[(t - 2) * K + a];
+            const int32_t tc = ci[(t - 1) * K + c];
+            s = cl[(t - 1) * K + c];
+            for (int r = 0; r < rank; ++r)
+              s += oracle_bf16_to_double(code_a[(int64_t)ta * rank + r]) * hh[r] *
+                   oracle_bf16_to_double(code_b[(int64_t)tc * rank + r]);
+          }
+          tr[((int64_t)(t - 1) * K + a) * K + c] = s;
+        }
+      }
+    }
+    /* the walk */
+    int32_t* out = draft_ids + (int64_t)b * positions;
+    out[0] = boundary[b];
+    if (mode == ORACLE_SELECT_GREEDY) {
+      int prev = 0; /* rank of the chosen predecessor (the boundary at t=1) */
+      for (int t = 1; t <= P1; ++t) {
+        const double* row = tr + ((int64_t)(t - 1) * K + prev) * K;
+        int best = 0;
+        double second = -INFINITY;
+        for (int c = 1; c < K; ++c) {
+          if (row[c] > row[best]) {
+            if (row[best] > second) second = row[best];
+            best = c;
+          } else if (row[c] > second) {
+            second = row[c];
+          }
+        }
+        if (row[best] - second < mg) mg = row[best] - second;
+        out[t] = ci[(t - 1) * K + best];
+        prev = best;
+      }
+    } else {
+      /* exact MAP: best[t][c] = max_a best[t-1][a] + S_t(a, c) */
+      double best[16][16];
+      int back[16][16];
+      for (int c = 0; c < K; ++c) {
+        best[1][c] = tr[(int64_t)0 * K * K + 0 * K + c];
+        back[1][c] = 0;
+      }
+      for (int t = 2; t <= P1; ++t) {
+        for (int c = 0; c < K; ++c) {
+          int arg = 0;
+          double v = best[t - 1][0] + tr[((int64_t)(t - 1) * K + 0) * K + c];
+          double second = -INFINITY;
+          for (int a = 1; a < K; ++a) {
+            const double w = best[t - 1][a] + tr[((int64_t)(t - 1) * K + a) * K + c];
+            if (w > v) {
+              if (v > second) second = v;
+              v = w;
+              arg = a;
+            } else if (w > second) {
+              second = w;
+            }
+          }
+          best[t][c] = v;
+          back[t][c] = arg;
+          if (v - second < mg) mg = v - second;
+        }
+      }
+      int c = 0;
+      double second = -INFINITY;
+      for (int i = 1; i < K; ++i) {
+        if (best[P1][i] > best[P1][c]) {
+          if (best[P1][c] > second) second = best[P1][c];
+          c = i;
+        } else if (best[P1][i] > second) {
+          second = best[P1][i];
+        }
+      }
+      if (best[P1][c] - second < mg) mg = best[P1][c] - second;
+      for (int t = P1; t >= 1; --t) {
+        out[t] = ci[(t - 1) * K + c];
+        c = back[t][c];
+      }
+    }
+    if (margin) margin[b] = mg;
+    free(hh);
   }
   return err;
 }
