@@ -300,6 +300,75 @@ int spec_stochastic_accept(const float* logits, const int32_t* draft_ids,
                            void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/* Walks of the DFlash2 candidate selector (spec_select_desc.mode). */
+#define SPEC_SELECT_GREEDY 0  /* best successor of the token already chosen */
+#define SPEC_SELECT_MAP 1     /* the chain with the best total score */
+
+/*
+ * Shape of a DFlash2 candidate selection.
+ *   batch      requests B
+ *   positions  P: draft block rows, position 0 the verified boundary token,
+ *              positions 1 .. P-1 drafted (2..16; 8 for the pages' model)
+ *   vocab      V <= 262,144
+ *   top        K candidates per position (1..16; 16 for the pages' model)
+ *   rank       R of the codebooks, a multiple of 8 up to 256 (256 on the
+ *              pages)
+ *   dim        D of the draft hidden state, a multiple of 16
+ *   mode       SPEC_SELECT_GREEDY or SPEC_SELECT_MAP
+ */
+typedef struct {
+  int32_t batch, positions, vocab, top, rank, dim, mode;
+} spec_select_desc;
+
+/* Workspace bytes for spec_dflash2_select (0 on a bad desc). */
+size_t spec_select_workspace_size(const spec_select_desc* desc);
+
+/*
+ * DFlash2 candidate selection: choose one draft chain from the top-K
+ * candidates of every draft position through learned transition scores
+ * ("MTP and DFlash2 at long context on XPU", "The part that makes DFlash2
+ * different": top 16 per position, S_t(a, b) = U_t(b) + dot(A(a) * H(h_t),
+ * B(b)) at rank 256, a short causal walk choosing the best successor of the
+ * candidate already chosen; "Selector and recurrent math": 16 x 16 tables
+ * for adjacent positions; "Qwen3.8-27B-FP8" page: an exact MAP over the
+ * chain as an option).
+ *
+ * Position t = 1 .. P-1 keeps the K best entries of cand_logits[b, t-1]
+ * (larger first, lower token id on ties).  With U_t(c) that candidate's
+ * logit, H_t = W_H h_t (h_t = hidden[b, t-1]) and A, B the predecessor and
+ * successor codebooks indexed by token id,
+ *     S_t(a, c) = U_t(c) + sum_r A[tok(a), r] H_t[r] B[tok(c), r],
+ * where a ranges over the candidates of t-1, or is the boundary token at
+ * t = 1.  Greedy: c_0 = boundary, c_t = argmax_c S_t(c_{t-1}, c).  MAP: the
+ * chain maximising sum_t S_t(c_{t-1}, c_t).  Ties go to the lower
+ * candidate rank.  Arithmetic is float32 (bf16 inputs); a decision whose
+ * best and runner-up scores lie within float32 rounding of each other may
+ * come out differently from an exact evaluation.
+ *
+ *   cand_logits  fp32 [B, P-1, V], finite or -inf (the target head's
+ *                candidate logits for each drafted position)
+ *   boundary     int32 [B] token ids
+ *   hidden       bf16 [B, P-1, D]; w_h bf16 [R, D] (4-byte aligned)
+ *   code_a, code_b  bf16 [V, R]
+ *   draft_ids    int32 [B, P] out: [boundary, c_1, .., c_{P-1}], the
+ *                draft_ids layout of spec_greedy_accept
+ *   cand_ids     optional int32 [B, P-1, K] out: candidate token ids in
+ *                rank order (-1 past the finite entries)
+ *   cand_logit   optional fp32 [B, P-1, K] out: their logits
+ *   trans        optional fp32 [B, P-1, K, K] out: trans[b, t-1, a, c] =
+ *                S_t(a, c); at t = 1 only a = 0 (the boundary) is defined,
+ *                rows a >= 1 are -inf
+ *   workspace    >= spec_select_workspace_size(desc) bytes, 256-byte
+ *                aligned; contents need no initialisation
+ * Four launches on `stream`; nothing is copied to the host.
+ */
+int spec_dflash2_select(const spec_select_desc* desc, const float* cand_logits,
+                        const int32_t* boundary, const void* hidden,
+                        const void* w_h, const void* code_a, const void* code_b,
+                        int32_t* draft_ids, int32_t* cand_ids,
+                        float* cand_logit, float* trans, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 /* Verify width policies (spec_width_policy.policy). */
 #define SPEC_WIDTH_FIXED 0     /* always q_max rows */
 #define SPEC_WIDTH_EWMA 1      /* EWMA of the accepted count + offset */

@@ -6,7 +6,7 @@ this package does not load the library; the first call does, and raises if
 it is missing.
 """
 from ._native import (SpecError, accept_workspace_size, alloc_workspace,
-                      desc_for, greedy_accept, greedy_accept_commit,
+                      desc_for, dflash2_select, dflash2_select_into, greedy_accept, greedy_accept_commit,
                       greedy_accept_commit_into, greedy_accept_into,
                       kv_append, load, make_desc, prepare_next_block,
                       prepare_next_block_into, stochastic_accept,
@@ -17,6 +17,7 @@ from ._native import (SpecError, accept_workspace_size, alloc_workspace,
 
 __all__ = [
     "SpecError", "accept_workspace_size", "alloc_workspace", "desc_for",
+    "dflash2_select", "dflash2_select_into",
     "greedy_accept", "greedy_accept_commit", "greedy_accept_commit_into",
     "greedy_accept_into", "kv_append", "load", "make_desc",
     "prepare_next_block", "prepare_next_block_into", "stochastic_accept",

@@ -36,7 +36,9 @@ EXPORTED = (
     "spec_last_error", "spec_version", "spec_verify_attention_noalloc",
     "spec_kv_append", "spec_greedy_accept_commit", "spec_prepare_next_block",
     "spec_stochastic_workspace_size", "spec_stochastic_accept",
+    "spec_select_workspace_size", "spec_dflash2_select",
 )
+SELECT_MODES = {"greedy": 0, "map": 1}
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
@@ -54,6 +56,13 @@ class AttnDesc(ctypes.Structure):
                 ("max_pages_per_seq", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32),
                 ("q_lens", ctypes.c_void_p)]
+
+
+class SelectDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("positions", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("top", ctypes.c_int32),
+                ("rank", ctypes.c_int32), ("dim", ctypes.c_int32),
+                ("mode", ctypes.c_int32)]
 
 
 class WidthPolicy(ctypes.Structure):
@@ -107,6 +116,11 @@ def load(path: str = LIB_PATH):
     lib.spec_stochastic_accept.argtypes = [P, P, P, P, i32, i32, i32, P, P, P,
                                            P, P, P, P, P, P, sz, P]
     lib.spec_stochastic_accept.restype = ctypes.c_int
+    lib.spec_select_workspace_size.argtypes = [ctypes.POINTER(SelectDesc)]
+    lib.spec_select_workspace_size.restype = sz
+    lib.spec_dflash2_select.argtypes = [ctypes.POINTER(SelectDesc), P, P, P,
+                                        P, P, P, P, P, P, P, P, sz, P]
+    lib.spec_dflash2_select.restype = ctypes.c_int
     lib.spec_last_error.argtypes = []
     lib.spec_last_error.restype = ctypes.c_char_p
     lib.spec_version.argtypes = []
@@ -363,6 +377,53 @@ def stochastic_accept(logits, draft_ids, temperature, u_accept, u_sample, *,
                            temperature, u_accept, u_sample, seq_lens, new,
                            acc, nxt, toks, workspace, stream)
     return acc, nxt, toks, new
+
+
+def select_desc(cand_logits, code_a, hidden, *, top: int = 16,
+                mode: str = "greedy") -> SelectDesc:
+    B, P1, V = cand_logits.shape
+    return SelectDesc(B, P1 + 1, V, top, code_a.shape[1], hidden.shape[2],
+                      SELECT_MODES[mode])
+
+
+def select_workspace_size(desc: SelectDesc) -> int:
+    n = load().spec_select_workspace_size(ctypes.byref(desc))
+    if n == 0:
+        raise SpecError(SPEC_ERR_ARG, load().spec_last_error().decode())
+    return int(n)
+
+
+def dflash2_select_into(desc: SelectDesc, cand_logits, boundary, hidden, w_h,
+                        code_a, code_b, draft_ids, cand_ids, cand_logit,
+                        trans, workspace: torch.Tensor, stream=None) -> None:
+    _check(load().spec_dflash2_select(
+        ctypes.byref(desc), _ptr(cand_logits), _ptr(boundary), _ptr(hidden),
+        _ptr(w_h), _ptr(code_a), _ptr(code_b), _ptr(draft_ids),
+        _ptr(cand_ids), _ptr(cand_logit), _ptr(trans), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+
+
+def dflash2_select(cand_logits, boundary, hidden, w_h, code_a, code_b, *,
+                   top: int = 16, mode: str = "greedy",
+                   workspace: Optional[torch.Tensor] = None, stream=None):
+    """DFlash2 candidate selection on device tensors.  Returns dict of
+    draft_ids [B, P], cand_ids [B, P-1, K], cand_logit [B, P-1, K] and
+    trans [B, P-1, K, K]."""
+    desc = select_desc(cand_logits, code_a, hidden, top=top, mode=mode)
+    B, P1 = cand_logits.shape[:2]
+    dev = cand_logits.device
+    out = {"draft_ids": torch.empty((B, P1 + 1), dtype=torch.int32,
+                                    device=dev),
+           "cand_ids": torch.empty((B, P1, top), dtype=torch.int32,
+                                   device=dev),
+           "cand_logit": torch.empty((B, P1, top), device=dev),
+           "trans": torch.empty((B, P1, top, top), device=dev)}
+    if workspace is None:
+        workspace = alloc_workspace(select_workspace_size(desc), dev)
+    dflash2_select_into(desc, cand_logits, boundary, hidden, w_h, code_a,
+                        code_b, out["draft_ids"], out["cand_ids"],
+                        out["cand_logit"], out["trans"], workspace, stream)
+    return out
 
 
 def greedy_accept(logits: torch.Tensor, draft_ids: torch.Tensor, *,

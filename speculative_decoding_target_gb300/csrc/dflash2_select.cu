@@ -1,0 +1,389 @@
+// DFlash2 candidate selection ("MTP and DFlash2 at long context on XPU",
+// "The part that makes DFlash2 different" and "Selector and recurrent math";
+// "Qwen3.8-27B-FP8" page: selector_rank 256, selector_top_k 16, an exact
+// MAP over the chain as an option).
+//
+// Draft position t = 1 .. P-1 keeps its K best candidate logits (larger
+// first, lower token id on ties).  A transition from candidate a at t-1 (the
+// boundary token at t = 1) to candidate b at t scores
+//     S_t(a, b) = U_t(b) + sum_r A[a, r] H_t[r] B[b, r],   H_t = W_H h_t,
+// and a walk from the boundary picks one chain: greedy (the best successor
+// of the token already chosen) or MAP (the best total score).  Ties go to
+// the lower candidate rank.
+//
+// Four launches:
+//   1. topk_partial_kernel, CTA per (8192-token chunk, position row): the
+//      chunk's K best in one streaming pass (K rounds of warp argmax over
+//      register-held logits, then a block merge);
+//   2. project_kernel: H = W_H h for every position row, bf16 mma.sync
+//      tiles with fp32 accumulation (a small contraction: the weights are
+//      read once);
+//   3. table_kernel, CTA per (position, request): the candidate lists of t
+//      and t-1 from the chunk lists, the 2 x K codebook rows, and the K x K
+//      table in fp32;
+//   4. walk_kernel, one warp per request: the greedy or MAP walk.
+#include <climits>
+
+#include "selector.cuh"
+
+namespace specv {
+namespace {
+
+// Larger value first, then lower token id: a total order on distinct ids.
+__device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
+  return a > b || (a == b && ia < ib);
+}
+
+__device__ __forceinline__ void warp_best(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+// ---- 1. chunk top-K -------------------------------------------------------
+
+__global__ void __launch_bounds__(kSelThreads)
+    topk_partial_kernel(const SelectParams p) {
+  constexpr int kPer = kSelChunk / kSelThreads;  // 32 logits per thread
+  constexpr int kWarps = kSelThreads / 32;
+  __shared__ float s_v[kWarps * 16];
+  __shared__ int s_i[kWarps * 16];
+  const int chunk = blockIdx.x, row = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* x = p.cand_logits + (long long)row * p.vocab;
+  const int begin = chunk * kSelChunk;
+  const int end = min(begin + kSelChunk, p.vocab);
+  float v[kPer];
+  int base[kPer / 4];  // token id of the first of each group of 4
+  if (p.vec4) {
+    const float4* x4 = reinterpret_cast<const float4*>(x + begin);
+    const int n4 = (end - begin) >> 2;
+#pragma unroll
+    for (int e = 0; e < kPer / 4; ++e) {
+      const int j = threadIdx.x + e * kSelThreads;
+      const float4 t = j < n4 ? __ldcs(x4 + j)
+                              : make_float4(-INFINITY, -INFINITY, -INFINITY,
+                                            -INFINITY);
+      v[4 * e] = t.x; v[4 * e + 1] = t.y; v[4 * e + 2] = t.z; v[4 * e + 3] = t.w;
+      base[e] = j < n4 ? begin + 4 * j : INT_MAX;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < kPer / 4; ++e) {
+      const int i0 = begin + 4 * (threadIdx.x + e * kSelThreads);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        v[4 * e + q] = i0 + q < end ? __ldcs(x + i0 + q) : -INFINITY;
+      base[e] = i0 < end ? i0 : INT_MAX;
+    }
+  }
+  auto id_of = [&](int e) {
+    const int b0 = base[e >> 2];
+    return b0 == INT_MAX || b0 + (e & 3) >= end ? INT_MAX : b0 + (e & 3);
+  };
+  // this thread's best not-yet-taken entry
+  uint32_t taken = 0;
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  auto refresh = [&]() {
+    bv = -INFINITY;
+    bi = INT_MAX;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int id = id_of(e);
+      if (!(taken >> e & 1u) && id != INT_MAX && better(v[e], id, bv, bi)) {
+        bv = v[e];
+        bi = id;
+      }
+    }
+  };
+  refresh();
+  for (int k = 0; k < p.top; ++k) {
+    float wv = bv;
+    int wi = bi;
+    warp_best(wv, wi);
+    if (lane == 0) {
+      s_v[warp * 16 + k] = wv;
+      s_i[warp * 16 + k] = wi;
+    }
+    if (wi != INT_MAX && wi == bi) {  // this thread held the winner
+#pragma unroll
+      for (int e = 0; e < kPer; ++e)
+        if (id_of(e) == wi) taken |= 1u << e;
+      refresh();
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {  // merge the warps' lists: lane l holds entries l, l+32..
+    constexpr int kHeld = kWarps * 16 / 32;
+    float hv[kHeld];
+    int hi[kHeld];
+#pragma unroll
+    for (int j = 0; j < kHeld; ++j) {
+      const int n = lane + 32 * j, w = n / 16, k = n % 16;
+      const bool ok = k < p.top;
+      hv[j] = ok ? s_v[w * 16 + k] : -INFINITY;
+      hi[j] = ok ? s_i[w * 16 + k] : INT_MAX;
+    }
+    float* ov = p.part_val + ((long long)row * p.chunks + chunk) * p.top;
+    int32_t* oi = p.part_idx + ((long long)row * p.chunks + chunk) * p.top;
+    for (int k = 0; k < p.top; ++k) {
+      float mv = -INFINITY;
+      int mi = INT_MAX;
+#pragma unroll
+      for (int j = 0; j < kHeld; ++j)
+        if (better(hv[j], hi[j], mv, mi)) {
+          mv = hv[j];
+          mi = hi[j];
+        }
+      float wv = mv;
+      int wi = mi;
+      warp_best(wv, wi);
+      if (lane == 0) {
+        ov[k] = wv;
+        oi[k] = wi;
+      }
+#pragma unroll
+      for (int j = 0; j < kHeld; ++j)
+        if (hi[j] == wi && wi != INT_MAX) {
+          hv[j] = -INFINITY;
+          hi[j] = INT_MAX;
+        }
+    }
+  }
+}
+
+// ---- 2. projection H = W_H h ---------------------------------------------------
+
+__device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+constexpr int kProjMTiles = 4;  // 64 rows of h per CTA
+
+// CTA (n tile of 8 projection rows, m block of 64 position rows); warp w
+// takes the k16 steps w, w + 8, ...; the 8 warps' partial tiles are summed
+// in a fixed order.
+__global__ void __launch_bounds__(256) project_kernel(const SelectParams p) {
+  __shared__ float s_acc[8][kProjMTiles * 16][8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int n0 = blockIdx.x * 8, m0 = blockIdx.y * kProjMTiles * 16;
+  const int rows = p.batch * (p.positions - 1);
+  const uint32_t* W = reinterpret_cast<const uint32_t*>(p.w_h);
+  const uint32_t* X = reinterpret_cast<const uint32_t*>(p.hidden);
+  const int d2 = p.dim >> 1;  // bf16 pairs per row
+  float acc[kProjMTiles][4];
+#pragma unroll
+  for (int m = 0; m < kProjMTiles; ++m)
+    acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+  const int ksteps = p.dim >> 4;
+  const int n = n0 + g;
+  for (int ks = warp; ks < ksteps; ks += 8) {
+    const int kp = ks * 8 + t4;  // pair index of columns 16 ks + 2 t4
+    uint32_t b0 = 0, b1 = 0;
+    if (n < p.rank) {
+      b0 = W[(long long)n * d2 + kp];
+      b1 = W[(long long)n * d2 + kp + 4];
+    }
+#pragma unroll
+    for (int m = 0; m < kProjMTiles; ++m) {
+      const int r0 = m0 + m * 16 + g, r1 = r0 + 8;
+      uint32_t a[4] = {0u, 0u, 0u, 0u};
+      if (r0 < rows) {
+        a[0] = X[(long long)r0 * d2 + kp];
+        a[2] = X[(long long)r0 * d2 + kp + 4];
+      }
+      if (r1 < rows) {
+        a[1] = X[(long long)r1 * d2 + kp];
+        a[3] = X[(long long)r1 * d2 + kp + 4];
+      }
+      mma_bf16_16816(acc[m], a, b0, b1);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kProjMTiles; ++m) {
+    s_acc[warp][m * 16 + g][2 * t4] = acc[m][0];
+    s_acc[warp][m * 16 + g][2 * t4 + 1] = acc[m][1];
+    s_acc[warp][m * 16 + g + 8][2 * t4] = acc[m][2];
+    s_acc[warp][m * 16 + g + 8][2 * t4 + 1] = acc[m][3];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < kProjMTiles * 16 * 8; e += 256) {
+    const int r = e >> 3, c = e & 7;
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += s_acc[w][r][c];
+    if (m0 + r < rows && n0 + c < p.rank)
+      p.proj[(long long)(m0 + r) * p.rank + n0 + c] = s;
+  }
+}
+
+// ---- 3. transition tables ---------------------------------------------------
+
+// The K best of a position row from its chunk lists, by one warp (every lane
+// gets the same lists); ids[k], vals[k] in smem.  Lane c holds chunk c's
+// sorted list as a register queue (one round of loads); each round the
+// lanes offer their heads and the winner shifts its queue.
+__device__ void merge_candidates(const SelectParams& p, int row, int* ids,
+                                 float* vals) {
+  const int lane = threadIdx.x & 31;
+  float qv[16];
+  int qi[16];
+  const float* pv = p.part_val + ((long long)row * p.chunks + lane) * p.top;
+  const int32_t* pi = p.part_idx + ((long long)row * p.chunks + lane) * p.top;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const bool ok = lane < p.chunks && k < p.top;
+    qv[k] = ok ? pv[k] : -INFINITY;
+    qi[k] = ok ? pi[k] : INT_MAX;
+  }
+  for (int k = 0; k < p.top; ++k) {
+    float wv = qv[0];
+    int wi = qi[0];
+    warp_best(wv, wi);
+    if (lane == 0) {
+      ids[k] = wi == INT_MAX ? -1 : wi;
+      vals[k] = wv;
+    }
+    if (wi != INT_MAX && wi == qi[0]) {
+#pragma unroll
+      for (int e = 0; e < 15; ++e) {
+        qv[e] = qv[e + 1];
+        qi[e] = qi[e + 1];
+      }
+      qv[15] = -INFINITY;
+      qi[15] = INT_MAX;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) table_kernel(const SelectParams p) {
+  __shared__ int s_ids[2][16];
+  __shared__ float s_vals[2][16];
+  __shared__ float s_ah[kSelMaxRank][17];  // A[a, r] H_t[r], column a
+  __shared__ float s_b[kSelMaxRank][17];   // B[c, r], column c
+  const int t = blockIdx.x + 1, b = blockIdx.y;  // position t = 1 .. P-1
+  const int warp = threadIdx.x >> 5;
+  const int P1 = p.positions - 1, K = p.top, R = p.rank;
+  const int row = b * P1 + t - 1;
+  if (warp == 0) merge_candidates(p, row, s_ids[1], s_vals[1]);
+  if (warp == 1 && t > 1) merge_candidates(p, row - 1, s_ids[0], s_vals[0]);
+  if (threadIdx.x == 64 && t == 1) s_ids[0][0] = p.boundary[b];
+  __syncthreads();
+  const int n_pred = t == 1 ? 1 : K;
+  // gather the codebook rows: predecessors scaled by H_t, successors
+  const float* h = p.proj + (long long)row * R;
+  for (int e = threadIdx.x; e < 16 * R; e += 256) {
+    const int a = e / R, r = e - a * R;
+    float va = 0.f, vb = 0.f;
+    if (a < n_pred && s_ids[0][a] >= 0)
+      va = __fmul_rn(__bfloat162float(p.code_a[(long long)s_ids[0][a] * R + r]),
+                     h[r]);
+    if (a < K && s_ids[1][a] >= 0)
+      vb = __bfloat162float(p.code_b[(long long)s_ids[1][a] * R + r]);
+    s_ah[r][a] = va;
+    s_b[r][a] = vb;
+  }
+  __syncthreads();
+  const int a = threadIdx.x >> 4, c = threadIdx.x & 15;
+  if (a < K && c < K) {
+    float s = -INFINITY;
+    if (a < n_pred) {
+      float acc = 0.f;
+      for (int r = 0; r < R; ++r) acc = fmaf(s_ah[r][a], s_b[r][c], acc);
+      s = s_vals[1][c] + acc;
+    }
+    p.trans[(((long long)b * P1 + t - 1) * K + a) * K + c] = s;
+    if (a == 0) {
+      p.cand_ids[((long long)b * P1 + t - 1) * K + c] = s_ids[1][c];
+      p.cand_logit[((long long)b * P1 + t - 1) * K + c] = s_vals[1][c];
+    }
+  }
+}
+
+// ---- 4. the walk ------------------------------------------------------------
+
+__global__ void __launch_bounds__(128) walk_kernel(const SelectParams p) {
+  __shared__ int s_back[4][16][16];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x * 4 + warp;
+  if (b >= p.batch) return;
+  const int P1 = p.positions - 1, K = p.top;
+  const float* tr = p.trans + (long long)b * P1 * K * K;
+  const int32_t* ci = p.cand_ids + (long long)b * P1 * K;
+  int32_t* out = p.draft_ids + (long long)b * p.positions;
+  if (lane == 0) out[0] = p.boundary[b];
+  if (p.mode == 0) {  // greedy
+    int prev = 0;
+    for (int t = 1; t <= P1; ++t) {
+      float v = lane < K ? tr[((long long)(t - 1) * K + prev) * K + lane]
+                         : -INFINITY;
+      int i = lane < K ? lane : INT_MAX;
+      warp_best(v, i);
+      prev = i;
+      if (lane == 0) out[t] = ci[(t - 1) * K + prev];
+    }
+    return;
+  }
+  // MAP: best_t(c) = max_a best_{t-1}(a) + S_t(a, c), lowest a on ties
+  float best = lane < K ? tr[lane] : -INFINITY;  // t = 1 from the boundary
+  for (int t = 2; t <= P1; ++t) {
+    float nb = -INFINITY;
+    int arg = 0;
+    for (int a2 = 0; a2 < K; ++a2) {
+      const float ba = __shfl_sync(0xffffffffu, best, a2);
+      const float w = lane < K
+          ? __fadd_rn(ba, tr[((long long)(t - 1) * K + a2) * K + lane])
+          : -INFINITY;
+      if (a2 == 0 || w > nb) {
+        nb = w;
+        arg = a2;
+      }
+    }
+    if (lane < K) s_back[warp][t - 1][lane] = arg;
+    best = nb;
+  }
+  float v = best;
+  int c = lane < K ? lane : INT_MAX;
+  warp_best(v, c);
+  __syncwarp();
+  if (lane == 0) {
+    for (int t = P1; t >= 1; --t) {
+      out[t] = ci[(t - 1) * K + c];
+      if (t > 1) c = s_back[warp][t - 1][c];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dflash2_select(const SelectParams& p, cudaStream_t s) {
+  const int rows = p.batch * (p.positions - 1);
+  topk_partial_kernel<<<dim3(p.chunks, rows), kSelThreads, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  project_kernel<<<dim3((p.rank + 7) / 8, (rows + kProjMTiles * 16 - 1) /
+                                              (kProjMTiles * 16)),
+                   256, 0, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  table_kernel<<<dim3(p.positions - 1, p.batch), 256, 0, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  walk_kernel<<<(p.batch + 3) / 4, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace specv

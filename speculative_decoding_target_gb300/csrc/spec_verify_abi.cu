@@ -10,6 +10,7 @@
 
 #include "append.cuh"
 #include "next_block.cuh"
+#include "selector.cuh"
 #include "stochastic.cuh"
 #include "common.cuh"
 #include "spec_verify.h"
@@ -536,6 +537,119 @@ int spec_stochastic_accept(const float* logits, const int32_t* draft_ids,
   if (e != cudaSuccess)
     return fail(SPEC_ERR_CUDA, "stochastic accept launch: %s",
                 cudaGetErrorString(e));
+  return SPEC_OK;
+}
+
+namespace {
+int check_select(const spec_select_desc* d) {
+  if (!d) return fail(SPEC_ERR_ARG, "desc is NULL");
+  if (d->batch < 0 || d->positions < 2 || d->positions > 16)
+    return fail(SPEC_ERR_ARG, "batch %d / positions %d (2..16)", d->batch,
+                d->positions);
+  if (d->top < 1 || d->top > 16)
+    return fail(SPEC_ERR_ARG, "top %d outside [1, 16]", d->top);
+  if (d->vocab < d->top || d->vocab > specv::kSelMaxChunks * specv::kSelChunk)
+    return fail(SPEC_ERR_ARG, "vocab %d outside [top, %d]", d->vocab,
+                specv::kSelMaxChunks * specv::kSelChunk);
+  if (d->rank < 8 || d->rank > specv::kSelMaxRank || d->rank % 8)
+    return fail(SPEC_ERR_ARG, "rank %d: a multiple of 8 in [8, %d]", d->rank,
+                specv::kSelMaxRank);
+  if (d->dim < 16 || d->dim % 16)
+    return fail(SPEC_ERR_ARG, "dim %d: a multiple of 16", d->dim);
+  if (d->mode != SPEC_SELECT_GREEDY && d->mode != SPEC_SELECT_MAP)
+    return fail(SPEC_ERR_ARG, "mode %d", d->mode);
+  if ((long long)d->batch * (d->positions - 1) > 65535)
+    return fail(SPEC_ERR_ARG, "batch * (positions - 1) exceeds 65535");
+  return SPEC_OK;
+}
+
+struct SelectLayout {
+  size_t part_val, part_idx, proj, trans, cand_ids, cand_logit, bytes;
+};
+
+SelectLayout select_layout(const spec_select_desc* d) {
+  const size_t rows = (size_t)d->batch * (d->positions - 1);
+  const size_t chunks = (d->vocab + specv::kSelChunk - 1) / specv::kSelChunk;
+  SelectLayout L;
+  size_t o = 0;
+  auto take = [&](size_t n) {
+    const size_t at = o;
+    o += round_up(n, 256);
+    return at;
+  };
+  L.part_val = take(rows * chunks * d->top * sizeof(float));
+  L.part_idx = take(rows * chunks * d->top * sizeof(int32_t));
+  L.proj = take(rows * d->rank * sizeof(float));
+  L.trans = take(rows * d->top * d->top * sizeof(float));
+  L.cand_ids = take(rows * d->top * sizeof(int32_t));
+  L.cand_logit = take(rows * d->top * sizeof(float));
+  L.bytes = o;
+  return L;
+}
+}  // namespace
+
+size_t spec_select_workspace_size(const spec_select_desc* desc) {
+  if (check_select(desc)) return 0;
+  return select_layout(desc).bytes;
+}
+
+int spec_dflash2_select(const spec_select_desc* desc, const float* cand_logits,
+                        const int32_t* boundary, const void* hidden,
+                        const void* w_h, const void* code_a, const void* code_b,
+                        int32_t* draft_ids, int32_t* cand_ids,
+                        float* cand_logit, float* trans, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  int rc = check_select(desc);
+  if (rc) return rc;
+  if (desc->batch == 0) return SPEC_OK;
+  if (!cand_logits || !boundary || !hidden || !w_h || !code_a || !code_b ||
+      !draft_ids)
+    return fail(SPEC_ERR_ARG, "NULL tensor pointer");
+  const void* a4[] = {cand_logits, boundary, hidden, w_h, draft_ids,
+                      cand_ids, cand_logit, trans};
+  for (const void* q : a4)
+    if (q && !aligned(q, 4))
+      return fail(SPEC_ERR_ALIGN, "tensors must be 4-byte aligned");
+  if (!aligned(code_a, 2) || !aligned(code_b, 2))
+    return fail(SPEC_ERR_ALIGN, "codebooks must be 2-byte aligned");
+  if (!workspace) return fail(SPEC_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 256))
+    return fail(SPEC_ERR_ALIGN, "workspace must be 256-byte aligned");
+  const SelectLayout L = select_layout(desc);
+  if (workspace_bytes < L.bytes)
+    return fail(SPEC_ERR_WORKSPACE, "workspace %zu bytes < %zu needed",
+                workspace_bytes, L.bytes);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  specv::SelectParams p;
+  std::memset(&p, 0, sizeof p);
+  p.cand_logits = cand_logits;
+  p.boundary = boundary;
+  p.hidden = static_cast<const __nv_bfloat16*>(hidden);
+  p.w_h = static_cast<const __nv_bfloat16*>(w_h);
+  p.code_a = static_cast<const __nv_bfloat16*>(code_a);
+  p.code_b = static_cast<const __nv_bfloat16*>(code_b);
+  p.cand_ids = cand_ids ? cand_ids : reinterpret_cast<int32_t*>(ws + L.cand_ids);
+  p.cand_logit = cand_logit ? cand_logit
+                            : reinterpret_cast<float*>(ws + L.cand_logit);
+  p.trans = trans ? trans : reinterpret_cast<float*>(ws + L.trans);
+  p.draft_ids = draft_ids;
+  p.part_val = reinterpret_cast<float*>(ws + L.part_val);
+  p.part_idx = reinterpret_cast<int32_t*>(ws + L.part_idx);
+  p.proj = reinterpret_cast<float*>(ws + L.proj);
+  p.batch = desc->batch;
+  p.positions = desc->positions;
+  p.vocab = desc->vocab;
+  p.top = desc->top;
+  p.rank = desc->rank;
+  p.dim = desc->dim;
+  p.mode = desc->mode;
+  p.chunks = (desc->vocab + specv::kSelChunk - 1) / specv::kSelChunk;
+  p.vec4 = (desc->vocab % 4 == 0) && aligned(cand_logits, 16);
+  cudaError_t e =
+      specv::launch_dflash2_select(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(SPEC_ERR_CUDA, "selector launch: %s", cudaGetErrorString(e));
   return SPEC_OK;
 }
 

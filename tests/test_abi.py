@@ -219,3 +219,30 @@ def test_stochastic_accept_argument_checks(lib):
     assert need > 0
     assert call(ws_bytes=need - 1) == _native.SPEC_ERR_WORKSPACE
     assert lib.spec_stochastic_workspace_size(2, 0, 1000) == 0
+
+
+def test_select_argument_checks(lib):
+    def d(**kw):
+        base = dict(batch=2, positions=8, vocab=248320, top=16, rank=256,
+                    dim=5120, mode=0)
+        base.update(kw)
+        return _native.SelectDesc(*base.values())
+
+    size = lib.spec_select_workspace_size
+    assert size(ctypes.byref(d())) > 0
+    for bad in (dict(positions=1), dict(positions=17), dict(top=0),
+                dict(top=17), dict(vocab=262145), dict(vocab=8, top=16),
+                dict(rank=260), dict(rank=12), dict(dim=24), dict(mode=2),
+                dict(batch=-1)):
+        assert size(ctypes.byref(d(**bad))) == 0, bad
+    f = lib.spec_dflash2_select
+
+    def call(desc, logits=FAKE, ws=FAKE, ws_bytes=1 << 30, hidden=FAKE):
+        return f(ctypes.byref(desc), logits, FAKE, hidden, FAKE, FAKE, FAKE,
+                 FAKE, None, None, None, ws, ws_bytes, None)
+
+    assert call(d(batch=0), logits=None) == _native.SPEC_OK
+    assert call(d(), logits=None) == _native.SPEC_ERR_ARG
+    assert call(d(), hidden=ctypes.c_void_p(0x100002)) == _native.SPEC_ERR_ALIGN
+    assert call(d(), ws=None) == _native.SPEC_ERR_WORKSPACE
+    assert call(d(), ws_bytes=16) == _native.SPEC_ERR_WORKSPACE
