@@ -377,6 +377,9 @@ def run_gpu(args, w: wl.VerifyWorkload):
     if not args.no_stochastic:
         result["stochastic"] = measure_stochastic(w, inp, dev, args.steps,
                                                   args.warmup, peak)
+    if not args.no_select:
+        result["dflash2_select"] = measure_select(w, dev, args.steps,
+                                                  args.warmup, peak)
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         host_inp = {k: (v.cpu() if torch.is_tensor(v) else v)
                     for k, v in inp.items()}
@@ -595,6 +598,83 @@ def measure_stochastic(w: wl.VerifyWorkload, inp, dev, steps: int,
     return out
 
 
+# ------------------------------------------------------ DFlash2 selector --
+
+SELECT_RANK, SELECT_HIDDEN, SELECT_TOP = 256, 5120, 16
+
+
+def select_bytes(w: wl.VerifyWorkload) -> int:
+    """Algorithmic bytes of one selection: the candidate logits of the
+    drafted positions, the projection weights and hidden states, and the
+    2 x K codebook rows gathered per position (bf16)."""
+    rows = w.batch * (w.q_len - 1)
+    return (rows * w.vocab * 4 + SELECT_RANK * SELECT_HIDDEN * 2 +
+            rows * SELECT_HIDDEN * 2 + rows * 2 * SELECT_TOP * SELECT_RANK * 2)
+
+
+def measure_select(w: wl.VerifyWorkload, dev, steps: int, warmup: int,
+                   peak: float):
+    """The DFlash2 selector on the workload's draft block (B requests, q_len
+    positions, top 16 of the vocabulary, rank 256, hidden 5,120), random
+    weights; greedy and MAP walks, CUDA events per call."""
+    import speculative_decoding_target_gb300 as sv
+    B, P, V = w.batch, w.q_len, w.vocab
+    if P < 2:
+        return None
+    g = torch.Generator(device=dev).manual_seed(w.seed + 41)
+    R, D = SELECT_RANK, SELECT_HIDDEN
+    logits = torch.randn((B, P - 1, V), generator=g, device=dev) * 2
+    boundary = torch.randint(0, V, (B,), generator=g, device=dev,
+                             dtype=torch.int32)
+    hidden = torch.randn((B, P - 1, D), generator=g, device=dev).to(
+        torch.bfloat16)
+    w_h = (torch.randn((R, D), generator=g, device=dev) / D ** 0.5).to(
+        torch.bfloat16)
+    code_a = (torch.randn((V, R), generator=g, device=dev) * 0.3).to(
+        torch.bfloat16)
+    code_b = (torch.randn((V, R), generator=g, device=dev) * 0.3).to(
+        torch.bfloat16)
+    out = torch.empty((B, P), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for mode in ("greedy", "map"):
+        desc = sv._native.select_desc(logits, code_a, hidden,
+                                      top=SELECT_TOP, mode=mode)
+        ws = sv.alloc_workspace(sv._native.select_workspace_size(desc), dev)
+
+        def call():
+            sv.dflash2_select_into(desc, logits, boundary, hidden, w_h,
+                                   code_a, code_b, out, None, None, None, ws,
+                                   stream)
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        res[mode + "_ms"] = round(statistics.mean(a.elapsed_time(b)
+                                                  for a, b in evs), 5)
+    nbytes = select_bytes(w)
+    res.update({
+        "shape": f"{B} requests x {P} positions, top {SELECT_TOP} of {V}, "
+                 f"rank {R}, hidden {D}",
+        "algorithmic_bytes": nbytes,
+        "achieved_gbs_greedy": round(nbytes / (res["greedy_ms"] * 1e-3) / 1e9,
+                                     1),
+        "frac_of_peak_greedy": round(
+            nbytes / (res["greedy_ms"] * 1e-3) / 1e9 / peak, 4),
+        "gpu_launches": 4 * 2 * steps,
+        "note": "four launches per call: chunked top-K over the candidate "
+                "logits (the streaming pass), the rank projection, the "
+                "transition tables, the walk",
+    })
+    return res
+
+
 # ----------------------------------------------------------- CPU baseline --
 
 def _oracle_step_estimate(w, host_inp, n_rows: int, n_acc_rows: int, rng):
@@ -704,6 +784,8 @@ def main():
                     help="skip the per-request width (ragged) step timing")
     ap.add_argument("--no-stochastic", action="store_true",
                     help="skip the rejection-sampling accept timing")
+    ap.add_argument("--no-select", action="store_true",
+                    help="skip the DFlash2 candidate selector timing")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--ref-rows", type=int, default=48)
     args = ap.parse_args()

@@ -21,7 +21,7 @@
 //   3. table_kernel, CTA per (position, request): the candidate lists of t
 //      and t-1 from the chunk lists, the 2 x K codebook rows, and the K x K
 //      table in fp32;
-//   4. walk_kernel, one warp per request: the greedy or MAP walk.
+//   4. walk_kernel, one warp (CTA) per request: the greedy or MAP walk.
 #include <climits>
 
 #include "selector.cuh"
@@ -48,19 +48,44 @@ __device__ __forceinline__ void warp_best(float& v, int& i) {
 
 // ---- 1. chunk top-K -------------------------------------------------------
 
-__global__ void __launch_bounds__(kSelThreads)
+// Exact top-K of a chunk without serial rounds.  (i) A bound: lane l's rank
+// among its warp's 32 lane maxima is a count (32 independent shuffles);
+// the maximum of rank K-1, T_w, has K values of the warp at or above it, so
+// the chunk's K best all lie at or above T = max_w T_w.  (ii) The values
+// >= T (about 1% of a chunk of random logits) go to a shared pool, and each
+// pool entry's rank is the number of entries that beat it (value, then
+// lower token id): entries of rank < K are the chunk's top K, already in
+// order.  A pool that overflows (heavy ties, or fewer than K finite values)
+// falls back to K block-wide argmax rounds over the whole chunk.
+constexpr int kSelPool = 512;
+
+// Rank of (v, i) among the warp's 32 pairs (0 = best).
+__device__ __forceinline__ int warp_rank(float v, int i) {
+  int r = 0;
+#pragma unroll
+  for (int l = 0; l < 32; ++l) {
+    const float ov = __shfl_sync(0xffffffffu, v, l);
+    const int oi = __shfl_sync(0xffffffffu, i, l);
+    r += better(ov, oi, v, i);
+  }
+  return r;
+}
+
+__global__ void __launch_bounds__(kSelThreads, 3)
     topk_partial_kernel(const SelectParams p) {
   constexpr int kPer = kSelChunk / kSelThreads;  // 32 logits per thread
   constexpr int kWarps = kSelThreads / 32;
-  __shared__ float s_v[kWarps * 16];
-  __shared__ int s_i[kWarps * 16];
+  __shared__ float s_tw[kWarps];
+  __shared__ float s_pv[kSelPool];
+  __shared__ int s_pi[kSelPool];
+  __shared__ int s_n;
   const int chunk = blockIdx.x, row = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* x = p.cand_logits + (long long)row * p.vocab;
   const int begin = chunk * kSelChunk;
   const int end = min(begin + kSelChunk, p.vocab);
+  // thread t holds tokens begin + 4 (t + 256 e) + q, q < 4, e < 8
   float v[kPer];
-  int base[kPer / 4];  // token id of the first of each group of 4
   if (p.vec4) {
     const float4* x4 = reinterpret_cast<const float4*>(x + begin);
     const int n4 = (end - begin) >> 2;
@@ -71,7 +96,6 @@ __global__ void __launch_bounds__(kSelThreads)
                               : make_float4(-INFINITY, -INFINITY, -INFINITY,
                                             -INFINITY);
       v[4 * e] = t.x; v[4 * e + 1] = t.y; v[4 * e + 2] = t.z; v[4 * e + 3] = t.w;
-      base[e] = j < n4 ? begin + 4 * j : INT_MAX;
     }
   } else {
 #pragma unroll
@@ -80,20 +104,63 @@ __global__ void __launch_bounds__(kSelThreads)
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         v[4 * e + q] = i0 + q < end ? __ldcs(x + i0 + q) : -INFINITY;
-      base[e] = i0 < end ? i0 : INT_MAX;
     }
   }
   auto id_of = [&](int e) {
-    const int b0 = base[e >> 2];
-    return b0 == INT_MAX || b0 + (e & 3) >= end ? INT_MAX : b0 + (e & 3);
+    const int id = begin + 4 * (threadIdx.x + (e >> 2) * kSelThreads) + (e & 3);
+    return id < end ? id : INT_MAX;
   };
-  // this thread's best not-yet-taken entry
+  // (i) the bound
+  float m = v[0];
+#pragma unroll
+  for (int e = 1; e < kPer; ++e) m = fmaxf(m, v[e]);
+  const int rk = warp_rank(m, lane);
+  const unsigned at = __ballot_sync(0xffffffffu, rk == p.top - 1);
+  const float tw = __shfl_sync(0xffffffffu, m, __ffs(at) - 1);
+  if (lane == 0) s_tw[warp] = tw;
+  if (threadIdx.x == 0) s_n = 0;
+  __syncthreads();
+  float T = s_tw[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) T = fmaxf(T, s_tw[w]);
+  // (ii) the pool of values >= T
+  const bool finite_bound = T > -INFINITY;
+  if (finite_bound) {
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      if (v[e] >= T) {
+        const int slot = atomicAdd(&s_n, 1);
+        if (slot < kSelPool) {
+          s_pv[slot] = v[e];
+          s_pi[slot] = id_of(e);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int n = s_n;
+  float* ov = p.part_val + ((long long)row * p.chunks + chunk) * p.top;
+  int32_t* oi = p.part_idx + ((long long)row * p.chunks + chunk) * p.top;
+  if (finite_bound && n <= kSelPool) {
+    for (int e = threadIdx.x; e < n; e += kSelThreads) {
+      const float ve = s_pv[e];
+      const int ie = s_pi[e];
+      int r = 0;
+      for (int f = 0; f < n; ++f) r += better(s_pv[f], s_pi[f], ve, ie);
+      if (r < p.top) {
+        ov[r] = ve;
+        oi[r] = ie;
+      }
+    }
+    return;
+  }
+  // fallback: K block-wide argmax rounds over every value of the chunk
+  __shared__ float s_bv[kWarps];
+  __shared__ int s_bi[kWarps];
   uint32_t taken = 0;
-  float bv = -INFINITY;
-  int bi = INT_MAX;
-  auto refresh = [&]() {
-    bv = -INFINITY;
-    bi = INT_MAX;
+  for (int k = 0; k < p.top; ++k) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
       const int id = id_of(e);
@@ -102,60 +169,29 @@ __global__ void __launch_bounds__(kSelThreads)
         bi = id;
       }
     }
-  };
-  refresh();
-  for (int k = 0; k < p.top; ++k) {
-    float wv = bv;
-    int wi = bi;
-    warp_best(wv, wi);
+    warp_best(bv, bi);
     if (lane == 0) {
-      s_v[warp * 16 + k] = wv;
-      s_i[warp * 16 + k] = wi;
+      s_bv[warp] = bv;
+      s_bi[warp] = bi;
     }
-    if (wi != INT_MAX && wi == bi) {  // this thread held the winner
+    __syncthreads();
+    float wv = s_bv[0];
+    int wi = s_bi[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w)
+      if (better(s_bv[w], s_bi[w], wv, wi)) {
+        wv = s_bv[w];
+        wi = s_bi[w];
+      }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      ov[k] = wv;
+      oi[k] = wi;
+    }
+    if (wi != INT_MAX)
 #pragma unroll
       for (int e = 0; e < kPer; ++e)
         if (id_of(e) == wi) taken |= 1u << e;
-      refresh();
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {  // merge the warps' lists: lane l holds entries l, l+32..
-    constexpr int kHeld = kWarps * 16 / 32;
-    float hv[kHeld];
-    int hi[kHeld];
-#pragma unroll
-    for (int j = 0; j < kHeld; ++j) {
-      const int n = lane + 32 * j, w = n / 16, k = n % 16;
-      const bool ok = k < p.top;
-      hv[j] = ok ? s_v[w * 16 + k] : -INFINITY;
-      hi[j] = ok ? s_i[w * 16 + k] : INT_MAX;
-    }
-    float* ov = p.part_val + ((long long)row * p.chunks + chunk) * p.top;
-    int32_t* oi = p.part_idx + ((long long)row * p.chunks + chunk) * p.top;
-    for (int k = 0; k < p.top; ++k) {
-      float mv = -INFINITY;
-      int mi = INT_MAX;
-#pragma unroll
-      for (int j = 0; j < kHeld; ++j)
-        if (better(hv[j], hi[j], mv, mi)) {
-          mv = hv[j];
-          mi = hi[j];
-        }
-      float wv = mv;
-      int wi = mi;
-      warp_best(wv, wi);
-      if (lane == 0) {
-        ov[k] = wv;
-        oi[k] = wi;
-      }
-#pragma unroll
-      for (int j = 0; j < kHeld; ++j)
-        if (hi[j] == wi && wi != INT_MAX) {
-          hv[j] = -INFINITY;
-          hi[j] = INT_MAX;
-        }
-    }
   }
 }
 
@@ -172,9 +208,11 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a,
 
 constexpr int kProjMTiles = 4;  // 64 rows of h per CTA
 
-// CTA (n tile of 8 projection rows, m block of 64 position rows); warp w
-// takes the k16 steps w, w + 8, ...; the 8 warps' partial tiles are summed
-// in a fixed order.
+// CTA (n tile of 8 projection rows, m block of 64 position rows, k slice z
+// of 128 columns); warp w takes the slice's k16 step w alone, so all of its
+// fragment loads are in flight together; the 8 warps' tiles are summed in a
+// fixed order into the slice's partial, and the table kernel sums the
+// D / 128 slices in a fixed order.
 __global__ void __launch_bounds__(256) project_kernel(const SelectParams p) {
   __shared__ float s_acc[8][kProjMTiles * 16][8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -190,10 +228,11 @@ __global__ void __launch_bounds__(256) project_kernel(const SelectParams p) {
     acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
   const int ksteps = p.dim >> 4;
   const int n = n0 + g;
-  for (int ks = warp; ks < ksteps; ks += 8) {
+  {
+    const int ks = blockIdx.z * 8 + warp;
     const int kp = ks * 8 + t4;  // pair index of columns 16 ks + 2 t4
     uint32_t b0 = 0, b1 = 0;
-    if (n < p.rank) {
+    if (n < p.rank && ks < ksteps) {
       b0 = W[(long long)n * d2 + kp];
       b1 = W[(long long)n * d2 + kp + 4];
     }
@@ -201,11 +240,11 @@ __global__ void __launch_bounds__(256) project_kernel(const SelectParams p) {
     for (int m = 0; m < kProjMTiles; ++m) {
       const int r0 = m0 + m * 16 + g, r1 = r0 + 8;
       uint32_t a[4] = {0u, 0u, 0u, 0u};
-      if (r0 < rows) {
+      if (r0 < rows && ks < ksteps) {
         a[0] = X[(long long)r0 * d2 + kp];
         a[2] = X[(long long)r0 * d2 + kp + 4];
       }
-      if (r1 < rows) {
+      if (r1 < rows && ks < ksteps) {
         a[1] = X[(long long)r1 * d2 + kp];
         a[3] = X[(long long)r1 * d2 + kp + 4];
       }
@@ -226,7 +265,7 @@ __global__ void __launch_bounds__(256) project_kernel(const SelectParams p) {
 #pragma unroll
     for (int w = 0; w < 8; ++w) s += s_acc[w][r][c];
     if (m0 + r < rows && n0 + c < p.rank)
-      p.proj[(long long)(m0 + r) * p.rank + n0 + c] = s;
+      p.proj[((long long)blockIdx.z * rows + m0 + r) * p.rank + n0 + c] = s;
   }
 }
 
@@ -274,27 +313,52 @@ __global__ void __launch_bounds__(256) table_kernel(const SelectParams p) {
   __shared__ float s_vals[2][16];
   __shared__ float s_ah[kSelMaxRank][17];  // A[a, r] H_t[r], column a
   __shared__ float s_b[kSelMaxRank][17];   // B[c, r], column c
+  __shared__ float s_h[kSelMaxRank];
   const int t = blockIdx.x + 1, b = blockIdx.y;  // position t = 1 .. P-1
-  const int warp = threadIdx.x >> 5;
   const int P1 = p.positions - 1, K = p.top, R = p.rank;
   const int row = b * P1 + t - 1;
+  // candidate lists of t (warp 0) and t-1 (warp 1), side by side
+  const int warp = threadIdx.x >> 5;
   if (warp == 0) merge_candidates(p, row, s_ids[1], s_vals[1]);
   if (warp == 1 && t > 1) merge_candidates(p, row - 1, s_ids[0], s_vals[0]);
   if (threadIdx.x == 64 && t == 1) s_ids[0][0] = p.boundary[b];
   __syncthreads();
   const int n_pred = t == 1 ? 1 : K;
-  // gather the codebook rows: predecessors scaled by H_t, successors
-  const float* h = p.proj + (long long)row * R;
-  for (int e = threadIdx.x; e < 16 * R; e += 256) {
+  // H_t = the sum of the projection's k slices, in slice order
+  const int rows = p.batch * P1;
+  for (int r = threadIdx.x; r < R; r += 256) {
+    float hv = 0.f;
+    const int slices = (p.dim + 127) >> 7;
+#pragma unroll 8
+    for (int z = 0; z < slices; ++z)
+      hv += p.proj[((long long)z * rows + row) * R + r];
+    s_h[r] = hv;
+  }
+  __syncthreads();
+  // gather the codebook rows (all loads issued first): predecessors scaled
+  // by H_t, successors as they are
+  constexpr int kIt = 16 * kSelMaxRank / 256;
+  __nv_bfloat16 ga[kIt], gb[kIt];
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    const int e = threadIdx.x + it * 256;
     const int a = e / R, r = e - a * R;
-    float va = 0.f, vb = 0.f;
-    if (a < n_pred && s_ids[0][a] >= 0)
-      va = __fmul_rn(__bfloat162float(p.code_a[(long long)s_ids[0][a] * R + r]),
-                     h[r]);
-    if (a < K && s_ids[1][a] >= 0)
-      vb = __bfloat162float(p.code_b[(long long)s_ids[1][a] * R + r]);
-    s_ah[r][a] = va;
-    s_b[r][a] = vb;
+    const bool in = e < 16 * R;
+    ga[it] = in && a < n_pred && s_ids[0][a] >= 0
+                 ? p.code_a[(long long)s_ids[0][a] * R + r]
+                 : __float2bfloat16(0.f);
+    gb[it] = in && a < K && s_ids[1][a] >= 0
+                 ? p.code_b[(long long)s_ids[1][a] * R + r]
+                 : __float2bfloat16(0.f);
+  }
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    const int e = threadIdx.x + it * 256;
+    if (e < 16 * R) {
+      const int a = e / R, r = e - a * R;
+      s_ah[r][a] = __fmul_rn(__bfloat162float(ga[it]), s_h[r]);
+      s_b[r][a] = __bfloat162float(gb[it]);
+    }
   }
   __syncthreads();
   const int a = threadIdx.x >> 4, c = threadIdx.x & 15;
@@ -315,38 +379,42 @@ __global__ void __launch_bounds__(256) table_kernel(const SelectParams p) {
 
 // ---- 4. the walk ------------------------------------------------------------
 
-__global__ void __launch_bounds__(128) walk_kernel(const SelectParams p) {
-  __shared__ int s_back[4][16][16];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x * 4 + warp;
-  if (b >= p.batch) return;
+__global__ void __launch_bounds__(32) walk_kernel(const SelectParams p) {
+  __shared__ int s_back[1][16][16];
+  __shared__ float s_tr[1][15 * 16 * 16];
+  __shared__ int s_ci[1][15 * 16];
+  const int warp = 0, lane = threadIdx.x;
+  const int b = blockIdx.x;
   const int P1 = p.positions - 1, K = p.top;
   const float* tr = p.trans + (long long)b * P1 * K * K;
   const int32_t* ci = p.cand_ids + (long long)b * P1 * K;
+  // the request's tables and candidates, in one round of loads
+  for (int e = lane; e < P1 * K * K; e += 32) s_tr[warp][e] = tr[e];
+  for (int e = lane; e < P1 * K; e += 32) s_ci[warp][e] = ci[e];
+  __syncwarp();
+  const float* T = s_tr[warp];
   int32_t* out = p.draft_ids + (long long)b * p.positions;
   if (lane == 0) out[0] = p.boundary[b];
   if (p.mode == 0) {  // greedy
     int prev = 0;
     for (int t = 1; t <= P1; ++t) {
-      float v = lane < K ? tr[((long long)(t - 1) * K + prev) * K + lane]
-                         : -INFINITY;
+      float v = lane < K ? T[((t - 1) * K + prev) * K + lane] : -INFINITY;
       int i = lane < K ? lane : INT_MAX;
       warp_best(v, i);
       prev = i;
-      if (lane == 0) out[t] = ci[(t - 1) * K + prev];
+      if (lane == 0) out[t] = s_ci[warp][(t - 1) * K + prev];
     }
     return;
   }
   // MAP: best_t(c) = max_a best_{t-1}(a) + S_t(a, c), lowest a on ties
-  float best = lane < K ? tr[lane] : -INFINITY;  // t = 1 from the boundary
+  float best = lane < K ? T[lane] : -INFINITY;  // t = 1 from the boundary
   for (int t = 2; t <= P1; ++t) {
     float nb = -INFINITY;
     int arg = 0;
     for (int a2 = 0; a2 < K; ++a2) {
       const float ba = __shfl_sync(0xffffffffu, best, a2);
-      const float w = lane < K
-          ? __fadd_rn(ba, tr[((long long)(t - 1) * K + a2) * K + lane])
-          : -INFINITY;
+      const float w = lane < K ? __fadd_rn(ba, T[((t - 1) * K + a2) * K + lane])
+                               : -INFINITY;
       if (a2 == 0 || w > nb) {
         nb = w;
         arg = a2;
@@ -361,7 +429,7 @@ __global__ void __launch_bounds__(128) walk_kernel(const SelectParams p) {
   __syncwarp();
   if (lane == 0) {
     for (int t = P1; t >= 1; --t) {
-      out[t] = ci[(t - 1) * K + c];
+      out[t] = s_ci[warp][(t - 1) * K + c];
       if (t > 1) c = s_back[warp][t - 1][c];
     }
   }
@@ -374,15 +442,16 @@ cudaError_t launch_dflash2_select(const SelectParams& p, cudaStream_t s) {
   topk_partial_kernel<<<dim3(p.chunks, rows), kSelThreads, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  project_kernel<<<dim3((p.rank + 7) / 8, (rows + kProjMTiles * 16 - 1) /
-                                              (kProjMTiles * 16)),
+  project_kernel<<<dim3((p.rank + 7) / 8,
+                        (rows + kProjMTiles * 16 - 1) / (kProjMTiles * 16),
+                        (p.dim + 127) / 128),
                    256, 0, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   table_kernel<<<dim3(p.positions - 1, p.batch), 256, 0, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  walk_kernel<<<(p.batch + 3) / 4, 128, 0, s>>>(p);
+  walk_kernel<<<p.batch, 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

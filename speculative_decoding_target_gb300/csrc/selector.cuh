@@ -19,7 +19,7 @@ struct SelectParams {
   int32_t* draft_ids;           // [B, P]
   float* part_val;              // [rows, chunks, K] chunk top-K values
   int32_t* part_idx;            // [rows, chunks, K] and token ids
-  float* proj;                  // [rows, R] H = W_H h
+  float* proj;                  // [D / 128, rows, R] slices of W_H h
   int batch, positions, vocab, top, rank, dim, mode, chunks;
   int vec4;                     // logits rows 16-byte aligned, vocab % 4 == 0
 };

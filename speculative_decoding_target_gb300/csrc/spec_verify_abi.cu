@@ -579,7 +579,7 @@ SelectLayout select_layout(const spec_select_desc* d) {
   };
   L.part_val = take(rows * chunks * d->top * sizeof(float));
   L.part_idx = take(rows * chunks * d->top * sizeof(int32_t));
-  L.proj = take(rows * d->rank * sizeof(float));
+  L.proj = take((size_t)((d->dim + 127) / 128) * rows * d->rank * sizeof(float));
   L.trans = take(rows * d->top * d->top * sizeof(float));
   L.cand_ids = take(rows * d->top * sizeof(int32_t));
   L.cand_logit = take(rows * d->top * sizeof(float));
