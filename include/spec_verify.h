@@ -360,7 +360,8 @@ size_t spec_select_workspace_size(const spec_select_desc* desc);
  *                rows a >= 1 are -inf
  *   workspace    >= spec_select_workspace_size(desc) bytes, 256-byte
  *                aligned; contents need no initialisation
- * Four launches on `stream`; nothing is copied to the host.
+ * A counter reset and three launches on `stream`; nothing is copied to the
+ * host.
  */
 int spec_dflash2_select(const spec_select_desc* desc, const float* cand_logits,
                         const int32_t* boundary, const void* hidden,

@@ -11,7 +11,7 @@
 // of the token already chosen) or MAP (the best total score).  Ties go to
 // the lower candidate rank.
 //
-// Four launches:
+// Three launches (after a reset of the per-request counters):
 //   1. topk_partial_kernel, CTA per (8192-token chunk, position row): the
 //      chunk's K best in one streaming pass (K rounds of warp argmax over
 //      register-held logits, then a block merge);
@@ -20,8 +20,8 @@
 //      read once);
 //   3. table_kernel, CTA per (position, request): the candidate lists of t
 //      and t-1 from the chunk lists, the 2 x K codebook rows, and the K x K
-//      table in fp32;
-//   4. walk_kernel, one warp (CTA) per request: the greedy or MAP walk.
+//      table in fp32; the request's last CTA to finish (a counter) then
+//      walks the chain, greedy or MAP, with one warp.
 #include <climits>
 
 #include "selector.cuh"
@@ -59,15 +59,13 @@ __device__ __forceinline__ void warp_best(float& v, int& i) {
 // falls back to K block-wide argmax rounds over the whole chunk.
 constexpr int kSelPool = 512;
 
-// Rank of (v, i) among the warp's 32 pairs (0 = best).
-__device__ __forceinline__ int warp_rank(float v, int i) {
+// Rank of lane `lane`'s value among the warp's 32 (0 = best, lower lane
+// first on ties).
+__device__ __forceinline__ int warp_rank(float v, int lane) {
   int r = 0;
 #pragma unroll
-  for (int l = 0; l < 32; ++l) {
-    const float ov = __shfl_sync(0xffffffffu, v, l);
-    const int oi = __shfl_sync(0xffffffffu, i, l);
-    r += better(ov, oi, v, i);
-  }
+  for (int l = 0; l < 32; ++l)
+    r += better(__shfl_sync(0xffffffffu, v, l), l, v, lane);
   return r;
 }
 
@@ -308,6 +306,64 @@ __device__ void merge_candidates(const SelectParams& p, int row, int* ids,
   }
 }
 
+// ---- 4. the walk -------------------------------------------------------------
+
+// The greedy or MAP walk of request b by one warp, from the tables and
+// candidates in global memory (staged in shared memory: s_tr >= (P-1) K K
+// floats, s_ci >= (P-1) K ints, s_back >= 16 x 16 ints).
+__device__ void walk_request(const SelectParams& p, int b, float* s_tr,
+                             int* s_ci, int* s_back) {
+  const int lane = threadIdx.x & 31;
+  const int P1 = p.positions - 1, K = p.top;
+  // volatile: other CTAs wrote these; the fence above orders them
+  const volatile float* tr = p.trans + (long long)b * P1 * K * K;
+  const volatile int32_t* ci = p.cand_ids + (long long)b * P1 * K;
+  for (int e = lane; e < P1 * K * K; e += 32) s_tr[e] = tr[e];
+  for (int e = lane; e < P1 * K; e += 32) s_ci[e] = ci[e];
+  __syncwarp();
+  int32_t* out = p.draft_ids + (long long)b * p.positions;
+  if (lane == 0) out[0] = p.boundary[b];
+  if (p.mode == 0) {  // greedy
+    int prev = 0;
+    for (int t = 1; t <= P1; ++t) {
+      float v = lane < K ? s_tr[((t - 1) * K + prev) * K + lane] : -INFINITY;
+      int i = lane < K ? lane : INT_MAX;
+      warp_best(v, i);
+      prev = i;
+      if (lane == 0) out[t] = s_ci[(t - 1) * K + prev];
+    }
+    return;
+  }
+  // MAP: best_t(c) = max_a best_{t-1}(a) + S_t(a, c), lowest a on ties
+  float best = lane < K ? s_tr[lane] : -INFINITY;  // t = 1 from the boundary
+  for (int t = 2; t <= P1; ++t) {
+    float nb = -INFINITY;
+    int arg = 0;
+    for (int a2 = 0; a2 < K; ++a2) {
+      const float ba = __shfl_sync(0xffffffffu, best, a2);
+      const float w = lane < K
+          ? __fadd_rn(ba, s_tr[((t - 1) * K + a2) * K + lane])
+          : -INFINITY;
+      if (a2 == 0 || w > nb) {
+        nb = w;
+        arg = a2;
+      }
+    }
+    if (lane < K) s_back[(t - 1) * 16 + lane] = arg;
+    best = nb;
+  }
+  float v = best;
+  int c = lane < K ? lane : INT_MAX;
+  warp_best(v, c);
+  __syncwarp();
+  if (lane == 0) {
+    for (int t = P1; t >= 1; --t) {
+      out[t] = s_ci[(t - 1) * K + c];
+      if (t > 1) c = s_back[(t - 1) * 16 + c];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) table_kernel(const SelectParams p) {
   __shared__ int s_ids[2][16];
   __shared__ float s_vals[2][16];
@@ -317,24 +373,27 @@ __global__ void __launch_bounds__(256) table_kernel(const SelectParams p) {
   const int t = blockIdx.x + 1, b = blockIdx.y;  // position t = 1 .. P-1
   const int P1 = p.positions - 1, K = p.top, R = p.rank;
   const int row = b * P1 + t - 1;
-  // candidate lists of t (warp 0) and t-1 (warp 1), side by side
+  // candidate lists of t (warp 0) and t-1 (warp 1), side by side with
+  // H_t = the sum of the projection's k slices in slice order (warps 2..7)
   const int warp = threadIdx.x >> 5;
-  if (warp == 0) merge_candidates(p, row, s_ids[1], s_vals[1]);
-  if (warp == 1 && t > 1) merge_candidates(p, row - 1, s_ids[0], s_vals[0]);
-  if (threadIdx.x == 64 && t == 1) s_ids[0][0] = p.boundary[b];
-  __syncthreads();
-  const int n_pred = t == 1 ? 1 : K;
-  // H_t = the sum of the projection's k slices, in slice order
   const int rows = p.batch * P1;
-  for (int r = threadIdx.x; r < R; r += 256) {
-    float hv = 0.f;
+  if (warp == 0) {
+    merge_candidates(p, row, s_ids[1], s_vals[1]);
+  } else if (warp == 1) {
+    if (t > 1) merge_candidates(p, row - 1, s_ids[0], s_vals[0]);
+    else if (threadIdx.x == 32) s_ids[0][0] = p.boundary[b];
+  } else {
     const int slices = (p.dim + 127) >> 7;
+    for (int r = threadIdx.x - 64; r < R; r += 192) {
+      float hv = 0.f;
 #pragma unroll 8
-    for (int z = 0; z < slices; ++z)
-      hv += p.proj[((long long)z * rows + row) * R + r];
-    s_h[r] = hv;
+      for (int z = 0; z < slices; ++z)
+        hv += p.proj[((long long)z * rows + row) * R + r];
+      s_h[r] = hv;
+    }
   }
   __syncthreads();
+  const int n_pred = t == 1 ? 1 : K;
   // gather the codebook rows (all loads issued first): predecessors scaled
   // by H_t, successors as they are
   constexpr int kIt = 16 * kSelMaxRank / 256;
@@ -375,64 +434,18 @@ __global__ void __launch_bounds__(256) table_kernel(const SelectParams p) {
       p.cand_logit[((long long)b * P1 + t - 1) * K + c] = s_vals[1][c];
     }
   }
-}
-
-// ---- 4. the walk ------------------------------------------------------------
-
-__global__ void __launch_bounds__(32) walk_kernel(const SelectParams p) {
-  __shared__ int s_back[1][16][16];
-  __shared__ float s_tr[1][15 * 16 * 16];
-  __shared__ int s_ci[1][15 * 16];
-  const int warp = 0, lane = threadIdx.x;
-  const int b = blockIdx.x;
-  const int P1 = p.positions - 1, K = p.top;
-  const float* tr = p.trans + (long long)b * P1 * K * K;
-  const int32_t* ci = p.cand_ids + (long long)b * P1 * K;
-  // the request's tables and candidates, in one round of loads
-  for (int e = lane; e < P1 * K * K; e += 32) s_tr[warp][e] = tr[e];
-  for (int e = lane; e < P1 * K; e += 32) s_ci[warp][e] = ci[e];
-  __syncwarp();
-  const float* T = s_tr[warp];
-  int32_t* out = p.draft_ids + (long long)b * p.positions;
-  if (lane == 0) out[0] = p.boundary[b];
-  if (p.mode == 0) {  // greedy
-    int prev = 0;
-    for (int t = 1; t <= P1; ++t) {
-      float v = lane < K ? T[((t - 1) * K + prev) * K + lane] : -INFINITY;
-      int i = lane < K ? lane : INT_MAX;
-      warp_best(v, i);
-      prev = i;
-      if (lane == 0) out[t] = s_ci[warp][(t - 1) * K + prev];
-    }
-    return;
-  }
-  // MAP: best_t(c) = max_a best_{t-1}(a) + S_t(a, c), lowest a on ties
-  float best = lane < K ? T[lane] : -INFINITY;  // t = 1 from the boundary
-  for (int t = 2; t <= P1; ++t) {
-    float nb = -INFINITY;
-    int arg = 0;
-    for (int a2 = 0; a2 < K; ++a2) {
-      const float ba = __shfl_sync(0xffffffffu, best, a2);
-      const float w = lane < K ? __fadd_rn(ba, T[((t - 1) * K + a2) * K + lane])
-                               : -INFINITY;
-      if (a2 == 0 || w > nb) {
-        nb = w;
-        arg = a2;
-      }
-    }
-    if (lane < K) s_back[warp][t - 1][lane] = arg;
-    best = nb;
-  }
-  float v = best;
-  int c = lane < K ? lane : INT_MAX;
-  warp_best(v, c);
-  __syncwarp();
-  if (lane == 0) {
-    for (int t = P1; t >= 1; --t) {
-      out[t] = s_ci[warp][(t - 1) * K + c];
-      if (t > 1) c = s_back[warp][t - 1][c];
-    }
-  }
+  // the request's last table CTA to finish walks the chain
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0)
+    s_last = atomicAdd(&p.counters[b], 1) == P1 - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp == 0)
+    walk_request(p, b, &s_ah[0][0], reinterpret_cast<int*>(&s_b[0][0]),
+                 reinterpret_cast<int*>(&s_b[0][0]) + 15 * 16);
 }
 
 }  // namespace
@@ -449,9 +462,6 @@ cudaError_t launch_dflash2_select(const SelectParams& p, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   table_kernel<<<dim3(p.positions - 1, p.batch), 256, 0, s>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  walk_kernel<<<p.batch, 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -20,6 +20,7 @@ struct SelectParams {
   float* part_val;              // [rows, chunks, K] chunk top-K values
   int32_t* part_idx;            // [rows, chunks, K] and token ids
   float* proj;                  // [D / 128, rows, R] slices of W_H h
+  int* counters;                // [B] finished table CTAs (zeroed per call)
   int batch, positions, vocab, top, rank, dim, mode, chunks;
   int vec4;                     // logits rows 16-byte aligned, vocab % 4 == 0
 };

@@ -564,7 +564,8 @@ int check_select(const spec_select_desc* d) {
 }
 
 struct SelectLayout {
-  size_t part_val, part_idx, proj, trans, cand_ids, cand_logit, bytes;
+  size_t part_val, part_idx, proj, trans, cand_ids, cand_logit, counters,
+      bytes;
 };
 
 SelectLayout select_layout(const spec_select_desc* d) {
@@ -583,6 +584,7 @@ SelectLayout select_layout(const spec_select_desc* d) {
   L.trans = take(rows * d->top * d->top * sizeof(float));
   L.cand_ids = take(rows * d->top * sizeof(int32_t));
   L.cand_logit = take(rows * d->top * sizeof(float));
+  L.counters = take((size_t)d->batch * sizeof(int));
   L.bytes = o;
   return L;
 }
@@ -637,6 +639,7 @@ int spec_dflash2_select(const spec_select_desc* desc, const float* cand_logits,
   p.part_val = reinterpret_cast<float*>(ws + L.part_val);
   p.part_idx = reinterpret_cast<int32_t*>(ws + L.part_idx);
   p.proj = reinterpret_cast<float*>(ws + L.proj);
+  p.counters = reinterpret_cast<int*>(ws + L.counters);
   p.batch = desc->batch;
   p.positions = desc->positions;
   p.vocab = desc->vocab;
@@ -646,8 +649,11 @@ int spec_dflash2_select(const spec_select_desc* desc, const float* cand_logits,
   p.mode = desc->mode;
   p.chunks = (desc->vocab + specv::kSelChunk - 1) / specv::kSelChunk;
   p.vec4 = (desc->vocab % 4 == 0) && aligned(cand_logits, 16);
-  cudaError_t e =
-      specv::launch_dflash2_select(p, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(p.counters, 0, desc->batch * sizeof(int), s);
+  if (e != cudaSuccess)
+    return fail(SPEC_ERR_CUDA, "counter reset: %s", cudaGetErrorString(e));
+  e = specv::launch_dflash2_select(p, s);
   if (e != cudaSuccess)
     return fail(SPEC_ERR_CUDA, "selector launch: %s", cudaGetErrorString(e));
   return SPEC_OK;
