@@ -112,10 +112,14 @@ __device__ __forceinline__ void plan_prefix(const AttnParams& p, int* s_pre) {
   __syncthreads();
 }
 
-// Effective grid: the launched grid capped at U (every CTA below it owns at
-// least one unit, so consecutive CTAs of a segment have consecutive ids).
+// Effective grid: the launched grid, capped so that every CTA owns at least
+// kMinUnitsPerCta units (a small workload cut finer would write more split
+// partials than it saves in parallel reads).  Every CTA below it owns at
+// least one unit, so consecutive CTAs of a segment have consecutive ids.
+constexpr int kMinUnitsPerCta = 4;
 __device__ __forceinline__ int effective_grid(int grid, long long U) {
-  return U < grid ? (int)U : grid;
+  const long long want = (U + kMinUnitsPerCta - 1) / kMinUnitsPerCta;
+  return want < grid ? (int)want : grid;
 }
 
 // Sum of splits of every segment before segment k (the partial-slot base of
@@ -145,6 +149,16 @@ __device__ __forceinline__ int find_request(const int* s_pre, int batch,
     if ((long long)hkv * s_pre[mid] <= u) lo = mid; else hi = mid - 1;
   }
   return lo;
+}
+
+// Programmatic dependent launch: a primary grid lets its dependent grid be
+// scheduled; the dependent waits until the primary grid has completed and
+// its memory operations are visible.
+__device__ __forceinline__ void tc_grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void tc_grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Record an error message for spec_last_error() and return `code`.

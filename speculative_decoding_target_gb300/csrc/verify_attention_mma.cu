@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mi = lane >> 3, lr = lane & 7;
+  tc_grid_launch_dependents();  // the merge kernel may be scheduled now
   const int g4 = lane >> 2, t4 = lane & 3;
 
   plan_prefix(p, s_pre);
@@ -379,6 +380,9 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
   const int S = seg_splits(s0, nt, U, P);
   if (S <= 1) return;
   const int base = slot_base_warp(p, s_pre, k, U, P);
+  // launched as a programmatic dependent of the split kernel: everything
+  // above overlapped its tail; the partials are read only once it is done
+  tc_grid_dependency_wait();
   const float* lse = p.part_lse + (long long)base * p.rows + r;
   float mx = -INFINITY;
   for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lse[(long long)s * p.rows]);
@@ -391,14 +395,31 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
     const float* o =
         p.part_o + ((long long)base * p.rows + r) * kHeadDim + lane * 8;
     const long long stride = (long long)p.rows * kHeadDim;
-    for (int s = 0; s < S; ++s) {
-      const float w = exp2f(lse[(long long)s * p.rows] - mx);
-      den += w;
-      const float4 x0 = *reinterpret_cast<const float4*>(o + s * stride);
-      const float4 x1 = *reinterpret_cast<const float4*>(o + s * stride + 4);
-      acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z;
-      acc[3] += w * x0.w; acc[4] += w * x1.x; acc[5] += w * x1.y;
-      acc[6] += w * x1.z; acc[7] += w * x1.w;
+    // eight splits at a time, every load issued before any is used
+    for (int sb = 0; sb < S; sb += 8) {
+      float lv[8];
+      float4 x0[8], x1[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int s = sb + j;
+        if (s < S) {
+          lv[j] = lse[(long long)s * p.rows];
+          x0[j] = *reinterpret_cast<const float4*>(o + s * stride);
+          x1[j] = *reinterpret_cast<const float4*>(o + s * stride + 4);
+        } else {
+          lv[j] = -INFINITY;
+          x0[j] = x1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (sb + j >= S) break;
+        const float w = exp2f(lv[j] - mx);
+        den += w;
+        acc[0] += w * x0[j].x; acc[1] += w * x0[j].y; acc[2] += w * x0[j].z;
+        acc[3] += w * x0[j].w; acc[4] += w * x1[j].x; acc[5] += w * x1[j].y;
+        acc[6] += w * x1[j].z; acc[7] += w * x1[j].w;
+      }
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
@@ -467,9 +488,18 @@ int verify_split_bf16_ctas_per_sm(int rows) {
 }
 
 cudaError_t launch_verify_merge(const AttnParams& p, cudaStream_t s) {
-  dim3 grid((p.rows + 7) / 8, p.batch * p.hkv);
-  verify_merge_kernel<<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  // a programmatic dependent launch: the merge grid may start once every
+  // split CTA has begun, and waits for the split grid before its reads
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.rows + 7) / 8, p.batch * p.hkv);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, verify_merge_kernel, p);
 }
 
 }  // namespace specv

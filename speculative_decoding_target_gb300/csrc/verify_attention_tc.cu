@@ -604,6 +604,8 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
   }
 }
 
+constexpr int kPieceThreads = 5 * 32;  // warps 1..5: MMA issuer + softmax
+
 template <bool kFp8>
 __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     verify_split_tc_kernel(const AttnParams p,
@@ -617,7 +619,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
+  // the merge kernel may be scheduled now; it waits for this grid to finish
+  tc_grid_launch_dependents();
   plan_prefix(p, s_pre);
   const long long U = (long long)p.hkv * s_pre[p.batch];
   const int P = effective_grid(p.grid, U);
@@ -674,27 +677,33 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     pc.tok_end = min(j1 * kUnit, pc.len);
     pc.n_tiles = (pc.tok_end - pc.tok_begin + kT - 1) / kT;
 
-    if (warp >= 2 && warp < 6) load_q_tmem<kFp8>(p, pc, tmem);
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
+    // The producer (warp 0) and the FP8 dequant warps run ahead across
+    // pieces, gated only by the ring barriers; the MMA issuer and the
+    // softmax warps (1..5) meet around each piece, so Q in TMEM is written
+    // after the previous piece's last MMA and read after it is complete.
     if (warp == 0) {
       // the whole warp: lanes issue the copies of their pages
       produce<kFp8>(cx, pc, gj0, smem, &tm_k, &tm_v);
       last_loaded = gj0 + pc.n_tiles - 1;
       __syncwarp();
-    } else if (warp == 1) {
-      if (lane == 0) mma_piece<kFp8>(cx, pc, gj0, tmem, smem);
-      __syncwarp();
-    } else if (warp < 6) {
-      softmax_piece<kFp8>(cx, pc, gj0, tmem, smem, s_pre, U, P, c);
-    } else if (kFp8) {
-      dequant_piece(cx, pc, gj0, smem);
+    } else if (warp >= 6) {
+      if (kFp8) dequant_piece(cx, pc, gj0, smem);
+    } else {
+      if (warp >= 2) load_q_tmem<kFp8>(p, pc, tmem);
+      tc::fence_before();
+      tc::bar_sync_named(1, kPieceThreads);
+      tc::fence_after();
+      if (warp == 1) {
+        if (lane == 0) mma_piece<kFp8>(cx, pc, gj0, tmem, smem);
+        __syncwarp();
+      } else {
+        softmax_piece<kFp8>(cx, pc, gj0, tmem, smem, s_pre, U, P, c);
+      }
+      tc::fence_before();
+      tc::bar_sync_named(1, kPieceThreads);
+      tc::fence_after();
     }
     gj0 += pc.n_tiles;
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
   }
 
   // teardown: no copy or MMA may still be in flight
