@@ -71,6 +71,15 @@ __device__ __forceinline__ int units_of(int len) {
   return (len + kUnit - 1) / kUnit;
 }
 
+// The plan runs on virtual units: every (request, KV head) segment is
+// charged kPieceCost units in front of its real ones, the fixed cost of a
+// piece (loading Q, the first tile's latency, the epilogue) in 64-token
+// tiles.  CTAs split the virtual units evenly and process the real units in
+// their range, so a CTA that starts a segment owns fewer real units.  In
+// virtual units segment (b, g) starts at hkv s_pre[b] + g nt'_b and its real
+// units at kPieceCost beyond that, nt'_b = s_pre[b+1] - s_pre[b].
+constexpr int kPieceCost = 3;
+
 // First unit of CTA c.
 __device__ __forceinline__ long long cta_start(int c, long long U, int P) {
   return (long long)c * U / P;
@@ -88,8 +97,9 @@ __device__ __forceinline__ int seg_splits(long long s0, int nt, long long U,
   return cta_of(s0 + nt - 1, U, P) - cta_of(s0, U, P) + 1;
 }
 
-// Exclusive prefix of units per request into s_pre[0..batch] (s_pre[0]=0).
-// Called by the whole block; ends with __syncthreads().
+// Exclusive prefix of virtual units per request (real units + kPieceCost)
+// into s_pre[0..batch] (s_pre[0] = 0).  Called by the whole block; ends
+// with __syncthreads().
 __device__ __forceinline__ void plan_prefix(const AttnParams& p, int* s_pre) {
   const int tid = threadIdx.x;
   if (tid < 32) {
@@ -97,8 +107,9 @@ __device__ __forceinline__ void plan_prefix(const AttnParams& p, int* s_pre) {
     const int lane = tid;
     for (int base = 0; base < p.batch; base += 32) {
       int b = base + lane;
-      int v = b < p.batch ? units_of(clamp_len(p.seq_lens[b], p.max_tokens))
-                          : 0;
+      int v = b < p.batch
+                  ? units_of(clamp_len(p.seq_lens[b], p.max_tokens)) + kPieceCost
+                  : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         int n = __shfl_up_sync(0xffffffffu, v, o);
@@ -131,9 +142,9 @@ __device__ __forceinline__ int slot_base_warp(const AttnParams& p,
   int acc = 0;
   for (int kk = lane; kk < k; kk += 32) {
     int b = kk / p.hkv, g = kk - b * p.hkv;
-    int nt = s_pre[b + 1] - s_pre[b];
-    long long s0 = (long long)p.hkv * s_pre[b] + (long long)g * nt;
-    acc += seg_splits(s0, nt, U, P);
+    int ntv = s_pre[b + 1] - s_pre[b];
+    long long rs = (long long)p.hkv * s_pre[b] + (long long)g * ntv + kPieceCost;
+    acc += seg_splits(rs, ntv - kPieceCost, U, P);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);

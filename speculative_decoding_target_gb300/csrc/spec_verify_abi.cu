@@ -148,7 +148,8 @@ int check_desc(const spec_attn_desc* d) {
   if (max_tokens > (1LL << 30))
     return fail(SPEC_ERR_ARG, "max_pages_per_seq * page_size exceeds 2^30");
   const long long units = (long long)d->batch * d->num_kv_heads *
-                          ((max_tokens + specv::kUnit - 1) / specv::kUnit);
+                          ((max_tokens + specv::kUnit - 1) / specv::kUnit +
+                           specv::kPieceCost);
   if (units > (1LL << 30))
     return fail(SPEC_ERR_ARG, "batch * kv heads * units exceeds 2^30");
   if (d->batch * (long long)d->num_kv_heads > 65535)

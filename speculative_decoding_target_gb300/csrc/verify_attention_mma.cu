@@ -150,13 +150,18 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
 
   while (u < u_end) {
     const int b = find_request(s_pre, p.batch, p.hkv, u);
-    const int nt = s_pre[b + 1] - s_pre[b];
+    const int ntv = s_pre[b + 1] - s_pre[b];  // virtual units
     const long long rb = (long long)p.hkv * s_pre[b];
-    const int g = (int)((u - rb) / nt);
-    const long long s0 = rb + (long long)g * nt;
-    const int j0 = (int)(u - s0);
-    const int j1 = (int)(u_end - s0 < nt ? u_end - s0 : nt);
-    u = s0 + j1;
+    const int g = (int)((u - rb) / ntv);
+    const long long vs = rb + (long long)g * ntv;
+    const int j0v = (int)(u - vs);
+    const int j1v = (int)(u_end - vs < ntv ? u_end - vs : ntv);
+    u = vs + j1v;
+    // real units of the piece; a range of phantom units only does nothing
+    const int j0 = max(j0v - kPieceCost, 0), j1 = max(j1v - kPieceCost, 0);
+    if (j1 <= j0) continue;  // uniform over the CTA
+    const int nt = ntv - kPieceCost;
+    const long long s0 = vs + kPieceCost;  // the segment's first real unit
 
     const int len = clamp_len(p.seq_lens[b], p.max_tokens);
     const int qb = block_rows(p, b);
@@ -364,7 +369,8 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
   plan_prefix(p, s_pre);
   const long long U = (long long)p.hkv * s_pre[p.batch];
   const int k = blockIdx.y, b = k / p.hkv, g = k - b * p.hkv;
-  const int nt = s_pre[b + 1] - s_pre[b];
+  const int ntv = s_pre[b + 1] - s_pre[b];  // virtual units
+  const int nt = ntv - kPieceCost;           // real units
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + warp;
   if (r >= p.rows) return;
@@ -376,7 +382,8 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
     return;
   }
   const int P = effective_grid(p.grid, U);
-  const long long s0 = (long long)p.hkv * s_pre[b] + (long long)g * nt;
+  const long long s0 =
+      (long long)p.hkv * s_pre[b] + (long long)g * ntv + kPieceCost;
   const int S = seg_splits(s0, nt, U, P);
   if (S <= 1) return;
   const int base = slot_base_warp(p, s_pre, k, U, P);

@@ -665,13 +665,18 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   while (u < u_end) {
     Piece pc;
     pc.b = find_request(s_pre, p.batch, p.hkv, u);
-    pc.nt = s_pre[pc.b + 1] - s_pre[pc.b];
+    const int ntv = s_pre[pc.b + 1] - s_pre[pc.b];  // virtual units
     const long long rb = (long long)p.hkv * s_pre[pc.b];
-    pc.g = (int)((u - rb) / pc.nt);
-    pc.s0 = rb + (long long)pc.g * pc.nt;
-    const int j0 = (int)(u - pc.s0);
-    const int j1 = (int)(u_end - pc.s0 < pc.nt ? u_end - pc.s0 : pc.nt);
-    u = pc.s0 + j1;
+    pc.g = (int)((u - rb) / ntv);
+    const long long vs = rb + (long long)pc.g * ntv;
+    const int j0v = (int)(u - vs);
+    const int j1v = (int)(u_end - vs < ntv ? u_end - vs : ntv);
+    u = vs + j1v;
+    // real units of the piece; a range of phantom units only does nothing
+    const int j0 = max(j0v - kPieceCost, 0), j1 = max(j1v - kPieceCost, 0);
+    if (j1 <= j0) continue;  // the same decision in every warp
+    pc.nt = ntv - kPieceCost;
+    pc.s0 = vs + kPieceCost;  // the segment's first real unit
     pc.len = clamp_len(p.seq_lens[pc.b], p.max_tokens);
     pc.tok_begin = j0 * kUnit;
     pc.tok_end = min(j1 * kUnit, pc.len);
