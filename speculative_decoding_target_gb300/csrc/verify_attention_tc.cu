@@ -417,26 +417,34 @@ __device__ __forceinline__ void load_q_tmem(const AttnParams& p, const Piece& pc
       p.q + (((long long)pc.b * p.q_len + i) * p.hq + h) * kHeadDim);
   const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16) + kColQ;
 #pragma unroll 1
-  for (int cb = 0; cb < 4; ++cb) {  // 64 channels = 32 columns per step
-    uint32_t v[32];
+  for (int half = 0; half < 2; ++half) {  // 128 channels: loads in flight
+    uint4 xs[16];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      uint4 x = valid ? __ldg(src + cb * 8 + k) : make_uint4(0, 0, 0, 0);
-      if (kFp8) {  // bf16 pairs -> fp16 pairs
-        uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+    for (int k = 0; k < 16; ++k)
+      xs[k] = valid ? __ldg(src + half * 16 + k) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
-          const __half2 h2 = __floats2half2_rn(__low2float(b2), __high2float(b2));
-          w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+    for (int cq = 0; cq < 2; ++cq) {  // 64 channels = 32 columns per store
+      const int cb = half * 2 + cq;
+      uint32_t v[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        uint4 x = xs[cq * 8 + k];
+        if (kFp8) {  // bf16 pairs -> fp16 pairs
+          uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+            const __half2 h2 = __floats2half2_rn(__low2float(b2), __high2float(b2));
+            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
         }
+        v[4 * k] = x.x;
+        v[4 * k + 1] = x.y;
+        v[4 * k + 2] = x.z;
+        v[4 * k + 3] = x.w;
       }
-      v[4 * k] = x.x;
-      v[4 * k + 1] = x.y;
-      v[4 * k + 2] = x.z;
-      v[4 * k + 3] = x.w;
+      tc::tmem_st32(lane_base + cb * 32, reinterpret_cast<const float*>(v));
     }
-    tc::tmem_st32(lane_base + cb * 32, reinterpret_cast<const float*>(v));
   }
   tc::tmem_wait_st();
 }
@@ -456,6 +464,12 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
   const int lim = causal_limit(pc.len, block_rows(p, pc.b), i);
   const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
   const float sl2 = p.scale_log2;
+  // where this piece's result goes (independent of the tiles: worked out
+  // here, off the epilogue's critical path)
+  const int S = seg_splits(pc.s0, pc.nt, U, P);
+  const int slot = S > 1 ? slot_base_warp(p, s_pre, pc.b * p.hkv + pc.g, U, P) +
+                               (c - cta_of(pc.s0, U, P))
+                         : 0;
 
   float m = -INFINITY, l = 0.f;
   for (int jt = 0; jt < pc.n_tiles; ++jt) {
@@ -556,18 +570,17 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
   tc::fence_after();
   const float inv = l > 0.f ? 1.f / l : 0.f;
   const float mu = m == -INFINITY ? 0.f : m;
-  const int S = seg_splits(pc.s0, pc.nt, U, P);
   const int head = pc.g * p.group + (r - i * p.group);
   if (S == 1) {
     __nv_bfloat16* dst =
         p.out + (((long long)pc.b * p.q_len + i) * p.hq + head) * kHeadDim;
 #pragma unroll 1
-    for (int cb = 0; cb < 8; ++cb) {
-      float o[32];
-      tc::tmem_ld32(lane_base + cb * 32, o);
+    for (int cb = 0; cb < 8; cb += 2) {  // 64 columns per TMEM load
+      float o[64];
+      tc::tmem_ld64(lane_base + cb * 32, o);
       if (valid) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 8; ++k) {
           uint4 v;
           __nv_bfloat162 t;
           t = __floats2bfloat162_rn(o[8 * k] * inv, o[8 * k + 1] * inv);
@@ -583,16 +596,14 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
       }
     }
   } else {
-    const int k = pc.b * p.hkv + pc.g;
-    const int slot = slot_base_warp(p, s_pre, k, U, P) + (c - cta_of(pc.s0, U, P));
     float* dst = p.part_o + ((long long)slot * p.rows + r) * kHeadDim;
 #pragma unroll 1
-    for (int cb = 0; cb < 8; ++cb) {
-      float o[32];
-      tc::tmem_ld32(lane_base + cb * 32, o);
+    for (int cb = 0; cb < 8; cb += 2) {  // 64 columns per TMEM load
+      float o[64];
+      tc::tmem_ld64(lane_base + cb * 32, o);
       if (valid) {
 #pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4)
+        for (int k4 = 0; k4 < 16; ++k4)
           *reinterpret_cast<float4*>(dst + cb * 32 + 4 * k4) =
               make_float4(o[4 * k4] * inv, o[4 * k4 + 1] * inv,
                           o[4 * k4 + 2] * inv, o[4 * k4 + 3] * inv);
@@ -735,10 +746,9 @@ template <bool kFp8>
 cudaError_t launch(const AttnParams& p, const CUtensorMap& tm_k,
                    const CUtensorMap& tm_v, cudaStream_t s) {
   using C = Cfg<kFp8>;
-  cudaError_t e = cudaFuncSetAttribute(verify_split_tc_kernel<kFp8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmem);
-  if (e != cudaSuccess) return e;
+  // the shared-memory attribute was set on this device by ctas_per_sm(),
+  // which sizing the grid always runs first (an attribute call per launch
+  // costs microseconds of host time)
   verify_split_tc_kernel<kFp8><<<p.grid, C::kThreads, C::kSmem, s>>>(p, tm_k, tm_v);
   return cudaGetLastError();
 }
