@@ -667,10 +667,11 @@ def measure_select(w: wl.VerifyWorkload, dev, steps: int, warmup: int,
                                      1),
         "frac_of_peak_greedy": round(
             nbytes / (res["greedy_ms"] * 1e-3) / 1e9 / peak, 4),
-        "gpu_launches": 4 * 2 * steps,
-        "note": "four launches per call: chunked top-K over the candidate "
-                "logits (the streaming pass), the rank projection, the "
-                "transition tables, the walk",
+        "gpu_launches": 3 * 2 * steps,
+        "note": "three launches per call (after a counter reset): chunked "
+                "top-K over the candidate logits (the streaming pass), the "
+                "rank projection, the transition tables with the walk in "
+                "each request's last table CTA",
     })
     return res
 

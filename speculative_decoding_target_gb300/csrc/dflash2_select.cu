@@ -48,26 +48,15 @@ __device__ __forceinline__ void warp_best(float& v, int& i) {
 
 // ---- 1. chunk top-K -------------------------------------------------------
 
-// Exact top-K of a chunk without serial rounds.  (i) A bound: lane l's rank
-// among its warp's 32 lane maxima is a count (32 independent shuffles);
-// the maximum of rank K-1, T_w, has K values of the warp at or above it, so
-// the chunk's K best all lie at or above T = max_w T_w.  (ii) The values
-// >= T (about 1% of a chunk of random logits) go to a shared pool, and each
-// pool entry's rank is the number of entries that beat it (value, then
-// lower token id): entries of rank < K are the chunk's top K, already in
-// order.  A pool that overflows (heavy ties, or fewer than K finite values)
+// Exact top-K of a chunk (K <= 16) without serial rounds.  (i) A bound:
+// each of the 8 warps holds two values at or above its second largest lane
+// maximum, so the chunk holds 16 >= K values at or above the smallest of
+// those, T, and its K best all lie at or above T.  (ii) The values >= T
+// (under 1% of a chunk of random logits) go to a shared pool, and each pool
+// entry's rank is the number of entries that beat it (value, then lower
+// token id): entries of rank < K are the chunk's top K, already in order.  A pool that overflows (heavy ties, or fewer than K finite values)
 // falls back to K block-wide argmax rounds over the whole chunk.
 constexpr int kSelPool = 512;
-
-// Rank of lane `lane`'s value among the warp's 32 (0 = best, lower lane
-// first on ties).
-__device__ __forceinline__ int warp_rank(float v, int lane) {
-  int r = 0;
-#pragma unroll
-  for (int l = 0; l < 32; ++l)
-    r += better(__shfl_sync(0xffffffffu, v, l), l, v, lane);
-  return r;
-}
 
 __global__ void __launch_bounds__(kSelThreads, 3)
     topk_partial_kernel(const SelectParams p) {
@@ -108,19 +97,24 @@ __global__ void __launch_bounds__(kSelThreads, 3)
     const int id = begin + 4 * (threadIdx.x + (e >> 2) * kSelThreads) + (e & 3);
     return id < end ? id : INT_MAX;
   };
-  // (i) the bound
+  // (i) the bound: every warp holds two values at or above its second
+  // largest lane maximum, so the 8 warps hold 16 >= K values at or above
+  // the smallest of those
   float m = v[0];
 #pragma unroll
   for (int e = 1; e < kPer; ++e) m = fmaxf(m, v[e]);
-  const int rk = warp_rank(m, lane);
-  const unsigned at = __ballot_sync(0xffffffffu, rk == p.top - 1);
-  const float tw = __shfl_sync(0xffffffffu, m, __ffs(at) - 1);
-  if (lane == 0) s_tw[warp] = tw;
+  float m1 = m;
+  int l1 = lane;
+  warp_best(m1, l1);
+  float m2 = lane == l1 ? -INFINITY : m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+  if (lane == 0) s_tw[warp] = m2;
   if (threadIdx.x == 0) s_n = 0;
   __syncthreads();
   float T = s_tw[0];
 #pragma unroll
-  for (int w = 1; w < kWarps; ++w) T = fmaxf(T, s_tw[w]);
+  for (int w = 1; w < kWarps; ++w) T = fminf(T, s_tw[w]);
   // (ii) the pool of values >= T
   const bool finite_bound = T > -INFINITY;
   if (finite_bound) {
