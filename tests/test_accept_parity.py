@@ -102,3 +102,10 @@ def test_full_size_workloads(name):
     a = ref["accept_len"]
     assert sum((a >= j).mean() for j in range(1, w.q_len)) == \
         pytest.approx(a.mean(), abs=1e-12)
+
+
+def test_row_limit():
+    # batch * q_len up to the 65,535-row limit of the argmax grid
+    inp = wl.make_accept_inputs(batch=4095, q_len=16, vocab=33, accept_p=0.9,
+                                seed=4095, device=DEV)
+    _run_both(inp["logits"], inp["draft_ids"])

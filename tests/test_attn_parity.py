@@ -169,3 +169,42 @@ def test_full_size_workloads_sampled_rows(name):
     rows = _sample_rows(w, n, w.seed)
     ref = oracle_attention(inp, rows=np.asarray(rows, np.int64))
     assert_attention_close(rows_of(out, rows), ref, fp8, name)
+
+
+def test_hundreds_of_tiny_requests():
+    # many segments: the plan's prefix over the batch, phantom-only CTAs,
+    # split slots across hundreds of (request, head) segments
+    g = torch.Generator().manual_seed(17)
+    prefixes = torch.randint(0, 90, (600,), generator=g).tolist()
+    prefixes[0] = 0
+    inp = _case(600, 8, prefixes, 16, seed=600)
+    _check_all(inp, "600 tiny requests")
+
+
+def test_every_sequence_empty_gives_zero_output():
+    inp = _case(5, 8, [40, 0, 7, 100, 3], 16, seed=8)
+    inp["seq_lens"] = torch.zeros(5, dtype=torch.int32, device=DEV)
+    out = gpu_attention(inp)
+    torch.cuda.synchronize()
+    assert torch.all(out.float() == 0)
+
+
+def test_fp8_widest_tile_with_ragged_widths():
+    # q_len 16 x group 8 = 128 rows, every TMEM lane in use
+    inp = _case(4, 16, [700, 70, 1500, 5], 64, kv_dtype="fp8_e4m3", hq=32,
+                hkv=4, seed=128)
+    import speculative_decoding_target_gb300 as sv
+    ql = torch.tensor([16, 9, 1, 0], dtype=torch.int32, device=DEV)
+    out = sv.verify_attention(inp["q"], inp["k_pages"], inp["v_pages"],
+                              inp["page_table"], inp["seq_lens"],
+                              scale=inp["scale"], k_scales=inp["k_scales"],
+                              v_scales=inp["v_scales"], q_lens=ql)
+    torch.cuda.synchronize()
+    bits = wl.to_numpy_bits
+    import oracle
+    ref = oracle.verify_attention(
+        bits(inp["q"]), bits(inp["k_pages"]), bits(inp["v_pages"]),
+        inp["page_table"].cpu().numpy(), inp["seq_lens"].cpu().numpy(),
+        num_kv_heads=4, scale=inp["scale"], k_scales=bits(inp["k_scales"]),
+        v_scales=bits(inp["v_scales"]), q_lens=ql.cpu().numpy())
+    assert_attention_close(rows_of(out), ref, True, "fp8 128-row tile")
