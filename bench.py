@@ -268,52 +268,8 @@ def run_gpu(args, w: wl.VerifyWorkload):
     # its inputs from pinned host memory and reads its results back
     e2e = None
     if not args.no_e2e:
-        host = {k: inp[k].cpu().pin_memory()
-                for k in ("q", "page_table", "seq_lens", "logits",
-                          "draft_ids")}
-        dev_in = {k: torch.empty_like(inp[k]) for k in host}
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h_acc = torch.empty(w.batch, dtype=torch.int32).pin_memory()
-        h_nxt = torch.empty(w.batch, dtype=torch.int32).pin_memory()
-        h_tok = torch.empty((w.batch, w.q_len), dtype=torch.int32).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = sum(t.numel() * t.element_size()
-                  for t in (h_out, h_acc, h_nxt, h_tok))
-
-        def e2e_step():
-            for k, t in host.items():
-                dev_in[k].copy_(t, non_blocking=True)
-            _native.verify_attention_into(
-                desc, dev_in["q"], inp["k_pages"], inp["v_pages"],
-                inp["k_scales"], inp["v_scales"], dev_in["page_table"],
-                dev_in["seq_lens"], inp["scale"], out, attn_ws, stream)
-            _native.greedy_accept_into(dev_in["logits"], dev_in["draft_ids"],
-                                       acc, nxt, toks, acc_ws, stream)
-            h_out.copy_(out, non_blocking=True)
-            h_acc.copy_(acc, non_blocking=True)
-            h_nxt.copy_(nxt, non_blocking=True)
-            h_tok.copy_(toks, non_blocking=True)
-
-        for _ in range(args.warmup):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
-        e_ms = e0.elapsed_time(e1)
-        e_ms = max_over_ranks(e_ms, dev)
-        e2e = {"value": round(job_throughput(ws_n, args.steps, e_ms), 3),
-               "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h),
-               "note": "KV pool resident in HBM (it is the cache state); "
-                       "per-step q, page table, seq_lens, logits and drafts "
-                       "copied in, out/accept/next/tokens copied back"}
+        e2e = measure_e2e(args, w, inp, desc, attn_ws, acc_ws, out, stream,
+                          dev, ws_n, barrier)
 
     kv_b, logit_b = algorithmic_bytes(w, seq_lens)
     attn_avg_s = statistics.mean(attn_ms) / 1e3
@@ -388,6 +344,107 @@ def run_gpu(args, w: wl.VerifyWorkload):
         import torch.distributed as dist
         dist.destroy_process_group()
     return result, rank
+
+
+# ------------------------------------------------------------- end to end --
+
+def measure_e2e(args, w, inp, desc, attn_ws, acc_ws, out, stream, dev, ws_n,
+                barrier):
+    """The verify step through the public API with host buffers: every step
+    copies its q, page table, seq_lens, logits and drafts in from pinned host
+    memory and reads its out / accept / next / tokens back.  Two sets of
+    device buffers let step k+1's copy-in (one stream) and step k-1's
+    read-back (another) overlap step k's kernels; events keep each set's
+    copy-in after the compute that last read it and its compute after the
+    read-back of its previous result.  The KV pool stays resident: it is
+    the cache state, not a per-step input."""
+    from speculative_decoding_target_gb300 import _native
+    keys = ("q", "page_table", "seq_lens", "logits", "draft_ids")
+    host = {k: inp[k].cpu().pin_memory() for k in keys}
+    dev_in = [{k: torch.empty_like(inp[k]) for k in keys} for _ in range(2)]
+    i32 = dict(dtype=torch.int32, device=dev)
+    dev_out = [dict(out=torch.empty_like(out),
+                    acc=torch.empty(w.batch, **i32),
+                    nxt=torch.empty(w.batch, **i32),
+                    toks=torch.empty((w.batch, w.q_len), **i32))
+               for _ in range(2)]
+    h_out = [dict(out=torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                  acc=torch.empty(w.batch, dtype=torch.int32).pin_memory(),
+                  nxt=torch.empty(w.batch, dtype=torch.int32).pin_memory(),
+                  toks=torch.empty((w.batch, w.q_len),
+                                   dtype=torch.int32).pin_memory())
+             for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
+    s_in, s_back = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    copied = [ev(), ev()]
+    computed = [ev(), ev()]
+    read = [ev(), ev()]
+    used = [False, False]
+
+    def copy_in(k):
+        b = k & 1
+        with torch.cuda.stream(s_in):
+            if used[b]:
+                s_in.wait_event(computed[b])  # the set's last reader is done
+            for name, t in host.items():
+                dev_in[b][name].copy_(t, non_blocking=True)
+            copied[b].record(s_in)
+
+    def compute(k):
+        b = k & 1
+        stream.wait_event(copied[b])
+        if used[b]:
+            stream.wait_event(read[b])  # the set's last result was read back
+        d, o = dev_in[b], dev_out[b]
+        _native.verify_attention_into(
+            desc, d["q"], inp["k_pages"], inp["v_pages"], inp["k_scales"],
+            inp["v_scales"], d["page_table"], d["seq_lens"], inp["scale"],
+            o["out"], attn_ws, stream)
+        _native.greedy_accept_into(d["logits"], d["draft_ids"], o["acc"],
+                                   o["nxt"], o["toks"], acc_ws, stream)
+        computed[b].record(stream)
+        used[b] = True
+
+    def read_back(k):
+        b = k & 1
+        with torch.cuda.stream(s_back):
+            s_back.wait_event(computed[b])
+            for name, t in h_out[b].items():
+                t.copy_(dev_out[b][name], non_blocking=True)
+            read[b].record(s_back)
+
+    def run(n, start_ev=None):
+        if start_ev is not None:
+            s_in.wait_event(start_ev)
+        copy_in(0)
+        for k in range(n):
+            compute(k)
+            if k + 1 < n:
+                copy_in(k + 1)  # overlaps compute(k)
+            read_back(k)
+        stream.wait_event(read[(n - 1) & 1])
+
+    run(args.warmup)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(args.steps, e0)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    return {"value": round(job_throughput(ws_n, args.steps, e_ms), 3),
+            "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h),
+            "note": "KV pool resident in HBM (it is the cache state); every "
+                    "step copies its q, page table, seq_lens, logits and "
+                    "drafts in from pinned host memory and its out / "
+                    "accept / next / tokens back, double-buffered so that "
+                    "copies overlap the previous step's kernels"}
 
 
 # ------------------------------------------------------ block KV append --
