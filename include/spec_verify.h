@@ -44,7 +44,7 @@ extern "C" {
 #define SPEC_ERR_ARG (-1)         /* null pointer, bad size or shape */
 #define SPEC_ERR_ALIGN (-2)       /* pointer not aligned as documented */
 #define SPEC_ERR_WORKSPACE (-3)   /* workspace missing or too small */
-#define SPEC_ERR_UNSUPPORTED (-4) /* valid request this build does not run */
+#define SPEC_ERR_UNSUPPORTED (-4) /* valid request this library does not run */
 #define SPEC_ERR_CUDA (-5)        /* CUDA runtime error (no device, launch) */
 
 /* Device-side status bits (see spec_verify_status). */
