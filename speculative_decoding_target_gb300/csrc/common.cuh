@@ -183,6 +183,14 @@ cudaError_t launch_verify_split_tc(const AttnParams& p, const CUtensorMap& tm_k,
                                    const CUtensorMap& tm_v, cudaStream_t s);
 int verify_split_tc_ctas_per_sm(bool fp8);
 int verify_split_tc_box_rows(int page_size);
+// FP8 KV with at most kFp8tMaxRows block rows per KV head: the kernel with
+// K and V^T as tensor-memory operands (tensor maps over the byte pools with
+// boxes of 128 bytes x box_rows rows).
+constexpr int kFp8tMaxRows = 64;
+cudaError_t launch_verify_split_fp8t(const AttnParams& p,
+                                     const CUtensorMap& tm_k,
+                                     const CUtensorMap& tm_v, cudaStream_t s);
+int verify_split_fp8t_ctas_per_sm();
 // The tcgen05 kernel loads whole 8-row swizzle groups (and, for FP8 KV,
 // 16-byte multiples of the scales) per page run, so it needs pages of at
 // least 8 tokens; smaller bf16 pages take the mma.sync kernel.

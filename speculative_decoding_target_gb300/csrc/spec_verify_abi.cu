@@ -36,13 +36,21 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_sms[kMaxDevices];
-int g_occ[kMaxDevices][11];  // split-kernel CTAs per SM: [w] mma.sync with w
+int g_occ[kMaxDevices][12];  // split-kernel CTAs per SM: [w] mma.sync with w
                              // compute warps, [9] tcgen05 bf16, [10] tcgen05
-                             // FP8
+                             // FP8, [11] tcgen05 FP8 with TMEM KV operands
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool use_tc(const spec_attn_desc* d) {
   return d->page_size >= specv::kTcMinPageSize;
+}
+
+// FP8 KV blocks of at most kFp8tMaxRows rows take the kernel whose K and V^T
+// tiles are tensor-memory operands.
+bool use_fp8t(const spec_attn_desc* d) {
+  return d->kv_dtype == SPEC_KV_FP8_E4M3 && use_tc(d) &&
+         (long long)d->q_len * (d->num_q_heads / d->num_kv_heads) <=
+             specv::kFp8tMaxRows;
 }
 
 int tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
@@ -83,6 +91,28 @@ int make_pool_map(CUtensorMap* map, const void* base, long long rows,
   return SPEC_OK;
 }
 
+// 2-D view of an FP8 page pool: rows = num_pages * Hkv * page_size, 256
+// bytes per row; boxes of 128 bytes x box_rows rows with the 128-byte
+// swizzle.
+int make_pool_map_u8(CUtensorMap* map, const void* base, long long rows,
+                     int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int rc = tensor_map_encoder(&enc);
+  if (rc) return rc;
+  cuuint64_t dims[2] = {(cuuint64_t)specv::kHeadDim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)specv::kHeadDim};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t elem[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                   const_cast<void*>(base), dims, strides, box, elem,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(SPEC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return SPEC_OK;
+}
+
 int current_device(int* dev) {
   cudaError_t e = cudaGetDevice(dev);
   if (e != cudaSuccess)
@@ -98,7 +128,8 @@ int split_grid(int rows, bool tc, bool fp8, int* grid) {
   int dev;
   int rc = current_device(&dev);
   if (rc) return rc;
-  const int w = tc ? (fp8 ? 10 : 9) : (rows + 15) / 16;
+  const bool fp8t = tc && fp8 && rows <= specv::kFp8tMaxRows;
+  const int w = fp8t ? 11 : (tc ? (fp8 ? 10 : 9) : (rows + 15) / 16);
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_sms[dev]) {
     int n = 0;
@@ -109,8 +140,9 @@ int split_grid(int rows, bool tc, bool fp8, int* grid) {
     g_sms[dev] = n;
   }
   if (!g_occ[dev][w]) {
-    int occ = tc ? specv::verify_split_tc_ctas_per_sm(fp8)
-                 : specv::verify_split_bf16_ctas_per_sm(rows);
+    int occ = fp8t ? specv::verify_split_fp8t_ctas_per_sm()
+              : tc  ? specv::verify_split_tc_ctas_per_sm(fp8)
+                    : specv::verify_split_bf16_ctas_per_sm(rows);
     if (occ <= 0)
       return fail(SPEC_ERR_CUDA, "split kernel does not fit on an SM");
     g_occ[dev][w] = occ;
@@ -282,14 +314,19 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
   p.box_rows = specv::verify_split_tc_box_rows(desc->page_size);
   p.scale_log2 = scale * 1.4426950408889634f;
   const bool tc = use_tc(desc);
+  const bool fp8t = use_fp8t(desc);
   CUtensorMap tm_k, tm_v;
-  std::memset(&tm_k, 0, sizeof tm_k);  // unused by the FP8 variant
+  std::memset(&tm_k, 0, sizeof tm_k);  // unused by the bulk-copy FP8 kernel
   std::memset(&tm_v, 0, sizeof tm_v);
+  const long long pool_rows =
+      (long long)desc->num_pages * desc->num_kv_heads * desc->page_size;
   if (tc && !fp8) {
-    const long long pool_rows =
-        (long long)desc->num_pages * desc->num_kv_heads * desc->page_size;
     rc = make_pool_map(&tm_k, k_pages, pool_rows, p.box_rows);
     if (!rc) rc = make_pool_map(&tm_v, v_pages, pool_rows, p.box_rows);
+    if (rc) return rc;
+  } else if (fp8t) {
+    rc = make_pool_map_u8(&tm_k, k_pages, pool_rows, p.box_rows);
+    if (!rc) rc = make_pool_map_u8(&tm_v, v_pages, pool_rows, p.box_rows);
     if (rc) return rc;
   }
 
@@ -300,8 +337,9 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
     if (e != cudaSuccess)
       return fail(SPEC_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
   }
-  e = tc ? specv::launch_verify_split_tc(p, tm_k, tm_v, s)
-         : specv::launch_verify_split_bf16(p, s);
+  e = fp8t ? specv::launch_verify_split_fp8t(p, tm_k, tm_v, s)
+       : tc  ? specv::launch_verify_split_tc(p, tm_k, tm_v, s)
+             : specv::launch_verify_split_bf16(p, s);
   if (e != cudaSuccess)
     return fail(SPEC_ERR_CUDA, "split kernel launch: %s", cudaGetErrorString(e));
   e = specv::launch_verify_merge(p, s);

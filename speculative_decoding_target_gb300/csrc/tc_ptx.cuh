@@ -49,6 +49,22 @@ __device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of the same condition.  try_wait may suspend the thread
+// for a while when the phase is not complete yet, so a thread that polls
+// several barriers in turn uses test_wait: a barrier that is still open
+// must not delay the check of the next one.
+__device__ __forceinline__ bool bar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // ---- TMA ---------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map,
                                             uint32_t bar, int x, int y) {

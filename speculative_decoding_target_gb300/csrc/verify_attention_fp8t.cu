@@ -1,0 +1,854 @@
+// Split-KV paged GQA verify attention for FP8-E4M3 KV with fp16 scales
+// ("Qwen3.8-27B-FP8" page, "Implemented execution path": E4M3 cache with
+// per-token / per-KV-head FP16 scales over 64-channel blocks), for blocks of
+// at most 64 query rows per KV head, on the tcgen05 tensor cores with both
+// KV operands held in tensor memory.
+//
+// The attention of one (request, KV head) piece is computed transposed:
+//   S^T = K Q^T      M = 128 cached tokens, N = NR query rows, K = channels
+//   O^T += V^T P^T   M = 128 channels (two halves), N = NR rows, K = tokens
+// so the MMA's 128-row dimension is filled with keys or channels and its
+// N dimension is the verify block's own q_len x group rows ("MTP and DFlash2
+// at long context on XPU", Part III: the block's query positions folded into
+// the head dimension, so each KV byte is read once).  The dequantised K tile
+// and the transposed V tile are written by the dequant warps straight into
+// tensor memory as A operands, so the fp16 copies never pass through shared
+// memory: per 128 tokens, shared memory carries the staged FP8 bytes (TMA
+// write + one read), the Q and P operand reads of the MMAs and the P
+// stores, about half the traffic of dequantising into shared-memory
+// operands.  NR = q_len x group rounded up to 16.
+//
+// Tensor memory (512 columns):
+//   [0, 128)    K tile: lane = token, column c = channels 2c (low), 2c + 1
+//   [128, 256)  V^T tile: half h at 128 + 64 h; lane = channel 128 h + lane,
+//               column c = tokens 2c (low), 2c + 1
+//   [256, 384)  O^T: half h at 256 + 64 h; lane = channel, column = row
+//   [384, 512)  two S^T buffers at 384 + 64 b: lane = token, column = row
+//
+// Warp roles (320 threads):
+//   warp 0      producer: per 128-token tile, lane i loads page run i
+//               (min(page_size, 64) tokens): 2-D TMA boxes of 128 bytes x
+//               run with the 128-byte swizzle for each half of the K and V
+//               rows, and 1-D bulk copies of the run's K and V scales, into
+//               a 2-stage staging ring.
+//   warp 1      MMA issuer (one thread): S^T_j (16 MMAs, A = K tile in TMEM,
+//               B = Q from shared memory) and O^T += V^T_j P^T_j (2 x 8 MMAs,
+//               A = V^T tile in TMEM, B = P^T from shared memory), each as
+//               soon as its inputs are ready.
+//   warps 2..5  softmax: one thread per token lane.  Load S^T_j, mask, keep
+//               a running maximum m per row shared by all 128 threads
+//               (raised only when a score passes it by more than 2^8, which
+//               rescales O^T and the partial sums), write P^T_j = 2^(s - m)
+//               (fp16) to shared memory, and accumulate per-thread partial
+//               row sums; the epilogue sums them over the tokens, reads O^T
+//               and writes the bf16 output or an fp32 partial.
+//   warps 6..9  dequant: token lane L converts K row L into TMEM lane L
+//               (fp16(e4m3 * scale)); then channel lane c gathers V[t][c]
+//               for the tile's 128 tokens with a 4 x 4 byte transpose inside
+//               each lane quad (two shuffles and two byte permutes per
+//               word) and writes the V^T tile.
+//
+// Every wait is bounded (about two seconds of clock); a wait that runs out
+// sets SPEC_STATUS_TIMEOUT in the status word (checked mode) and makes every
+// later wait of the CTA return at once, so the kernel always finishes.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "spec_verify.h"
+#include "tc_ptx.cuh"
+#include "tmem_io.cuh"
+
+namespace specv {
+namespace {
+
+constexpr int kTile = 128;                  // tokens per tile
+constexpr int kStages = 2;                  // staging ring depth
+constexpr int kHalf = kTile * 128;          // 128-channel half of K or V
+constexpr int kOffK = 0;                    // K halves, 128-byte swizzle
+constexpr int kOffV = 2 * kHalf;            // V halves
+constexpr int kOffKS = 4 * kHalf;           // K scales [token][4] fp16
+constexpr int kOffVS = kOffKS + kTile * 8;  // V scales [token][4] fp16
+constexpr int kOffVT = kOffVS + kTile * 8;  // V scales [4][token] (dequant)
+constexpr int kStageBytes = kOffVT + 4 * kTile * 2;
+constexpr int kRowsMax = 64;                // NR of the largest instance
+constexpr int kOffQ = kStages * kStageBytes;
+constexpr int kOffP = kOffQ + kRowsMax * 512;
+constexpr int kPBytes = kTile * 128;        // one P^T buffer
+constexpr int kOffRed = kOffP + 2 * kPBytes;
+constexpr uint32_t kColK = 0, kColV = 128;
+constexpr int kSub = 64;                    // tokens per V^T slot
+// Tensor-memory columns of the NR-row instance: V^T slots of 64 tokens
+// (three when NR <= 48, so V of the next tile is converted while PV of the
+// current one runs; two at NR = 64), then O^T and the S^T buffers.
+template <int NR>
+struct Cols {
+  static constexpr int kVSlots = NR <= 48 ? 3 : 2;
+  static constexpr uint32_t kO = kColV + 64 * kVSlots;  // O^T half h: kO + h NR
+  static constexpr uint32_t kS = kO + 2 * NR;           // S^T buffer b: kS + b NR
+  static_assert(kS + 2 * NR <= 512, "tensor memory holds 512 columns");
+};
+constexpr uint32_t kTmemCols = 512;
+constexpr long long kWaitCycles = 4000000000LL;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr int kThreads = 352;
+constexpr int kPieceThreads = 6 * 32;       // warps 1..5 and 10
+static_assert(kStageBytes % 1024 == 0 && kOffQ % 1024 == 0 &&
+                  kOffP % 1024 == 0,
+              "swizzled operands need 1024-byte alignment");
+
+// Softmax exchange area (shared memory).
+struct Red {
+  float colmax[4][kRowsMax];  // per-warp column maxima of raw scores
+  float m[2][kRowsMax];       // running maximum (base 2), two generations
+  float mu[2][kRowsMax];      // the same with -inf replaced by 0
+  float alpha[kRowsMax];      // rescale factor of the last update
+  float lsum_w[4][kRowsMax];  // per-warp row sums
+  float lsum[kRowsMax];
+  int lim[kRowsMax];          // causal limit of each row in this piece
+  long long out_off[kRowsMax];  // output row offset (elements), -1: none
+  int flag[2][4];
+};
+constexpr int kOffPre = kOffRed + (int)((sizeof(Red) + 127) / 128 * 128);
+constexpr int kPreBytes = ((kMaxBatch + 1) * 4 + 127) / 128 * 128;
+constexpr int kSmem = kOffPre + kPreBytes + 1024;  // + alignment slack
+
+struct Bars {
+  uint64_t f8_full[kStages];   // staged bytes landed (TMA / bulk tx)
+  uint64_t f8_empty[kStages];  // dequant warps done with the stage
+  uint64_t k_full;             // K tile written to TMEM
+  uint64_t v_full[3];          // V^T slot written to TMEM
+  uint64_t v_empty[3];         // PV of the slot's 64 tokens complete
+  uint64_t s_full[2];          // S^T_j complete (also: K tile free again)
+  uint64_t p_full[2];          // P^T_j in shared memory (S^T_j consumed)
+  uint64_t pv_done[2];         // O^T += V^T_j P^T_j complete
+  uint64_t drain;
+};
+
+struct Ctx {
+  Bars* bars;
+  volatile int* abort;
+  const AttnParams* p;
+  void* smem;  // 1024-byte aligned dynamic shared memory
+};
+
+struct Piece {
+  int b, g, nt, len, tok_begin, tok_end, n_tiles;
+  long long s0;
+};
+
+__device__ __noinline__ bool wait_slow(uint32_t a, uint32_t parity,
+                                       volatile int* abort, uint32_t* status,
+                                       bool ignore_abort) {
+  if (!ignore_abort && *abort) return false;
+  const long long t0 = clock64();
+  while (true) {
+    if (tc::bar_try_wait(a, parity)) return true;
+    if (!ignore_abort && *abort) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort = 1;
+      if (status) atomicOr(status, SPEC_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool wait_bar(const Ctx& cx, uint64_t* bar,
+                                         uint32_t parity,
+                                         bool ignore_abort = false) {
+  const uint32_t a = tc::smem_u32(bar);
+  if (tc::bar_try_wait(a, parity)) return true;
+  return wait_slow(a, parity, cx.abort, cx.p->status, ignore_abort);
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src,
+                                          uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ---- warp 0: staging of the piece's FP8 tiles ------------------------------
+__device__ __forceinline__ int box_page(const AttnParams& p, const Piece& pc,
+                                        int jt, int lane) {
+  const int t = pc.tok_begin + jt * kTile + lane * p.box_rows;
+  if (jt >= pc.n_tiles || t >= pc.tok_end || lane * p.box_rows >= kTile)
+    return 0;
+  int page = __ldg(p.page_table + (long long)pc.b * p.max_pages +
+                   (t >> p.log2_ps));
+  if (page < 0 || page >= p.num_pages) {
+    if (p.status) atomicOr(p.status, SPEC_STATUS_BAD_PAGE);
+    page = 0;  // in bounds; the affected rows are unspecified
+  }
+  return page;
+}
+
+__device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
+                        const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
+  const AttnParams& p = *cx.p;
+  const int lane = threadIdx.x & 31;
+  const int rpb = p.box_rows;
+  const uint8_t* ksb = reinterpret_cast<const uint8_t*>(p.k_scales);
+  const uint8_t* vsb = reinterpret_cast<const uint8_t*>(p.v_scales);
+  int page = box_page(p, pc, 0, lane);
+  for (int jt = 0; jt < pc.n_tiles; ++jt) {
+    const int next_page = box_page(p, pc, jt + 1, lane);
+    const int gj = gj0 + jt, st = gj % kStages;
+    const int t0 = pc.tok_begin + jt * kTile;
+    const int ntok = min(kTile, pc.tok_end - t0);
+    const int nbox = (ntok + rpb - 1) / rpb;
+    const int t = t0 + lane * rpb;
+    const long long row =
+        ((long long)(page * p.hkv + pc.g) << p.log2_ps) + (t & (p.page_size - 1));
+    if (gj >= kStages)
+      wait_bar(cx, &cx.bars->f8_empty[st], ((gj / kStages) - 1) & 1);
+    const uint32_t full = tc::smem_u32(&cx.bars->f8_full[st]);
+    if (lane == 0)
+      tc::bar_arrive_expect_tx(full, (uint32_t)(nbox * rpb * (4 * 128 + 2 * 8)));
+    __syncwarp();
+    if (lane < nbox) {
+      const uint32_t base = tc::smem_u32(smem + st * kStageBytes);
+      const uint32_t o = lane * rpb;
+      tc::tma_load_2d(base + kOffK + o * 128, tm_k, full, 0, (int)row);
+      tc::tma_load_2d(base + kOffK + kHalf + o * 128, tm_k, full, 128, (int)row);
+      tc::tma_load_2d(base + kOffV + o * 128, tm_v, full, 0, (int)row);
+      tc::tma_load_2d(base + kOffV + kHalf + o * 128, tm_v, full, 128, (int)row);
+      bulk_copy(base + kOffKS + o * 8, ksb + row * 8, rpb * 8, full);
+      bulk_copy(base + kOffVS + o * 8, vsb + row * 8, rpb * 8, full);
+    }
+    page = next_page;
+  }
+}
+
+// ---- warps 6..9: FP8 -> fp16 into the TMEM operand tiles -------------------
+// Four E4M3 bytes -> two f16x2 (bytes 0,1 and bytes 2,3), each multiplied
+// by its scale pair: the hardware E4M3x2 -> f16x2 conversion on each 16-bit
+// half of the word, then one fp16 multiply per pair.
+__device__ __forceinline__ void e4m3x4_scaled(uint32_t w, uint32_t s01,
+                                              uint32_t s23, uint32_t& lo,
+                                              uint32_t& hi) {
+  uint32_t a, b;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}"
+      : "=r"(a), "=r"(b)
+      : "r"(w));
+  const __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&a),
+                            *reinterpret_cast<const __half2*>(&s01));
+  const __half2 y = __hmul2(*reinterpret_cast<const __half2*>(&b),
+                            *reinterpret_cast<const __half2*>(&s23));
+  lo = *reinterpret_cast<const uint32_t*>(&x);
+  hi = *reinterpret_cast<const uint32_t*>(&y);
+}
+
+// Two transposed 16 x 16 byte blocks (x2): matrix m's rows are addressed by
+// lanes 16 m .. 16 m + 15.  Thread 4 g + j receives, per matrix, column g
+// (d0) and column g + 8 (d1), each holding rows 4 j .. 4 j + 3.
+__device__ __forceinline__ void ldsm_x2_trans_b8(uint32_t addr, uint32_t* d) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t dup_half(uint32_t h16) {
+  return (h16 & 0xFFFFu) | (h16 << 16);
+}
+
+template <int NR>
+__device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
+                              uint8_t* smem, uint32_t tmem) {
+  constexpr int VS = Cols<NR>::kVSlots;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q4 = warp & 3;              // TMEM lane quarter of this warp
+  const int L = 32 * q4 + lane;         // token (K) or channel (V^T) lane
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
+  const int jq = lane & 3;  // token quad of the transposed V blocks
+  const int kswz = L & 7;
+
+  for (int jt = 0; jt < pc.n_tiles; ++jt) {
+    const int gj = gj0 + jt, st = gj % kStages;
+    const int t0 = pc.tok_begin + jt * kTile;
+    const int ntok = min(kTile, pc.tok_end - t0);
+    uint8_t* sp = smem + st * kStageBytes;
+    wait_bar(cx, &cx.bars->f8_full[st], (gj / kStages) & 1);
+
+    // V scales of token L, transposed to [block][token] for the V^T pass
+    {
+      const uint2 v4 = *reinterpret_cast<const uint2*>(sp + kOffVS + L * 8);
+      uint16_t* vt = reinterpret_cast<uint16_t*>(sp + kOffVT);
+      vt[0 * kTile + L] = (uint16_t)(v4.x & 0xFFFFu);
+      vt[1 * kTile + L] = (uint16_t)(v4.x >> 16);
+      vt[2 * kTile + L] = (uint16_t)(v4.y & 0xFFFFu);
+      vt[3 * kTile + L] = (uint16_t)(v4.y >> 16);
+    }
+
+    // ---- K: token L -> lane L.  The K tile is free once S^T_{j-1} is done.
+    if (gj > 0) wait_bar(cx, &cx.bars->s_full[(gj - 1) & 1], ((gj - 1) >> 1) & 1);
+    tc::fence_after();
+    if (32 * q4 < ntok) {  // warp-uniform; lanes past the tile are masked
+      const uint2 k4 = *reinterpret_cast<const uint2*>(sp + kOffKS + L * 8);
+      const uint32_t ksc[4] = {dup_half(k4.x), dup_half(k4.x >> 16),
+                               dup_half(k4.y), dup_half(k4.y >> 16)};
+      uint4 raw[16];  // the whole row: every load in flight at once
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc)
+        raw[cc] = *reinterpret_cast<const uint4*>(
+            sp + kOffK + (cc >> 3) * kHalf + L * 128 + (((cc & 7) ^ kswz) << 4));
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        uint32_t o[32];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint4 r4 = raw[blk * 4 + cc];
+          const uint32_t w[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            e4m3x4_scaled(w[e], ksc[blk], ksc[blk], o[cc * 8 + 2 * e],
+                          o[cc * 8 + 2 * e + 1]);
+        }
+        tc::tmem_st_cols<32>(lane_base + kColK + blk * 32, o);
+      }
+    }
+    tc::tmem_wait_st();
+    tc::fence_before();
+    __syncwarp();
+    if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->k_full));
+
+    // ---- V^T, one 64-token slot at a time: 16 x 16 blocks (16 tokens x 16
+    // channels) through the transposing matrix load: thread 4 g + j gets
+    // channel g (and g + 8) of tokens 4 j .. 4 j + 3, which after the
+    // conversion is the register layout of a 16-lane x 256-bit TMEM store
+    // (lane = channel, column = token pair).  Warp q4 covers channels
+    // 32 q4 .. 32 q4 + 31 of each half.  The transposed scales come from
+    // all four warps.
+    tc::bar_sync_named(3, 128);
+#pragma unroll 1
+    for (int sub = 0; sub < 2; ++sub) {
+      const int u = 2 * gj + sub, slot = u % VS;
+      if (u >= VS)  // the slot's previous 64 tokens are through PV
+        wait_bar(cx, &cx.bars->v_empty[slot], ((u / VS) - 1) & 1);
+      tc::fence_after();
+#pragma unroll 1
+      for (int hg = 0; hg < 4; ++hg) {
+        const int h = hg >> 1, gi = hg & 1;  // half, 16-channel group
+        const int cg = 2 * q4 + gi;          // 16-byte chunk of the half row
+        const uint8_t* vb = sp + kOffV + h * kHalf;
+        const uint16_t* vsc = reinterpret_cast<const uint16_t*>(
+            sp + kOffVT + (2 * h + (q4 >> 1)) * (kTile * 2));
+        uint32_t o[16];  // token block tb of the slot: o[4 tb .. 4 tb + 3]
+#pragma unroll
+        for (int tb = 0; tb < 4; tb += 2) {
+          const int T = kSub * sub + 16 * tb + lane;  // lanes 16..31: next block
+          uint32_t d[4];
+          ldsm_x2_trans_b8(tc::smem_u32(vb + T * 128 + ((cg ^ (T & 7)) << 4)), d);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const uint2 sc = *reinterpret_cast<const uint2*>(
+                vsc + kSub * sub + 16 * (tb + m) + 4 * jq);
+            e4m3x4_scaled(d[2 * m], sc.x, sc.y, o[4 * (tb + m)],
+                          o[4 * (tb + m) + 1]);
+            e4m3x4_scaled(d[2 * m + 1], sc.x, sc.y, o[4 * (tb + m) + 2],
+                          o[4 * (tb + m) + 3]);
+          }
+        }
+        if (ntok < kTile) {  // tokens past the piece: zero (0 * NaN poisons PV)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int tk = kSub * sub + 16 * (k >> 2) + 4 * jq + 2 * (k & 1);
+            if (tk >= ntok) o[k] = 0u;
+            else if (tk + 1 >= ntok) o[k] &= 0xFFFFu;
+          }
+        }
+        tc::tmem_st_16x256b_x4(lane_base + ((uint32_t)(16 * gi) << 16) + kColV +
+                                   slot * 64 + h * 32,
+                               o);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->v_full[slot]));
+    }
+    if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->f8_empty[st]));
+  }
+}
+
+// ---- MMA issue: warp 1 issues S^T_j, warp 10 issues O^T += V^T_j P^T_j --------
+// Two issuing threads, each waiting (bounded, without polling) for its own
+// inputs in tile order, so a ready PV never waits behind a QK^T issue and
+// the other way round.  A commit tracks the MMAs of its own thread.
+template <int NR>
+__device__ void qk_piece(const Ctx& cx, const Piece& pc, int gj0,
+                         uint32_t tmem) {
+  // kind::f16 with fp16 A and B, fp32 D, M = 128, N = NR, B K-major
+  constexpr uint32_t kIdQK = (1u << 4) | ((uint32_t)(NR >> 3) << 17) |
+                             ((uint32_t)(128 >> 4) << 24);
+  const uint64_t qdesc = tc::desc_sw128(
+      tc::smem_u32(reinterpret_cast<uint8_t*>(cx.smem) + kOffQ), 16, 1024);
+  for (int jt = 0; jt < pc.n_tiles; ++jt) {
+    const int gj = gj0 + jt;
+    wait_bar(cx, &cx.bars->k_full, gj & 1);
+    // the S^T buffer of tile gj is free once softmax consumed tile gj-2
+    if (gj >= 2) wait_bar(cx, &cx.bars->p_full[gj & 1], ((gj >> 1) - 1) & 1);
+    tc::fence_after();
+    const uint32_t d = tmem + Cols<NR>::kS + (gj & 1) * NR;
+    // descriptors as the base descriptor plus constant address steps
+    // (address field = byte address / 16; every operand lies below 256 KB,
+    // so the field never carries)
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      tc::mma_bf16_ta(d, tmem + kColK + k * 8,
+                      qdesc + (uint64_t)(((k >> 2) * (NR * 128) + (k & 3) * 32) >> 4),
+                      kIdQK, k > 0 ? 1u : 0u);
+    tc::commit(tc::smem_u32(&cx.bars->s_full[gj & 1]));
+  }
+}
+
+template <int NR>
+__device__ void pv_piece(const Ctx& cx, const Piece& pc, int gj0,
+                         uint32_t tmem) {
+  using C = Cols<NR>;
+  // B = P^T is MN-major
+  constexpr uint32_t kIdPV = (1u << 4) | (1u << 16) |
+                             ((uint32_t)(NR >> 3) << 17) |
+                             ((uint32_t)(128 >> 4) << 24);
+  uint8_t* smem = reinterpret_cast<uint8_t*>(cx.smem);
+  const uint64_t pdesc0 = tc::desc_sw128(tc::smem_u32(smem + kOffP), 8192, 1024);
+  const uint64_t pdesc1 =
+      tc::desc_sw128(tc::smem_u32(smem + kOffP + kPBytes), 8192, 1024);
+  for (int jt = 0; jt < pc.n_tiles; ++jt) {
+    const int gj = gj0 + jt;
+    const int t0 = pc.tok_begin + jt * kTile;
+    const int nk = (min(kTile, pc.tok_end - t0) + 15) >> 4;
+    const uint64_t pdesc = (gj & 1) ? pdesc1 : pdesc0;
+    wait_bar(cx, &cx.bars->p_full[gj & 1], (gj >> 1) & 1);
+    // two halves of 64 tokens, each from its V^T slot, so a slot is
+    // released as soon as its tokens are through
+#pragma unroll 1
+    for (int sub = 0; sub < 2; ++sub) {
+      const int u = 2 * gj + sub, slot = u % C::kVSlots;
+      wait_bar(cx, &cx.bars->v_full[slot], (u / C::kVSlots) & 1);
+      tc::fence_after();
+      const uint32_t acc0 = (jt > 0 || sub > 0) ? 1u : 0u;
+      // the two channel halves accumulate into separate O^T tiles: their
+      // MMAs alternate so that two independent chains are in flight
+#pragma unroll
+      for (int k = 0; k < kSub / 16; ++k) {
+        if (4 * sub + k < nk) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tc::mma_bf16_ta(
+                tmem + C::kO + h * NR, tmem + kColV + slot * 64 + h * 32 + k * 8,
+                pdesc + (uint64_t)(((4 * sub + k) * 2048) >> 4), kIdPV,
+                k > 0 ? 1u : acc0);
+        }
+      }
+      tc::commit(tc::smem_u32(&cx.bars->v_empty[slot]));
+    }
+    tc::commit(tc::smem_u32(&cx.bars->pv_done[gj & 1]));
+  }
+}
+
+// ---- warps 2..5: Q, softmax and epilogue -------------------------------------
+// Q of the piece as the QK^T B operand: NR rows x 256 fp16 channels, four
+// 64-channel column blocks of NR x 128 bytes, 128-byte swizzle; rows past
+// the block are zeros.  Also the rows' causal limits and output offsets.
+template <int NR>
+__device__ void load_q(const AttnParams& p, const Piece& pc, uint8_t* smem,
+                       Red* red, int slot, int S) {
+  const int tid = threadIdx.x - 64;  // 0..127
+  const int qb = block_rows(p, pc.b);
+  constexpr int kPer = NR * 32 / 128;  // 16-byte chunks per thread
+  uint4 x[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const int idx = tid + 128 * e, r = idx >> 5, ch = idx & 31;
+    const int i = r / p.group;
+    const bool ok = r < p.rows && i < qb;
+    const int head = pc.g * p.group + (r - i * p.group);
+    x[e] = ok ? __ldg(reinterpret_cast<const uint4*>(
+                    p.q + (((long long)pc.b * p.q_len + i) * p.hq + head) *
+                              kHeadDim + ch * 8))
+              : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const int idx = tid + 128 * e, r = idx >> 5, ch = idx & 31;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&x[e]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // bf16 pairs -> fp16 pairs
+      const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+      const __half2 h2 = __floats2half2_rn(__low2float(b2), __high2float(b2));
+      w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    const int cb = ch >> 3, c16 = ch & 7;
+    *reinterpret_cast<uint4*>(smem + kOffQ + cb * (NR * 128) + r * 128 +
+                              ((c16 ^ (r & 7)) << 4)) = x[e];
+  }
+  if (tid < NR) {
+    const int r = tid, i = r / p.group;
+    const bool ok = r < p.rows && i < qb;
+    red->lim[r] = ok ? causal_limit(pc.len, qb, i) : 0;
+    const int head = pc.g * p.group + (r - i * p.group);
+    red->out_off[r] =
+        r >= p.rows ? -1LL
+                    : (S == 1 ? (((long long)pc.b * p.q_len + i) * p.hq + head) * kHeadDim
+                              : ((long long)slot * p.rows + r) * kHeadDim);
+  }
+  tc::fence_proxy_async_smem();
+}
+
+template <int NR>
+__device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
+                              uint32_t tmem, uint8_t* smem, Red* red, int slot,
+                              int S) {
+  const AttnParams& p = *cx.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q4 = warp & 3;
+  const int L = 32 * q4 + lane;
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
+  const float sl2 = p.scale_log2;
+  const int qb = block_rows(p, pc.b);
+  const int lim0 = causal_limit(pc.len, qb, 0);  // the smallest row limit
+
+  float lp[NR];  // this token's share of each row sum
+#pragma unroll
+  for (int r = 0; r < NR; ++r) lp[r] = 0.f;
+  int mi = 0;
+  for (int jt = 0; jt < pc.n_tiles; ++jt) {
+    const int gj = gj0 + jt;
+    const int t0 = pc.tok_begin + jt * kTile;
+    const int ntok = min(kTile, pc.tok_end - t0);
+    wait_bar(cx, &cx.bars->s_full[gj & 1], (gj >> 1) & 1);
+    tc::fence_after();
+    float s[NR];
+    tc::tmem_ld_cols<NR>(lane_base + Cols<NR>::kS + (gj & 1) * NR,
+                         reinterpret_cast<uint32_t*>(s));
+    if (ntok < kTile || t0 + kTile > lim0) {  // masks reach this tile
+      const bool in = L < ntok;
+      const int t = t0 + L;
+      const int4* lim4 = reinterpret_cast<const int4*>(red->lim);
+#pragma unroll
+      for (int r4 = 0; r4 < NR / 4; ++r4) {
+        const int4 lm = lim4[r4];
+        if (!in || t >= lm.x) s[4 * r4] = -INFINITY;
+        if (!in || t >= lm.y) s[4 * r4 + 1] = -INFINITY;
+        if (!in || t >= lm.z) s[4 * r4 + 2] = -INFINITY;
+        if (!in || t >= lm.w) s[4 * r4 + 3] = -INFINITY;
+      }
+    }
+    // raise m when a score passes it by more than 2^8 (always on the
+    // piece's first tile); the decision is shared by the four warps
+    bool slow = jt == 0;
+    if (!slow) {
+      const float4* mu4 = reinterpret_cast<const float4*>(red->mu[mi]);
+      bool need = false;
+#pragma unroll
+      for (int r4 = 0; r4 < NR / 4; ++r4) {
+        const float4 m = mu4[r4];
+        need |= fmaf(s[4 * r4], sl2, -m.x) > kRescaleLog2;
+        need |= fmaf(s[4 * r4 + 1], sl2, -m.y) > kRescaleLog2;
+        need |= fmaf(s[4 * r4 + 2], sl2, -m.z) > kRescaleLog2;
+        need |= fmaf(s[4 * r4 + 3], sl2, -m.w) > kRescaleLog2;
+      }
+      const bool any = __any_sync(0xffffffffu, need);
+      if (lane == 0) red->flag[gj & 1][q4] = any ? 1 : 0;
+      tc::bar_sync_named(2, 128);
+      slow = (red->flag[gj & 1][0] | red->flag[gj & 1][1] |
+              red->flag[gj & 1][2] | red->flag[gj & 1][3]) != 0;
+    }
+    if (slow) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        float v = s[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) red->colmax[q4][r] = v;
+      }
+      tc::bar_sync_named(2, 128);
+      if (L < NR) {
+        // scale > 0, so the max of the raw scores gives the max of the scaled
+        const float cm = fmaxf(fmaxf(red->colmax[0][L], red->colmax[1][L]),
+                               fmaxf(red->colmax[2][L], red->colmax[3][L])) * sl2;
+        const float mo = red->m[mi][L];
+        float mn = mo, al = 1.f;
+        if (jt == 0) {
+          mn = cm;
+        } else if (mo != -INFINITY && cm > mo + kRescaleLog2) {
+          mn = cm;
+          al = exp2f(mo - mn);
+        }
+        red->m[mi ^ 1][L] = mn;
+        red->mu[mi ^ 1][L] = mn == -INFINITY ? 0.f : mn;
+        red->alpha[L] = al;
+      }
+      tc::bar_sync_named(2, 128);
+      mi ^= 1;
+      if (jt > 0) {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) lp[r] *= red->alpha[r];
+        // O^T must be final for tile gj-1 before it is rescaled
+        wait_bar(cx, &cx.bars->pv_done[(gj - 1) & 1], ((gj - 1) >> 1) & 1);
+        tc::fence_after();
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < NR; c0 += 16) {
+            uint32_t o[16];
+            const uint32_t ta = lane_base + Cols<NR>::kO + h * NR + c0;
+            tc::tmem_ld_cols<16>(ta, o);
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              o[k] = __float_as_uint(__uint_as_float(o[k]) * red->alpha[c0 + k]);
+            tc::tmem_st16(ta, o);
+          }
+        }
+        tc::tmem_wait_st();
+      }
+    }
+    // P^T_j = 2^(s - m): this token's row of the MN-major B operand, eight
+    // rows (one 16-byte chunk) at a time.  The P^T buffer of tile gj is free
+    // once PV of tile gj-2 is done.
+    if (gj >= 2) wait_bar(cx, &cx.bars->pv_done[gj & 1], ((gj >> 1) - 1) & 1);
+    const float4* mu4 = reinterpret_cast<const float4*>(red->mu[mi]);
+    uint8_t* prow = smem + kOffP + (gj & 1) * kPBytes + L * 128;
+#pragma unroll
+    for (int n8 = 0; n8 < NR / 8; ++n8) {
+      const float4 ma = mu4[2 * n8], mb = mu4[2 * n8 + 1];
+      const float m8[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = 8 * n8 + 2 * e;
+        const float x0 = exp2f(fmaf(s[r], sl2, -m8[2 * e]));
+        const float x1 = exp2f(fmaf(s[r + 1], sl2, -m8[2 * e + 1]));
+        lp[r] += x0;
+        lp[r + 1] += x1;
+        const __half2 hh = __floats2half2_rn(x0, x1);
+        pk[e] = *reinterpret_cast<const uint32_t*>(&hh);
+      }
+      *reinterpret_cast<uint4*>(prow + ((n8 ^ (L & 7)) << 4)) =
+          make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before();
+    __syncwarp();
+    if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->p_full[gj & 1]));
+  }
+
+  // epilogue: row sums over the tokens, then O = O^T / l
+  const int gl = gj0 + pc.n_tiles - 1;
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float v = lp[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red->lsum_w[q4][r] = v;
+  }
+  tc::bar_sync_named(2, 128);
+  if (L < NR)
+    red->lsum[L] = (red->lsum_w[0][L] + red->lsum_w[1][L]) +
+                   (red->lsum_w[2][L] + red->lsum_w[3][L]);
+  tc::bar_sync_named(2, 128);
+  wait_bar(cx, &cx.bars->pv_done[gl & 1], (gl >> 1) & 1);
+  tc::fence_after();
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {  // channel L + 128 h of every row
+#pragma unroll 1
+    for (int c0 = 0; c0 < NR; c0 += 16) {
+      uint32_t o[16];
+      tc::tmem_ld_cols<16>(lane_base + Cols<NR>::kO + h * NR + c0, o);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int r = c0 + k;
+        const long long off = red->out_off[r];
+        if (off < 0) continue;
+        const float l = red->lsum[r];
+        const float inv = (red->lim[r] > 0 && l > 0.f) ? 1.f / l : 0.f;
+        const float v = __uint_as_float(o[k]) * inv;
+        if (S == 1)
+          p.out[off + 128 * h + L] = __float2bfloat16_rn(v);
+        else
+          p.part_o[off + 128 * h + L] = v;
+      }
+    }
+  }
+  if (S > 1 && L < p.rows) {
+    const float l = red->lsum[L];
+    p.part_lse[(long long)slot * p.rows + L] =
+        (red->lim[L] > 0 && l > 0.f) ? red->mu[mi][L] + log2f(l) : -INFINITY;
+  }
+}
+
+template <int NR>
+__global__ void __launch_bounds__(kThreads, 1)
+    verify_split_fp8t_kernel(const AttnParams p,
+                             const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  int* s_pre = reinterpret_cast<int*>(smem + kOffPre);
+  Red* red = reinterpret_cast<Red*>(smem + kOffRed);
+  __shared__ __align__(8) Bars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the merge kernel may be scheduled now; it waits for this grid to finish
+  tc_grid_launch_dependents();
+  plan_prefix(p, s_pre);
+  const long long U = (long long)p.hkv * s_pre[p.batch];
+  const int P = effective_grid(p.grid, U);
+  const int c = blockIdx.x;
+  if (c >= P) return;  // uniform over the CTA, before any TMEM or barrier use
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::bar_init(tc::smem_u32(&bars.f8_full[s]), 1);
+      tc::bar_init(tc::smem_u32(&bars.f8_empty[s]), 4);
+    }
+    tc::bar_init(tc::smem_u32(&bars.k_full), 4);
+    for (int s = 0; s < 3; ++s) {
+      tc::bar_init(tc::smem_u32(&bars.v_full[s]), 4);
+      tc::bar_init(tc::smem_u32(&bars.v_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::bar_init(tc::smem_u32(&bars.s_full[s]), 1);
+      tc::bar_init(tc::smem_u32(&bars.p_full[s]), 4);
+      tc::bar_init(tc::smem_u32(&bars.pv_done[s]), 1);
+    }
+    tc::bar_init(tc::smem_u32(&bars.drain), 2);
+    s_abort = 0;
+    tc::bar_fence_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&s_tmem), kTmemCols);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = s_tmem;
+  Ctx cx{&bars, &s_abort, &p, smem};
+
+  long long u = cta_start(c, U, P);
+  const long long u_end = cta_start(c + 1, U, P);
+  int gj0 = 0;
+  int last_loaded = -1;  // last tile index the producer loaded
+  while (u < u_end) {
+    Piece pc;
+    pc.b = find_request(s_pre, p.batch, p.hkv, u);
+    const int ntv = s_pre[pc.b + 1] - s_pre[pc.b];  // virtual units
+    const long long rb = (long long)p.hkv * s_pre[pc.b];
+    pc.g = (int)((u - rb) / ntv);
+    const long long vs = rb + (long long)pc.g * ntv;
+    const int j0v = (int)(u - vs);
+    const int j1v = (int)(u_end - vs < ntv ? u_end - vs : ntv);
+    u = vs + j1v;
+    // real units of the piece; a range of phantom units only does nothing
+    const int j0 = max(j0v - kPieceCost, 0), j1 = max(j1v - kPieceCost, 0);
+    if (j1 <= j0) continue;  // the same decision in every warp
+    pc.nt = ntv - kPieceCost;
+    pc.s0 = vs + kPieceCost;  // the segment's first real unit
+    pc.len = clamp_len(p.seq_lens[pc.b], p.max_tokens);
+    pc.tok_begin = j0 * kUnit;
+    pc.tok_end = min(j1 * kUnit, pc.len);
+    pc.n_tiles = (pc.tok_end - pc.tok_begin + kTile - 1) / kTile;
+
+    // The producer and the dequant warps run ahead across pieces, gated by
+    // the ring and operand barriers; the MMA issuer and the softmax warps
+    // meet around each piece, so Q is rewritten only after the previous
+    // piece's last MMA and O^T is read before the next piece's first PV.
+    if (warp == 0) {
+      produce(cx, pc, gj0, smem, &tm_k, &tm_v);
+      last_loaded = gj0 + pc.n_tiles - 1;
+      __syncwarp();
+    } else if (warp >= 6 && warp < 10) {
+      dequant_piece<NR>(cx, pc, gj0, smem, tmem);
+    } else {
+      int S = 0, slot = 0;
+      if (warp >= 2 && warp < 6) {
+        // where this piece's result goes
+        S = seg_splits(pc.s0, pc.nt, U, P);
+        slot = S > 1 ? slot_base_warp(p, s_pre, pc.b * p.hkv + pc.g, U, P) +
+                           (c - cta_of(pc.s0, U, P))
+                     : 0;
+        load_q<NR>(p, pc, smem, red, slot, S);
+      }
+      tc::fence_before();
+      tc::bar_sync_named(1, kPieceThreads);
+      tc::fence_after();
+      if (warp == 1 || warp == 10) {
+        if (lane == 0) {
+          if (warp == 1) qk_piece<NR>(cx, pc, gj0, tmem);
+          else pv_piece<NR>(cx, pc, gj0, tmem);
+        }
+        __syncwarp();
+      } else {
+        softmax_piece<NR>(cx, pc, gj0, tmem, smem, red, slot, S);
+      }
+      tc::fence_before();
+      tc::bar_sync_named(1, kPieceThreads);
+      tc::fence_after();
+    }
+    gj0 += pc.n_tiles;
+  }
+
+  // teardown: no copy or MMA may still be in flight
+  if (warp == 0 && lane == 0) {
+    for (int gj = max(0, last_loaded - kStages + 1); gj <= last_loaded; ++gj)
+      wait_bar(cx, &bars.f8_full[gj % kStages], (gj / kStages) & 1, true);
+  }
+  if ((warp == 1 || warp == 10) && lane == 0) {  // both MMA issuers
+    tc::commit(tc::smem_u32(&bars.drain));
+    wait_bar(cx, &bars.drain, 0, true);
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int NR>
+cudaError_t launch(const AttnParams& p, const CUtensorMap& tm_k,
+                   const CUtensorMap& tm_v, cudaStream_t s) {
+  // the shared-memory attribute was set by verify_split_fp8t_ctas_per_sm(),
+  // which sizing the grid always runs first
+  verify_split_fp8t_kernel<NR><<<p.grid, kThreads, kSmem, s>>>(p, tm_k, tm_v);
+  return cudaGetLastError();
+}
+
+template <int NR>
+bool set_smem() {
+  return cudaFuncSetAttribute(verify_split_fp8t_kernel<NR>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmem) == cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_verify_split_fp8t(const AttnParams& p,
+                                     const CUtensorMap& tm_k,
+                                     const CUtensorMap& tm_v, cudaStream_t s) {
+  const int nr = (p.rows + 15) / 16 * 16;
+  switch (nr) {
+    case 16: return launch<16>(p, tm_k, tm_v, s);
+    case 32: return launch<32>(p, tm_k, tm_v, s);
+    case 48: return launch<48>(p, tm_k, tm_v, s);
+    case 64: return launch<64>(p, tm_k, tm_v, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int verify_split_fp8t_ctas_per_sm() {
+  if (!set_smem<16>() || !set_smem<32>() || !set_smem<48>() || !set_smem<64>())
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &n, verify_split_fp8t_kernel<48>, kThreads, kSmem) != cudaSuccess)
+    return 0;
+  return n < 1 ? 0 : 1;  // TMEM: one 512-column allocation per SM
+}
+
+}  // namespace specv

@@ -364,9 +364,9 @@ __device__ void mma_piece(const Ctx& cx, const Piece& pc, int gj0, uint32_t tmem
     if (qk < pc.n_tiles) {
       const int gj = gj0 + qk;
       // the S/P buffer of tile gj is free once PV of tile gj-2 is done
-      if (tc::bar_try_wait(tc::smem_u32(&cx.bars->kv_full[gj % C::kStages]),
+      if (tc::bar_test_wait(tc::smem_u32(&cx.bars->kv_full[gj % C::kStages]),
                            (gj / C::kStages) & 1) &&
-          (gj < 2 || tc::bar_try_wait(tc::smem_u32(&cx.bars->pv_done[gj & 1]),
+          (gj < 2 || tc::bar_test_wait(tc::smem_u32(&cx.bars->pv_done[gj & 1]),
                                       ((gj >> 1) - 1) & 1))) {
         tc::fence_after();
         issue_qk<kFp8>(cx, gj, tmem, smem);
@@ -376,9 +376,9 @@ __device__ void mma_piece(const Ctx& cx, const Piece& pc, int gj0, uint32_t tmem
     }
     if (pv < qk) {
       const int gj = gj0 + pv;
-      if (tc::bar_try_wait(tc::smem_u32(&cx.bars->p_full[gj & 1]),
+      if (tc::bar_test_wait(tc::smem_u32(&cx.bars->p_full[gj & 1]),
                            (gj >> 1) & 1) &&
-          (!kFp8 || tc::bar_try_wait(tc::smem_u32(&cx.bars->v_full[gj % C::kStages]),
+          (!kFp8 || tc::bar_test_wait(tc::smem_u32(&cx.bars->v_full[gj % C::kStages]),
                                      (gj / C::kStages) & 1))) {
         tc::fence_after();
         issue_pv<kFp8>(cx, gj, pv == 0, tmem, smem);
