@@ -18,35 +18,45 @@
 // stores, about half the traffic of dequantising into shared-memory
 // operands.  NR = q_len x group rounded up to 16.
 //
-// Tensor memory (512 columns):
+// Tensor memory (512 columns; NR = rows rounded up to 16, at most 64):
 //   [0, 128)    K tile: lane = token, column c = channels 2c (low), 2c + 1
-//   [128, 256)  V^T tile: half h at 128 + 64 h; lane = channel 128 h + lane,
+//   [128, ...)  V^T slots of 64 tokens (three when NR <= 48, else two), 64
+//               columns each: half h at + 32 h; lane = channel 128 h + lane,
 //               column c = tokens 2c (low), 2c + 1
-//   [256, 384)  O^T: half h at 256 + 64 h; lane = channel, column = row
-//   [384, 512)  two S^T buffers at 384 + 64 b: lane = token, column = row
+//   then O^T (half h at + h NR; lane = channel, column = row) and two S^T
+//   buffers of NR columns (lane = token, column = row).
 //
-// Warp roles (320 threads):
-//   warp 0      producer: per 128-token tile, lane i loads page run i
-//               (min(page_size, 64) tokens): 2-D TMA boxes of 128 bytes x
-//               run with the 128-byte swizzle for each half of the K and V
-//               rows, and 1-D bulk copies of the run's K and V scales, into
-//               a 2-stage staging ring.
-//   warp 1      MMA issuer (one thread): S^T_j (16 MMAs, A = K tile in TMEM,
-//               B = Q from shared memory) and O^T += V^T_j P^T_j (2 x 8 MMAs,
-//               A = V^T tile in TMEM, B = P^T from shared memory), each as
-//               soon as its inputs are ready.
-//   warps 2..5  softmax: one thread per token lane.  Load S^T_j, mask, keep
-//               a running maximum m per row shared by all 128 threads
-//               (raised only when a score passes it by more than 2^8, which
-//               rescales O^T and the partial sums), write P^T_j = 2^(s - m)
-//               (fp16) to shared memory, and accumulate per-thread partial
-//               row sums; the epilogue sums them over the tokens, reads O^T
-//               and writes the bf16 output or an fp32 partial.
-//   warps 6..9  dequant: token lane L converts K row L into TMEM lane L
-//               (fp16(e4m3 * scale)); then channel lane c gathers V[t][c]
-//               for the tile's 128 tokens with a 4 x 4 byte transpose inside
-//               each lane quad (two shuffles and two byte permutes per
-//               word) and writes the V^T tile.
+// Shared memory: a 2-slot ring of staged K bytes (+ scales) and a 3-slot
+// ring of staged V bytes (+ scales): K is converted first and its slot
+// released early, V is held until its conversion ends.  Then Q (the QK^T B
+// operand) and the P^T buffer (the PV B operand).
+//
+// Warp roles (512 threads; 128 registers each):
+//   warps 0..3    softmax: one thread per token lane.  Load S^T_j in
+//                 16-column chunks, mask, keep a running maximum m per row
+//                 shared by all 128 threads (raised only when a score passes
+//                 it by more than 2^8, which rescales O^T and the partial
+//                 sums), write P^T_j = 2^(s - m) (fp16) to shared memory and
+//                 accumulate per-thread partial row sums; the epilogue sums
+//                 them over the tokens, reads O^T and writes the bf16 output
+//                 or an fp32 partial.
+//   warps 4..11   dequant, two sets of four warps taking alternate tiles:
+//                 token lane L converts K row L into TMEM lane L
+//                 (fp16(e4m3 * scale)); then, per 64-token V^T slot, a
+//                 transposing 16 x 16 byte-matrix load hands thread 4 g + j
+//                 channel g (and g + 8) of four consecutive tokens, which
+//                 after the conversion is the register layout of a 16-lane x
+//                 256-bit TMEM store (lane = channel, column = token pair).
+//   warp 12       producer: per 128-token tile, lane i loads page run i
+//                 (min(page_size, 64) tokens): 2-D TMA boxes of 128 bytes x
+//                 run with the 128-byte swizzle for each half of the K and V
+//                 rows, and 1-D bulk copies of the run's scales.
+//   warp 13       QK^T issuer (one thread): S^T_j, 16 MMAs, A = K tile in
+//                 TMEM, B = Q from shared memory.
+//   warp 14       PV issuer (one thread): O^T += V^T_j P^T_j per 64-token
+//                 slot, 2 x 4 MMAs, A = V^T slot in TMEM, B = P^T.
+//   The two issuers wait (bounded) for their own inputs in tile order, so a
+//   ready PV never waits behind a QK^T issue.
 //
 // Every wait is bounded (about two seconds of clock); a wait that runs out
 // sets SPEC_STATUS_TIMEOUT in the status word (checked mode) and makes every
@@ -62,19 +72,24 @@ namespace specv {
 namespace {
 
 constexpr int kTile = 128;                  // tokens per tile
-constexpr int kStages = 2;                  // staging ring depth
+// Staging: separate rings for the K and the V bytes of a tile.  K is
+// converted first and released early, V is held until its conversion
+// ends, so V gets the deeper ring.
 constexpr int kHalf = kTile * 128;          // 128-channel half of K or V
-constexpr int kOffK = 0;                    // K halves, 128-byte swizzle
-constexpr int kOffV = 2 * kHalf;            // V halves
-constexpr int kOffKS = 4 * kHalf;           // K scales [token][4] fp16
-constexpr int kOffVS = kOffKS + kTile * 8;  // V scales [token][4] fp16
-constexpr int kOffVT = kOffVS + kTile * 8;  // V scales [4][token] (dequant)
-constexpr int kStageBytes = kOffVT + 4 * kTile * 2;
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;
+constexpr int kSBytes = 2 * kHalf;          // K or V bytes, two halves
+constexpr int kKSlot = kSBytes + kTile * 8;             // + K scales
+constexpr int kVSlot = kSBytes + kTile * 8 + kTile * 8;  // + V scales, transposed
+constexpr int kOffKS = kSBytes;             // scales [token][4] fp16 in a slot
+constexpr int kOffVT = kSBytes + kTile * 8; // V scales [4][token] (dequant)
+constexpr int kOffKR = 0;                   // K ring
+constexpr int kOffVR = kKStages * kKSlot;   // V ring
 constexpr int kRowsMax = 64;                // NR of the largest instance
-constexpr int kOffQ = kStages * kStageBytes;
+constexpr int kOffQ = kOffVR + kVStages * kVSlot;
 constexpr int kOffP = kOffQ + kRowsMax * 512;
-constexpr int kPBytes = kTile * 128;        // one P^T buffer
-constexpr int kOffRed = kOffP + 2 * kPBytes;
+constexpr int kPBytes = kTile * 128;        // the P^T buffer
+constexpr int kOffRed = kOffP + kPBytes;
 constexpr uint32_t kColK = 0, kColV = 128;
 constexpr int kSub = 64;                    // tokens per V^T slot
 // Tensor-memory columns of the NR-row instance: V^T slots of 64 tokens
@@ -90,9 +105,10 @@ struct Cols {
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kThreads = 352;
-constexpr int kPieceThreads = 6 * 32;       // warps 1..5 and 10
-static_assert(kStageBytes % 1024 == 0 && kOffQ % 1024 == 0 &&
+constexpr int kThreads = 512;
+constexpr int kPieceThreads = 6 * 32;       // warps 0..3, 13 and 14
+constexpr int kWarpProducer = 12, kWarpQK = 13, kWarpPV = 14;
+static_assert(kKSlot % 1024 == 0 && kVSlot % 1024 == 0 && kOffQ % 1024 == 0 &&
                   kOffP % 1024 == 0,
               "swizzled operands need 1024-byte alignment");
 
@@ -113,8 +129,10 @@ constexpr int kPreBytes = ((kMaxBatch + 1) * 4 + 127) / 128 * 128;
 constexpr int kSmem = kOffPre + kPreBytes + 1024;  // + alignment slack
 
 struct Bars {
-  uint64_t f8_full[kStages];   // staged bytes landed (TMA / bulk tx)
-  uint64_t f8_empty[kStages];  // dequant warps done with the stage
+  uint64_t k8_full[kKStages];  // staged K bytes landed (TMA / bulk tx)
+  uint64_t k8_empty[kKStages]; // dequant warps done with the K slot
+  uint64_t v8_full[kVStages];  // staged V bytes landed
+  uint64_t v8_empty[kVStages]; // dequant warps done with the V slot
   uint64_t k_full;             // K tile written to TMEM
   uint64_t v_full[3];          // V^T slot written to TMEM
   uint64_t v_empty[3];         // PV of the slot's 64 tokens complete
@@ -198,28 +216,32 @@ __device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
   int page = box_page(p, pc, 0, lane);
   for (int jt = 0; jt < pc.n_tiles; ++jt) {
     const int next_page = box_page(p, pc, jt + 1, lane);
-    const int gj = gj0 + jt, st = gj % kStages;
+    const int gj = gj0 + jt;
     const int t0 = pc.tok_begin + jt * kTile;
     const int ntok = min(kTile, pc.tok_end - t0);
     const int nbox = (ntok + rpb - 1) / rpb;
     const int t = t0 + lane * rpb;
     const long long row =
         ((long long)(page * p.hkv + pc.g) << p.log2_ps) + (t & (p.page_size - 1));
-    if (gj >= kStages)
-      wait_bar(cx, &cx.bars->f8_empty[st], ((gj / kStages) - 1) & 1);
-    const uint32_t full = tc::smem_u32(&cx.bars->f8_full[st]);
-    if (lane == 0)
-      tc::bar_arrive_expect_tx(full, (uint32_t)(nbox * rpb * (4 * 128 + 2 * 8)));
-    __syncwarp();
-    if (lane < nbox) {
-      const uint32_t base = tc::smem_u32(smem + st * kStageBytes);
-      const uint32_t o = lane * rpb;
-      tc::tma_load_2d(base + kOffK + o * 128, tm_k, full, 0, (int)row);
-      tc::tma_load_2d(base + kOffK + kHalf + o * 128, tm_k, full, 128, (int)row);
-      tc::tma_load_2d(base + kOffV + o * 128, tm_v, full, 0, (int)row);
-      tc::tma_load_2d(base + kOffV + kHalf + o * 128, tm_v, full, 128, (int)row);
-      bulk_copy(base + kOffKS + o * 8, ksb + row * 8, rpb * 8, full);
-      bulk_copy(base + kOffVS + o * 8, vsb + row * 8, rpb * 8, full);
+    const uint32_t bytes = (uint32_t)(nbox * rpb * (2 * 128 + 8));
+    const uint32_t o = lane * rpb;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {  // the K bytes, then the V bytes
+      const int S = kv ? kVStages : kKStages, st = gj % S;
+      uint64_t* empty = kv ? cx.bars->v8_empty : cx.bars->k8_empty;
+      uint64_t* fullb = kv ? cx.bars->v8_full : cx.bars->k8_full;
+      if (gj >= S) wait_bar(cx, &empty[st], ((gj / S) - 1) & 1);
+      const uint32_t full = tc::smem_u32(&fullb[st]);
+      if (lane == 0) tc::bar_arrive_expect_tx(full, bytes);
+      __syncwarp();
+      if (lane < nbox) {
+        const uint32_t base = tc::smem_u32(smem + (kv ? kOffVR + st * kVSlot
+                                                      : kOffKR + st * kKSlot));
+        const CUtensorMap* tm = kv ? tm_v : tm_k;
+        tc::tma_load_2d(base + o * 128, tm, full, 0, (int)row);
+        tc::tma_load_2d(base + kHalf + o * 128, tm, full, 128, (int)row);
+        bulk_copy(base + kOffKS + o * 8, (kv ? vsb : ksb) + row * 8, rpb * 8, full);
+      }
     }
     page = next_page;
   }
@@ -255,13 +277,45 @@ __device__ __forceinline__ void ldsm_x2_trans_b8(uint32_t addr, uint32_t* d) {
       : "r"(addr));
 }
 
+// Loads of one V^T conversion step `it` (slot half it / 4, channel half
+// (it / 2) % 2, 16-channel group it % 2) for lane quarter q4: the four
+// transposed 16 x 16 blocks of the slot half's 64 tokens (d[2 tb], d[2 tb+1]
+// = channel g and g + 8 of tokens 16 tb + 4 j .. + 3) and their scale pairs
+// (s[2 tb], s[2 tb + 1] = tokens 16 tb + 4 j + {0, 1} and + {2, 3}).
+__device__ __forceinline__ void load_v_step(const uint8_t* vp, int it, int q4,
+                                            int lane, int jq, uint32_t* d,
+                                            uint32_t* s) {
+  const int sub = it >> 2, h = (it >> 1) & 1, gi = it & 1;
+  const int cg = 2 * q4 + gi;  // 16-byte chunk of the half row
+  const uint8_t* vb = vp + h * kHalf;
+  const uint16_t* vsc = reinterpret_cast<const uint16_t*>(
+      vp + kOffVT + (2 * h + (q4 >> 1)) * (kTile * 2));
+#pragma unroll
+  for (int tb = 0; tb < 4; tb += 2) {
+    const int T = kSub * sub + 16 * tb + lane;  // lanes 16..31: the next block
+    uint32_t x[4];
+    ldsm_x2_trans_b8(tc::smem_u32(vb + T * 128 + ((cg ^ (T & 7)) << 4)), x);
+    d[2 * tb] = x[0];
+    d[2 * tb + 1] = x[1];
+    d[2 * tb + 2] = x[2];
+    d[2 * tb + 3] = x[3];
+  }
+#pragma unroll
+  for (int tb = 0; tb < 4; ++tb) {
+    const uint2 p = *reinterpret_cast<const uint2*>(vsc + kSub * sub + 16 * tb +
+                                                    4 * jq);
+    s[2 * tb] = p.x;
+    s[2 * tb + 1] = p.y;
+  }
+}
+
 __device__ __forceinline__ uint32_t dup_half(uint32_t h16) {
   return (h16 & 0xFFFFu) | (h16 << 16);
 }
 
 template <int NR>
 __device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
-                              uint8_t* smem, uint32_t tmem) {
+                              uint8_t* smem, uint32_t tmem, int set) {
   constexpr int VS = Cols<NR>::kVSlots;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q4 = warp & 3;              // TMEM lane quarter of this warp
@@ -270,35 +324,28 @@ __device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
   const int jq = lane & 3;  // token quad of the transposed V blocks
   const int kswz = L & 7;
 
-  for (int jt = 0; jt < pc.n_tiles; ++jt) {
-    const int gj = gj0 + jt, st = gj % kStages;
+  // the two warp sets take alternate tiles (by global tile index)
+  for (int jt = (set - gj0) & 1; jt < pc.n_tiles; jt += 2) {
+    const int gj = gj0 + jt;
     const int t0 = pc.tok_begin + jt * kTile;
     const int ntok = min(kTile, pc.tok_end - t0);
-    uint8_t* sp = smem + st * kStageBytes;
-    wait_bar(cx, &cx.bars->f8_full[st], (gj / kStages) & 1);
-
-    // V scales of token L, transposed to [block][token] for the V^T pass
-    {
-      const uint2 v4 = *reinterpret_cast<const uint2*>(sp + kOffVS + L * 8);
-      uint16_t* vt = reinterpret_cast<uint16_t*>(sp + kOffVT);
-      vt[0 * kTile + L] = (uint16_t)(v4.x & 0xFFFFu);
-      vt[1 * kTile + L] = (uint16_t)(v4.x >> 16);
-      vt[2 * kTile + L] = (uint16_t)(v4.y & 0xFFFFu);
-      vt[3 * kTile + L] = (uint16_t)(v4.y >> 16);
-    }
+    const int sk = gj % kKStages, sv = gj % kVStages;
+    uint8_t* kp = smem + kOffKR + sk * kKSlot;
+    uint8_t* vp = smem + kOffVR + sv * kVSlot;
+    wait_bar(cx, &cx.bars->k8_full[sk], (gj / kKStages) & 1);
 
     // ---- K: token L -> lane L.  The K tile is free once S^T_{j-1} is done.
     if (gj > 0) wait_bar(cx, &cx.bars->s_full[(gj - 1) & 1], ((gj - 1) >> 1) & 1);
     tc::fence_after();
     if (32 * q4 < ntok) {  // warp-uniform; lanes past the tile are masked
-      const uint2 k4 = *reinterpret_cast<const uint2*>(sp + kOffKS + L * 8);
+      const uint2 k4 = *reinterpret_cast<const uint2*>(kp + kOffKS + L * 8);
       const uint32_t ksc[4] = {dup_half(k4.x), dup_half(k4.x >> 16),
                                dup_half(k4.y), dup_half(k4.y >> 16)};
       uint4 raw[16];  // the whole row: every load in flight at once
 #pragma unroll
       for (int cc = 0; cc < 16; ++cc)
         raw[cc] = *reinterpret_cast<const uint4*>(
-            sp + kOffK + (cc >> 3) * kHalf + L * 128 + (((cc & 7) ^ kswz) << 4));
+            kp + (cc >> 3) * kHalf + L * 128 + (((cc & 7) ^ kswz) << 4));
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {
         uint32_t o[32];
@@ -317,7 +364,21 @@ __device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
     tc::tmem_wait_st();
     tc::fence_before();
     __syncwarp();
-    if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->k_full));
+    if (lane == 0) {
+      tc::bar_arrive(tc::smem_u32(&cx.bars->k_full));
+      tc::bar_arrive(tc::smem_u32(&cx.bars->k8_empty[sk]));
+    }
+
+    // V scales of token L, transposed to [block][token] for the V^T pass
+    wait_bar(cx, &cx.bars->v8_full[sv], (gj / kVStages) & 1);
+    {
+      const uint2 v4 = *reinterpret_cast<const uint2*>(vp + kOffKS + L * 8);
+      uint16_t* vt = reinterpret_cast<uint16_t*>(vp + kOffVT);
+      vt[0 * kTile + L] = (uint16_t)(v4.x & 0xFFFFu);
+      vt[1 * kTile + L] = (uint16_t)(v4.x >> 16);
+      vt[2 * kTile + L] = (uint16_t)(v4.y & 0xFFFFu);
+      vt[3 * kTile + L] = (uint16_t)(v4.y >> 16);
+    }
 
     // ---- V^T, one 64-token slot at a time: 16 x 16 blocks (16 tokens x 16
     // channels) through the transposing matrix load: thread 4 g + j gets
@@ -326,7 +387,7 @@ __device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
     // (lane = channel, column = token pair).  Warp q4 covers channels
     // 32 q4 .. 32 q4 + 31 of each half.  The transposed scales come from
     // all four warps.
-    tc::bar_sync_named(3, 128);
+    tc::bar_sync_named(3 + set, 128);
 #pragma unroll 1
     for (int sub = 0; sub < 2; ++sub) {
       const int u = 2 * gj + sub, slot = u % VS;
@@ -336,25 +397,15 @@ __device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
 #pragma unroll 1
       for (int hg = 0; hg < 4; ++hg) {
         const int h = hg >> 1, gi = hg & 1;  // half, 16-channel group
-        const int cg = 2 * q4 + gi;          // 16-byte chunk of the half row
-        const uint8_t* vb = sp + kOffV + h * kHalf;
-        const uint16_t* vsc = reinterpret_cast<const uint16_t*>(
-            sp + kOffVT + (2 * h + (q4 >> 1)) * (kTile * 2));
+        uint32_t d[8], sc[8];
+        load_v_step(vp, 4 * sub + hg, q4, lane, jq, d, sc);
         uint32_t o[16];  // token block tb of the slot: o[4 tb .. 4 tb + 3]
 #pragma unroll
-        for (int tb = 0; tb < 4; tb += 2) {
-          const int T = kSub * sub + 16 * tb + lane;  // lanes 16..31: next block
-          uint32_t d[4];
-          ldsm_x2_trans_b8(tc::smem_u32(vb + T * 128 + ((cg ^ (T & 7)) << 4)), d);
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            const uint2 sc = *reinterpret_cast<const uint2*>(
-                vsc + kSub * sub + 16 * (tb + m) + 4 * jq);
-            e4m3x4_scaled(d[2 * m], sc.x, sc.y, o[4 * (tb + m)],
-                          o[4 * (tb + m) + 1]);
-            e4m3x4_scaled(d[2 * m + 1], sc.x, sc.y, o[4 * (tb + m) + 2],
-                          o[4 * (tb + m) + 3]);
-          }
+        for (int tb = 0; tb < 4; ++tb) {
+          e4m3x4_scaled(d[2 * tb], sc[2 * tb], sc[2 * tb + 1], o[4 * tb],
+                        o[4 * tb + 1]);
+          e4m3x4_scaled(d[2 * tb + 1], sc[2 * tb], sc[2 * tb + 1],
+                        o[4 * tb + 2], o[4 * tb + 3]);
         }
         if (ntok < kTile) {  // tokens past the piece: zero (0 * NaN poisons PV)
 #pragma unroll
@@ -373,7 +424,7 @@ __device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
       __syncwarp();
       if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->v_full[slot]));
     }
-    if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->f8_empty[st]));
+    if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->v8_empty[sv]));
   }
 }
 
@@ -417,14 +468,11 @@ __device__ void pv_piece(const Ctx& cx, const Piece& pc, int gj0,
                              ((uint32_t)(NR >> 3) << 17) |
                              ((uint32_t)(128 >> 4) << 24);
   uint8_t* smem = reinterpret_cast<uint8_t*>(cx.smem);
-  const uint64_t pdesc0 = tc::desc_sw128(tc::smem_u32(smem + kOffP), 8192, 1024);
-  const uint64_t pdesc1 =
-      tc::desc_sw128(tc::smem_u32(smem + kOffP + kPBytes), 8192, 1024);
+  const uint64_t pdesc = tc::desc_sw128(tc::smem_u32(smem + kOffP), 8192, 1024);
   for (int jt = 0; jt < pc.n_tiles; ++jt) {
     const int gj = gj0 + jt;
     const int t0 = pc.tok_begin + jt * kTile;
     const int nk = (min(kTile, pc.tok_end - t0) + 15) >> 4;
-    const uint64_t pdesc = (gj & 1) ? pdesc1 : pdesc0;
     wait_bar(cx, &cx.bars->p_full[gj & 1], (gj >> 1) & 1);
     // two halves of 64 tokens, each from its V^T slot, so a slot is
     // released as soon as its tokens are through
@@ -460,7 +508,7 @@ __device__ void pv_piece(const Ctx& cx, const Piece& pc, int gj0,
 template <int NR>
 __device__ void load_q(const AttnParams& p, const Piece& pc, uint8_t* smem,
                        Red* red, int slot, int S) {
-  const int tid = threadIdx.x - 64;  // 0..127
+  const int tid = threadIdx.x;  // softmax warps 0..3
   const int qb = block_rows(p, pc.b);
   constexpr int kPer = NR * 32 / 128;  // 16-byte chunks per thread
   uint4 x[kPer];
@@ -502,6 +550,25 @@ __device__ void load_q(const AttnParams& p, const Piece& pc, uint8_t* smem,
   tc::fence_proxy_async_smem();
 }
 
+// 16 score columns of S^T_j for this token, masked: a token past the tile
+// or past row r's causal limit scores -inf.
+__device__ __forceinline__ void load_scores16(uint32_t taddr, int c0,
+                                              bool masked, bool in, int t,
+                                              const Red* red, float* v) {
+  tc::tmem_ld_cols<16>(taddr, reinterpret_cast<uint32_t*>(v));
+  if (masked) {
+    const int4* lim4 = reinterpret_cast<const int4*>(red->lim + c0);
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const int4 lm = lim4[k4];
+      if (!in || t >= lm.x) v[4 * k4] = -INFINITY;
+      if (!in || t >= lm.y) v[4 * k4 + 1] = -INFINITY;
+      if (!in || t >= lm.z) v[4 * k4 + 2] = -INFINITY;
+      if (!in || t >= lm.w) v[4 * k4 + 3] = -INFINITY;
+    }
+  }
+}
+
 template <int NR>
 __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
                               uint32_t tmem, uint8_t* smem, Red* red, int slot,
@@ -515,7 +582,9 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
   const int qb = block_rows(p, pc.b);
   const int lim0 = causal_limit(pc.len, qb, 0);  // the smallest row limit
 
-  float lp[NR];  // this token's share of each row sum
+  // This token's share of each row sum.  The scores are re-read from TMEM
+  // in 16-column chunks by each pass rather than held in registers.
+  float lp[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) lp[r] = 0.f;
   int mi = 0;
@@ -523,37 +592,30 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
     const int gj = gj0 + jt;
     const int t0 = pc.tok_begin + jt * kTile;
     const int ntok = min(kTile, pc.tok_end - t0);
+    const uint32_t sbuf = lane_base + Cols<NR>::kS + (gj & 1) * NR;
+    const bool masked = ntok < kTile || t0 + kTile > lim0;
+    const bool in = L < ntok;
+    const int t = t0 + L;
     wait_bar(cx, &cx.bars->s_full[gj & 1], (gj >> 1) & 1);
     tc::fence_after();
-    float s[NR];
-    tc::tmem_ld_cols<NR>(lane_base + Cols<NR>::kS + (gj & 1) * NR,
-                         reinterpret_cast<uint32_t*>(s));
-    if (ntok < kTile || t0 + kTile > lim0) {  // masks reach this tile
-      const bool in = L < ntok;
-      const int t = t0 + L;
-      const int4* lim4 = reinterpret_cast<const int4*>(red->lim);
-#pragma unroll
-      for (int r4 = 0; r4 < NR / 4; ++r4) {
-        const int4 lm = lim4[r4];
-        if (!in || t >= lm.x) s[4 * r4] = -INFINITY;
-        if (!in || t >= lm.y) s[4 * r4 + 1] = -INFINITY;
-        if (!in || t >= lm.z) s[4 * r4 + 2] = -INFINITY;
-        if (!in || t >= lm.w) s[4 * r4 + 3] = -INFINITY;
-      }
-    }
     // raise m when a score passes it by more than 2^8 (always on the
     // piece's first tile); the decision is shared by the four warps
     bool slow = jt == 0;
     if (!slow) {
       const float4* mu4 = reinterpret_cast<const float4*>(red->mu[mi]);
       bool need = false;
+#pragma unroll 1
+      for (int c0 = 0; c0 < NR; c0 += 16) {
+        float v[16];
+        load_scores16(sbuf + c0, c0, masked, in, t, red, v);
 #pragma unroll
-      for (int r4 = 0; r4 < NR / 4; ++r4) {
-        const float4 m = mu4[r4];
-        need |= fmaf(s[4 * r4], sl2, -m.x) > kRescaleLog2;
-        need |= fmaf(s[4 * r4 + 1], sl2, -m.y) > kRescaleLog2;
-        need |= fmaf(s[4 * r4 + 2], sl2, -m.z) > kRescaleLog2;
-        need |= fmaf(s[4 * r4 + 3], sl2, -m.w) > kRescaleLog2;
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const float4 m = mu4[(c0 >> 2) + k4];
+          need |= fmaf(v[4 * k4], sl2, -m.x) > kRescaleLog2;
+          need |= fmaf(v[4 * k4 + 1], sl2, -m.y) > kRescaleLog2;
+          need |= fmaf(v[4 * k4 + 2], sl2, -m.z) > kRescaleLog2;
+          need |= fmaf(v[4 * k4 + 3], sl2, -m.w) > kRescaleLog2;
+        }
       }
       const bool any = __any_sync(0xffffffffu, need);
       if (lane == 0) red->flag[gj & 1][q4] = any ? 1 : 0;
@@ -562,13 +624,20 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
               red->flag[gj & 1][2] | red->flag[gj & 1][3]) != 0;
     }
     if (slow) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < NR; c0 += 16) {
+        float v[16];
+        load_scores16(sbuf + c0, c0, masked, in, t, red, v);
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        float v = s[r];
+        for (int k = 0; k < 16; ++k) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-        if (lane == 0) red->colmax[q4][r] = v;
+          for (int o = 16; o > 0; o >>= 1)
+            v[k] = fmaxf(v[k], __shfl_xor_sync(0xffffffffu, v[k], o));
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) red->colmax[q4][c0 + k] = v[k];
+        }
       }
       tc::bar_sync_named(2, 128);
       if (L < NR) {
@@ -611,29 +680,33 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
         tc::tmem_wait_st();
       }
     }
-    // P^T_j = 2^(s - m): this token's row of the MN-major B operand, eight
-    // rows (one 16-byte chunk) at a time.  The P^T buffer of tile gj is free
-    // once PV of tile gj-2 is done.
-    if (gj >= 2) wait_bar(cx, &cx.bars->pv_done[gj & 1], ((gj >> 1) - 1) & 1);
+    // P^T_j = 2^(s - m): this token's row of the MN-major B operand, 16 rows
+    // (two 16-byte chunks) at a time.  The P^T buffer is free once PV of
+    // tile gj-1 is done (long before, in the steady state).
+    if (gj >= 1) wait_bar(cx, &cx.bars->pv_done[(gj - 1) & 1], ((gj - 1) >> 1) & 1);
     const float4* mu4 = reinterpret_cast<const float4*>(red->mu[mi]);
-    uint8_t* prow = smem + kOffP + (gj & 1) * kPBytes + L * 128;
+    uint8_t* prow = smem + kOffP + L * 128;
 #pragma unroll
-    for (int n8 = 0; n8 < NR / 8; ++n8) {
-      const float4 ma = mu4[2 * n8], mb = mu4[2 * n8 + 1];
-      const float m8[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-      uint32_t pk[4];
+    for (int c0 = 0; c0 < NR; c0 += 16) {
+      float v[16];
+      load_scores16(sbuf + c0, c0, masked, in, t, red, v);
+      uint32_t pk[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = 8 * n8 + 2 * e;
-        const float x0 = exp2f(fmaf(s[r], sl2, -m8[2 * e]));
-        const float x1 = exp2f(fmaf(s[r + 1], sl2, -m8[2 * e + 1]));
-        lp[r] += x0;
-        lp[r + 1] += x1;
+      for (int e = 0; e < 8; ++e) {
+        const float4 m = mu4[(c0 >> 2) + (e >> 1)];
+        const float m0 = (e & 1) ? m.z : m.x, m1 = (e & 1) ? m.w : m.y;
+        const float x0 = exp2f(fmaf(v[2 * e], sl2, -m0));
+        const float x1 = exp2f(fmaf(v[2 * e + 1], sl2, -m1));
+        lp[c0 + 2 * e] += x0;
+        lp[c0 + 2 * e + 1] += x1;
         const __half2 hh = __floats2half2_rn(x0, x1);
         pk[e] = *reinterpret_cast<const uint32_t*>(&hh);
       }
+      const int n8 = c0 >> 3;
       *reinterpret_cast<uint4*>(prow + ((n8 ^ (L & 7)) << 4)) =
           make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4*>(prow + (((n8 + 1) ^ (L & 7)) << 4)) =
+          make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
     tc::fence_proxy_async_smem();
     tc::fence_before();
@@ -707,9 +780,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (c >= P) return;  // uniform over the CTA, before any TMEM or barrier use
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      tc::bar_init(tc::smem_u32(&bars.f8_full[s]), 1);
-      tc::bar_init(tc::smem_u32(&bars.f8_empty[s]), 4);
+    for (int s = 0; s < kKStages; ++s) {
+      tc::bar_init(tc::smem_u32(&bars.k8_full[s]), 1);
+      tc::bar_init(tc::smem_u32(&bars.k8_empty[s]), 4);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      tc::bar_init(tc::smem_u32(&bars.v8_full[s]), 1);
+      tc::bar_init(tc::smem_u32(&bars.v8_empty[s]), 4);
     }
     tc::bar_init(tc::smem_u32(&bars.k_full), 4);
     for (int s = 0; s < 3; ++s) {
@@ -725,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     tc::bar_fence_init();
   }
-  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&s_tmem), kTmemCols);
+  if (warp == kWarpQK) tc::tmem_alloc(tc::smem_u32(&s_tmem), kTmemCols);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -760,15 +837,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the ring and operand barriers; the MMA issuer and the softmax warps
     // meet around each piece, so Q is rewritten only after the previous
     // piece's last MMA and O^T is read before the next piece's first PV.
-    if (warp == 0) {
+    if (warp == kWarpProducer) {
       produce(cx, pc, gj0, smem, &tm_k, &tm_v);
       last_loaded = gj0 + pc.n_tiles - 1;
       __syncwarp();
-    } else if (warp >= 6 && warp < 10) {
-      dequant_piece<NR>(cx, pc, gj0, smem, tmem);
-    } else {
+    } else if (warp >= 4 && warp < 12) {
+      dequant_piece<NR>(cx, pc, gj0, smem, tmem, (warp - 4) >> 2);
+    } else if (warp < 4 || warp == kWarpQK || warp == kWarpPV) {
       int S = 0, slot = 0;
-      if (warp >= 2 && warp < 6) {
+      if (warp < 4) {
         // where this piece's result goes
         S = seg_splits(pc.s0, pc.nt, U, P);
         slot = S > 1 ? slot_base_warp(p, s_pre, pc.b * p.hkv + pc.g, U, P) +
@@ -779,9 +856,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before();
       tc::bar_sync_named(1, kPieceThreads);
       tc::fence_after();
-      if (warp == 1 || warp == 10) {
+      if (warp == kWarpQK || warp == kWarpPV) {
         if (lane == 0) {
-          if (warp == 1) qk_piece<NR>(cx, pc, gj0, tmem);
+          if (warp == kWarpQK) qk_piece<NR>(cx, pc, gj0, tmem);
           else pv_piece<NR>(cx, pc, gj0, tmem);
         }
         __syncwarp();
@@ -796,18 +873,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // teardown: no copy or MMA may still be in flight
-  if (warp == 0 && lane == 0) {
-    for (int gj = max(0, last_loaded - kStages + 1); gj <= last_loaded; ++gj)
-      wait_bar(cx, &bars.f8_full[gj % kStages], (gj / kStages) & 1, true);
+  if (warp == kWarpProducer && lane == 0) {
+    for (int gj = max(0, last_loaded - kKStages + 1); gj <= last_loaded; ++gj)
+      wait_bar(cx, &bars.k8_full[gj % kKStages], (gj / kKStages) & 1, true);
+    for (int gj = max(0, last_loaded - kVStages + 1); gj <= last_loaded; ++gj)
+      wait_bar(cx, &bars.v8_full[gj % kVStages], (gj / kVStages) & 1, true);
   }
-  if ((warp == 1 || warp == 10) && lane == 0) {  // both MMA issuers
+  if ((warp == kWarpQK || warp == kWarpPV) && lane == 0) {  // both issuers
     tc::commit(tc::smem_u32(&bars.drain));
     wait_bar(cx, &bars.drain, 0, true);
   }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWarpQK) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int NR>
