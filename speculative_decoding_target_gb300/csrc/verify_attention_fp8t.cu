@@ -26,10 +26,10 @@
 //   then O^T (half h at + h NR; lane = channel, column = row) and two S^T
 //   buffers of NR columns (lane = token, column = row).
 //
-// Shared memory: a 2-slot ring of staged K bytes (+ scales) and a 3-slot
-// ring of staged V bytes (+ scales): K is converted first and its slot
-// released early, V is held until its conversion ends.  Then Q (the QK^T B
-// operand) and the P^T buffer (the PV B operand).
+// Shared memory: 2-slot rings of staged K bytes (+ scales) and of staged V
+// bytes (+ scales): K is converted first and its slot released early, V is
+// held until its conversion ends.  Then Q (the QK^T B operand) and two P^T
+// buffers (the PV B operand).
 //
 // Warp roles (512 threads; 128 registers each):
 //   warps 0..3    softmax: one thread per token lane.  Load S^T_j in
@@ -72,12 +72,11 @@ namespace specv {
 namespace {
 
 constexpr int kTile = 128;                  // tokens per tile
-// Staging: separate rings for the K and the V bytes of a tile.  K is
-// converted first and released early, V is held until its conversion
-// ends, so V gets the deeper ring.
+// Staging: separate rings for the K and the V bytes of a tile, so the K
+// slot, converted first, is refilled while V is still being converted.
 constexpr int kHalf = kTile * 128;          // 128-channel half of K or V
 constexpr int kKStages = 2;
-constexpr int kVStages = 3;
+constexpr int kVStages = 2;
 constexpr int kSBytes = 2 * kHalf;          // K or V bytes, two halves
 constexpr int kKSlot = kSBytes + kTile * 8;             // + K scales
 constexpr int kVSlot = kSBytes + kTile * 8 + kTile * 8;  // + V scales, transposed
@@ -88,8 +87,8 @@ constexpr int kOffVR = kKStages * kKSlot;   // V ring
 constexpr int kRowsMax = 64;                // NR of the largest instance
 constexpr int kOffQ = kOffVR + kVStages * kVSlot;
 constexpr int kOffP = kOffQ + kRowsMax * 512;
-constexpr int kPBytes = kTile * 128;        // the P^T buffer
-constexpr int kOffRed = kOffP + kPBytes;
+constexpr int kPBytes = kTile * 128;        // one of two P^T buffers
+constexpr int kOffRed = kOffP + 2 * kPBytes;
 constexpr uint32_t kColK = 0, kColV = 128;
 constexpr int kSub = 64;                    // tokens per V^T slot
 // Tensor-memory columns of the NR-row instance: V^T slots of 64 tokens
@@ -468,11 +467,14 @@ __device__ void pv_piece(const Ctx& cx, const Piece& pc, int gj0,
                              ((uint32_t)(NR >> 3) << 17) |
                              ((uint32_t)(128 >> 4) << 24);
   uint8_t* smem = reinterpret_cast<uint8_t*>(cx.smem);
-  const uint64_t pdesc = tc::desc_sw128(tc::smem_u32(smem + kOffP), 8192, 1024);
+  const uint64_t pdesc0 = tc::desc_sw128(tc::smem_u32(smem + kOffP), 8192, 1024);
+  const uint64_t pdesc1 =
+      tc::desc_sw128(tc::smem_u32(smem + kOffP + kPBytes), 8192, 1024);
   for (int jt = 0; jt < pc.n_tiles; ++jt) {
     const int gj = gj0 + jt;
     const int t0 = pc.tok_begin + jt * kTile;
     const int nk = (min(kTile, pc.tok_end - t0) + 15) >> 4;
+    const uint64_t pdesc = (gj & 1) ? pdesc1 : pdesc0;
     wait_bar(cx, &cx.bars->p_full[gj & 1], (gj >> 1) & 1);
     // two halves of 64 tokens, each from its V^T slot, so a slot is
     // released as soon as its tokens are through
@@ -681,11 +683,11 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
       }
     }
     // P^T_j = 2^(s - m): this token's row of the MN-major B operand, 16 rows
-    // (two 16-byte chunks) at a time.  The P^T buffer is free once PV of
-    // tile gj-1 is done (long before, in the steady state).
-    if (gj >= 1) wait_bar(cx, &cx.bars->pv_done[(gj - 1) & 1], ((gj - 1) >> 1) & 1);
+    // (two 16-byte chunks) at a time.  The P^T buffer of tile gj is free
+    // once PV of tile gj-2 is done.
+    if (gj >= 2) wait_bar(cx, &cx.bars->pv_done[gj & 1], ((gj >> 1) - 1) & 1);
     const float4* mu4 = reinterpret_cast<const float4*>(red->mu[mi]);
-    uint8_t* prow = smem + kOffP + L * 128;
+    uint8_t* prow = smem + kOffP + (gj & 1) * kPBytes + L * 128;
 #pragma unroll
     for (int c0 = 0; c0 < NR; c0 += 16) {
       float v[16];
