@@ -41,28 +41,41 @@ UNIT = "steps/s"
 DEFAULT_WORKLOAD = "b8_q8_p32k"
 KERNEL_LAUNCHES_PER_STEP = 4   # split, merge, argmax partial, accept finalize
 
-# DRAM traffic of one launch of the dominant kernel (the tcgen05 split-KV
-# attention kernel), dram__bytes_read.sum + dram__bytes_write.sum from one
-# ncu capture (profiles/verify_split_tc_*.md), keyed by workload and valid
-# only while the kernel's sources still hash to the recorded value.
+# DRAM traffic of one launch of the dominant kernel (the split-KV attention
+# kernel), dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture
+# (profiles/verify_split_*.md), keyed by workload and valid only while that
+# kernel's sources still hash to the recorded value.
 NCU_TRAFFIC = {
-    "b8_q8_p32k": {"source_hash": "9217cbe2f390b8ad",
-                   "bytes_per_launch": 1077417472 + 4754688},
+    "b8_q8_p32k": {"kernel": "tc", "source_hash": "dfb5dcdea55c1096",
+                   "bytes_per_launch": 1077487104 + 5111552},
     # captured on the smaller FP8 case b8_q8_p16k_fp8 (276.96 MB
-    # algorithmic: 279.35 MB read + 4.70 MB written) and scaled to a full
+    # algorithmic: 279.95 MB read + 5.19 MB written) and scaled to a full
     # launch by the algorithmic bytes, which the traffic follows
-    "b32_q8_p1k128k_fp8": {"source_hash": "9217cbe2f390b8ad",
-                           "per_algorithmic_byte": (279346432 + 4695040)
+    "b32_q8_p1k128k_fp8": {"kernel": "fp8t", "source_hash": "72a7403f7c7430de",
+                           "per_algorithmic_byte": (279953664 + 5192704)
                            / (8 * 16392 * 4 * 528)},
 }
 NCU_TRAFFIC["b8_q8_p16k_fp8"] = NCU_TRAFFIC["b32_q8_p1k128k_fp8"]
-SPLIT_KERNEL_SOURCES = ("verify_attention_tc.cu", "common.cuh", "tc_ptx.cuh")
+
+# Sources of each split kernel: bf16 KV and FP8 blocks of more than 64 rows
+# per KV head take the tcgen05 kernel with Q in tensor memory; FP8 blocks of
+# at most 64 rows take the kernel with K and V^T in tensor memory.
+KERNEL_SOURCES = {
+    "tc": ("verify_attention_tc.cu", "common.cuh", "tc_ptx.cuh"),
+    "fp8t": ("verify_attention_fp8t.cu", "tmem_io.cuh", "common.cuh",
+             "tc_ptx.cuh"),
+}
 
 
-def kernel_source_hash() -> str:
+def split_kernel_of(w) -> str:
+    rows = w.q_len * (w.num_q_heads // w.num_kv_heads)
+    return "fp8t" if w.kv_dtype != "bf16" and rows <= 64 else "tc"
+
+
+def kernel_source_hash(kind: str = "tc") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_target_gb300", "csrc")
-    for fn in SPLIT_KERNEL_SOURCES:
+    for fn in KERNEL_SOURCES[kind]:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -275,7 +288,7 @@ def run_gpu(args, w: wl.VerifyWorkload):
     attn_avg_s = statistics.mean(attn_ms) / 1e3
     peak, peak_kind = measured_peaks()
     achieved = kv_b / attn_avg_s / 1e9
-    src_hash = kernel_source_hash()
+    src_hash = kernel_source_hash(split_kernel_of(w))
     traffic = None
     rec = NCU_TRAFFIC.get(w.name)
     if rec and rec.get("source_hash") == src_hash:
