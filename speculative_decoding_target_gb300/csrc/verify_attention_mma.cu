@@ -402,12 +402,12 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
     const float* o =
         p.part_o + ((long long)base * p.rows + r) * kHeadDim + lane * 8;
     const long long stride = (long long)p.rows * kHeadDim;
-    // eight splits at a time, every load issued before any is used
-    for (int sb = 0; sb < S; sb += 8) {
-      float lv[8];
-      float4 x0[8], x1[8];
+    // sixteen splits at a time, every load issued before any is used
+    for (int sb = 0; sb < S; sb += 16) {
+      float lv[16];
+      float4 x0[16], x1[16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 16; ++j) {
         const int s = sb + j;
         if (s < S) {
           lv[j] = lse[(long long)s * p.rows];
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
         }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 16; ++j) {
         if (sb + j >= S) break;
         const float w = exp2f(lv[j] - mx);
         den += w;

@@ -416,19 +416,19 @@ __device__ __forceinline__ void load_q_tmem(const AttnParams& p, const Piece& pc
   const uint4* src = reinterpret_cast<const uint4*>(
       p.q + (((long long)pc.b * p.q_len + i) * p.hq + h) * kHeadDim);
   const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16) + kColQ;
-#pragma unroll 1
-  for (int half = 0; half < 2; ++half) {  // 128 channels: loads in flight
-    uint4 xs[16];
+  uint4 xs[32];  // the whole row: every load in flight at once
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
-      xs[k] = valid ? __ldg(src + half * 16 + k) : make_uint4(0, 0, 0, 0);
+  for (int k = 0; k < 32; ++k)
+    xs[k] = valid ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
 #pragma unroll
     for (int cq = 0; cq < 2; ++cq) {  // 64 channels = 32 columns per store
       const int cb = half * 2 + cq;
       uint32_t v[32];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        uint4 x = xs[cq * 8 + k];
+        uint4 x = xs[half * 16 + cq * 8 + k];
         if (kFp8) {  // bf16 pairs -> fp16 pairs
           uint32_t* w = reinterpret_cast<uint32_t*>(&x);
 #pragma unroll
