@@ -364,21 +364,27 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
 
 // One warp per block row: out = sum_s 2^(lse_s - lse) o_s for split
 // segments; segments with no cached token get zero rows.
+// Two warps per block row: they take alternate batches of eight splits and
+// combine their sums through shared memory, so a long list of splits costs
+// half the rounds of dependent loads without more registers per thread.
+constexpr int kMergeRowsPerBlock = 4;
 __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
   __shared__ int s_pre[kMaxBatch + 1];
+  __shared__ float s_acc[kMergeRowsPerBlock][32][9];  // the odd warp's sums
   plan_prefix(p, s_pre);
   const long long U = (long long)p.hkv * s_pre[p.batch];
   const int k = blockIdx.y, b = k / p.hkv, g = k - b * p.hkv;
   const int ntv = s_pre[b + 1] - s_pre[b];  // virtual units
   const int nt = ntv - kPieceCost;           // real units
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 8 + warp;
-  if (r >= p.rows) return;
+  const int pr = warp >> 1, odd = warp & 1;  // row of the block, half
+  const int r = blockIdx.x * kMergeRowsPerBlock + pr;
+  if (r >= p.rows) return;  // both warps of the pair
   const int i = r / p.group, h = g * p.group + (r - i * p.group);
   __nv_bfloat16* dst =
       p.out + (((long long)b * p.q_len + i) * p.hq + h) * kHeadDim + lane * 8;
   if (nt == 0) {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    if (!odd) *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     return;
   }
   const int P = effective_grid(p.grid, U);
@@ -402,12 +408,13 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
     const float* o =
         p.part_o + ((long long)base * p.rows + r) * kHeadDim + lane * 8;
     const long long stride = (long long)p.rows * kHeadDim;
-    // sixteen splits at a time, every load issued before any is used
-    for (int sb = 0; sb < S; sb += 16) {
-      float lv[16];
-      float4 x0[16], x1[16];
+    // eight splits at a time, every load issued before any is used; the
+    // two warps of the pair take alternate batches
+    for (int sb = 8 * odd; sb < S; sb += 16) {
+      float lv[8];
+      float4 x0[8], x1[8];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < 8; ++j) {
         const int s = sb + j;
         if (s < S) {
           lv[j] = lse[(long long)s * p.rows];
@@ -419,7 +426,7 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
         }
       }
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < 8; ++j) {
         if (sb + j >= S) break;
         const float w = exp2f(lv[j] - mx);
         den += w;
@@ -429,6 +436,17 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
       }
     }
   }
+  // the odd warp hands its sums to the even one (named barrier of the pair)
+  if (odd) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s_acc[pr][lane][e] = acc[e];
+    s_acc[pr][lane][8] = den;
+  }
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + pr) : "memory");
+  if (odd) return;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] += s_acc[pr][lane][e];
+  den += s_acc[pr][lane][8];
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint4 v;
   v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
@@ -498,7 +516,8 @@ cudaError_t launch_verify_merge(const AttnParams& p, cudaStream_t s) {
   // a programmatic dependent launch: the merge grid may start once every
   // split CTA has begun, and waits for the split grid before its reads
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p.rows + 7) / 8, p.batch * p.hkv);
+  cfg.gridDim = dim3((p.rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock,
+                     p.batch * p.hkv);
   cfg.blockDim = dim3(256);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
