@@ -173,7 +173,8 @@ int spec_verify_status(const void* workspace, uint32_t* status_out,
 /*
  * Bytes of device workspace spec_greedy_accept needs for `rows` = batch *
  * q_len logits rows of `vocab` entries (per-row, per-vocabulary-chunk
- * argmax partials).  Returns 0 on bad sizes.
+ * argmax partials, and a per-request count of finished CTAs that the call
+ * zeroes itself).  Returns 0 on bad sizes.
  */
 size_t spec_accept_workspace_size(int32_t rows, int32_t vocab);
 
@@ -209,7 +210,7 @@ int spec_greedy_accept(const float* logits, const int32_t* draft_ids,
 
 /*
  * Greedy acceptance with per-request block widths and the cache length
- * after the commit, in the same two launches as spec_greedy_accept ("DFlash
+ * after the commit, in the same single launch as spec_greedy_accept ("DFlash
  * to dLLM self-spec, part 1", section 1.3.3: accept, bonus and new sequence
  * lengths from one kernel; section 1.3.2: the GPU-side lengths advance
  * without a copy to the host).

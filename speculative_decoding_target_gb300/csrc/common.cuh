@@ -207,6 +207,7 @@ struct AcceptParams {
   int32_t* out_tokens;
   float* part_val;   // [rows, chunks]
   int32_t* part_idx; // [rows, chunks]
+  int32_t* counters; // [batch]: finished CTAs per request (zeroed per call)
   int batch, q_len, vocab, rows, chunks;
   int vec4;          // logits rows are 16-byte aligned and vocab % 4 == 0
 };

@@ -3,11 +3,12 @@
 // section 1.1 verify comparison table, section 1.3.3 accept/bonus kernel,
 // section 1.6.1 commit_lens = accept_len + 1).
 //
-// Kernel 1 streams the fp32 logits once: CTA (chunk, row) reduces 8192
+// One launch streams the fp32 logits once: CTA (chunk, row) reduces 8192
 // entries with 16-byte streaming loads to a (maximum, first index) pair;
-// rows past a request's block width are skipped unread.  Kernel 2, one CTA
-// per request, reduces the chunk pairs of its rows, walks the drafts and
-// publishes the committed cache length.  The reduction order is arbitrary, so the combine is a total
+// rows past a request's block width are skipped unread.  The last CTA of a
+// request to finish (a per-request counter, zeroed before the launch) then
+// reduces the chunk pairs of its rows, walks the drafts and publishes the
+// committed cache length.  The reduction order is arbitrary, so the combine is a total
 // order that makes the result unique: NaN above every number (lower index
 // first among NaNs), then larger value, then lower index (so -0 == +0 ties
 // go to the lower index).
@@ -51,21 +52,16 @@ __device__ __forceinline__ bool hits(float e, float M, bool nanM) {
   return nanM ? e != e : e == M;
 }
 
-// One CTA per (8192-entry chunk, row).  Pass 1 takes the chunk's maximum
-// with one NaN-propagating max per logit; only threads that hold that
-// maximum then look for its first index among their own logits (in index
-// order), and the smallest such index wins.  The pair (maximum, first
+// The chunk pair of (chunk, row), by one CTA.  Pass 1 takes the chunk's
+// maximum with one NaN-propagating max per logit; only threads that hold
+// that maximum then look for its first index among their own logits (in
+// index order), and the smallest such index wins.  The pair (maximum, first
 // index) is the same one the total order above selects.
-__global__ void __launch_bounds__(kAcceptThreads)
-    argmax_partial_kernel(const AcceptParams p) {
+__device__ __forceinline__ void chunk_argmax(const AcceptParams& p, int chunk,
+                                             int row) {
   constexpr int kVec = kAcceptChunk / 4 / kAcceptThreads;  // float4 per thread
   __shared__ float s_m[kAcceptThreads / 32];
   __shared__ int s_i[kAcceptThreads / 32];
-  const int chunk = blockIdx.x, row = blockIdx.y;
-  if (p.q_lens) {  // uniform per CTA: the row lies past its block
-    const int b = row / p.q_len;
-    if (row - b * p.q_len >= min(max(p.q_lens[b], 0), p.q_len)) return;
-  }
   const float* x = p.logits + (long long)row * p.vocab;
   const int begin = chunk * kAcceptChunk;
   const int end = min(begin + kAcceptChunk, p.vocab);
@@ -134,20 +130,21 @@ __global__ void __launch_bounds__(kAcceptThreads)
   }
 }
 
-__global__ void accept_finalize_kernel(const AcceptParams p) {
-  __shared__ int s_t[32];
-  const int b = blockIdx.x;
+// Request b's accepted prefix and bonus token from its rows' chunk pairs,
+// by one CTA (the pairs are read past L1: other CTAs wrote them).
+__device__ __forceinline__ void finalize_request(const AcceptParams& p, int b) {
+  __shared__ int s_t[16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qb = p.q_lens ? min(max(p.q_lens[b], 0), p.q_len) : p.q_len;
-  if (warp < qb) {
-    const long long row = (long long)b * p.q_len + warp;
+  for (int j = warp; j < qb; j += kAcceptThreads / 32) {
+    const long long row = (long long)b * p.q_len + j;
     float bv = -INFINITY;
     int bi = INT_MAX;
     for (int c = lane; c < p.chunks; c += 32)
-      take(p.part_val[row * p.chunks + c], p.part_idx[row * p.chunks + c], bv,
-           bi);
+      take(__ldcg(p.part_val + row * p.chunks + c),
+           __ldcg(p.part_idx + row * p.chunks + c), bv, bi);
     warp_argmax(bv, bi);
-    if (lane == 0) s_t[warp] = bi;
+    if (lane == 0) s_t[j] = bi;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -169,14 +166,35 @@ __global__ void accept_finalize_kernel(const AcceptParams p) {
   }
 }
 
+// CTA (chunk, row): the chunk pair, then the per-request count; the
+// request's last CTA to finish reduces its rows.
+__global__ void __launch_bounds__(kAcceptThreads)
+    argmax_partial_kernel(const AcceptParams p) {
+  const int chunk = blockIdx.x, row = blockIdx.y;
+  const int b = row / p.q_len;
+  // uniform per CTA: a row past its block is not read, only counted
+  if (!p.q_lens || row - b * p.q_len < min(max(p.q_lens[b], 0), p.q_len))
+    chunk_argmax(p, chunk, row);
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's pair before its count
+    s_last = atomicAdd(p.counters + b, 1) == p.q_len * p.chunks - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    finalize_request(p, b);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_greedy_accept(const AcceptParams& p, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(int32_t) * p.batch, s);
+  if (e != cudaSuccess) return e;
   dim3 g1(p.chunks, p.rows);
   argmax_partial_kernel<<<g1, kAcceptThreads, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  accept_finalize_kernel<<<p.batch, 32 * p.q_len, 0, s>>>(p);
   return cudaGetLastError();
 }
 

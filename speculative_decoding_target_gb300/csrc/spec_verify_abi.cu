@@ -706,7 +706,8 @@ size_t spec_accept_workspace_size(int32_t rows, int32_t vocab) {
   const size_t chunks = ((size_t)vocab + specv::kAcceptChunk - 1) /
                         specv::kAcceptChunk;
   return round_up((size_t)rows * chunks * sizeof(float), 256) +
-         round_up((size_t)rows * chunks * sizeof(int32_t), 256) + 256;
+         round_up((size_t)rows * chunks * sizeof(int32_t), 256) +
+         round_up((size_t)rows * sizeof(int32_t), 256) + 256;
 }
 
 int spec_greedy_accept(const float* logits, const int32_t* draft_ids,
@@ -769,8 +770,10 @@ int spec_greedy_accept_commit(const float* logits, const int32_t* draft_ids,
   p.vec4 = (vocab % 4 == 0) && aligned(logits, 16);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.part_val = reinterpret_cast<float*>(ws);
-  p.part_idx = reinterpret_cast<int32_t*>(
-      ws + round_up((size_t)rows * p.chunks * sizeof(float), 256));
+  const size_t idx_off = round_up((size_t)rows * p.chunks * sizeof(float), 256);
+  p.part_idx = reinterpret_cast<int32_t*>(ws + idx_off);
+  p.counters = reinterpret_cast<int32_t*>(
+      ws + idx_off + round_up((size_t)rows * p.chunks * sizeof(int32_t), 256));
   cudaError_t e = specv::launch_greedy_accept(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return fail(SPEC_ERR_CUDA, "accept kernel launch: %s", cudaGetErrorString(e));

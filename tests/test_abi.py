@@ -123,11 +123,12 @@ def test_accept_argument_checks(lib):
 
 
 def test_accept_workspace_size_formula(lib):
-    # one (fp32 value, int32 index) pair per row and 8192-entry vocab chunk
+    # one (fp32 value, int32 index) pair per row and 8192-entry vocab
+    # chunk, and one completion counter per row (at most one per request)
     chunks = -(-248320 // 8192)
     n = lib.spec_accept_workspace_size(64, 248320)
-    assert n >= 64 * chunks * 8
-    assert n <= 64 * chunks * 8 + 3 * 256
+    assert n >= 64 * chunks * 8 + 64 * 4
+    assert n <= 64 * chunks * 8 + 64 * 4 + 4 * 256
     assert lib.spec_accept_workspace_size(-1, 10) == 0
 
 
