@@ -14,6 +14,7 @@
 // go to the lower index).
 #include <climits>
 
+#include "accept.cuh"
 #include "common.cuh"
 
 namespace specv {

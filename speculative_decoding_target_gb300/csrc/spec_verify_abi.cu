@@ -12,6 +12,7 @@
 #include "next_block.cuh"
 #include "selector.cuh"
 #include "stochastic.cuh"
+#include "accept.cuh"
 #include "common.cuh"
 #include "spec_verify.h"
 
