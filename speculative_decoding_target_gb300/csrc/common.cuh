@@ -2,17 +2,23 @@
 //
 // Work plan of the split-KV verify attention.  The KV of every (request b,
 // KV head g) pair -- a "segment" -- is cut into 64-token units.  Segments are
-// laid end to end in (b, g) order, giving U units in total; CTA c of the
-// fixed grid of P CTAs takes the contiguous unit range
-// [floor(c*U/P), floor((c+1)*U/P)), where P is the launched grid capped at
-// U so that no CTA's range is empty.  A segment touched by several CTAs is
-// "split": each touching CTA writes an fp32 partial (normalised output row
-// and base-2 log-sum-exp per block row) and the merge kernel combines them
-// ("Qwen3.8-27B-FP8" page, "Implemented execution path": split-context decode
-// with compact online-softmax partials and a merge).  A segment owned by one
-// CTA is written straight to the output.  Every kernel derives the same plan
-// from seq_lens on the device, so the grid never depends on host-side
-// lengths and the launch is graph-capturable.
+// laid end to end in (b, g) order, giving U units in total, and the unit
+// line is cut into contiguous chunks: P static chunks
+// [floor(c*A/P), floor((c+1)*A/P)) over the first A units, one per CTA of
+// the fixed grid (P is the launched grid capped so that no chunk is empty),
+// then R dynamic chunks [A + floor(j*(U-A)/R), A + floor((j+1)*(U-A)/R))
+// over the rest, which CTAs claim one at a time from a counter as they run
+// out of work, so CTAs that stream their KV faster take more of the tail.
+// With R = 0 (A = U) the plan is fully static.  A segment touched by several
+// chunks is "split": each touching chunk writes an fp32 partial (normalised
+// output row and base-2 log-sum-exp per block row) into its own slot and
+// the merge kernel combines them ("Qwen3.8-27B-FP8" page, "Implemented
+// execution path": split-context decode with compact online-softmax
+// partials and a merge).  A segment inside one chunk is written straight to
+// the output.  Every kernel derives the same plan from seq_lens on the
+// device, so the grid never depends on host-side lengths and the launch is
+// graph-capturable; which CTA runs a dynamic chunk changes from call to
+// call, what it computes and where it writes do not.
 #pragma once
 
 #include <cuda.h>
@@ -27,7 +33,7 @@ constexpr int kHeadDim = 256;
 constexpr int kUnit = 64;        // tokens per plan unit
 constexpr int kMaxRows = 128;    // q_len * group rows of one KV head
 constexpr int kMaxBatch = 1024;  // requests per call (shared-memory prefix)
-constexpr int kWsHeader = 256;   // bytes; word 0 = status
+constexpr int kWsHeader = 256;   // bytes; word 0 = status, word 1 = chunk counter
 
 struct AttnParams {
   const __nv_bfloat16* q;
@@ -46,6 +52,8 @@ struct AttnParams {
   int page_size, log2_ps, num_pages, max_pages;
   int max_tokens;     // max_pages * page_size: seq_lens clamp
   int grid;           // P: CTAs of the split kernel
+  int dyn_chunks;     // dynamic chunks per CTA (0: static plan)
+  int* chunk_ctr;     // dynamic chunks claimed so far (zeroed per call)
   int box_rows;       // TMA box height (tcgen05 kernel): min(page_size, 64)
   float scale_log2;   // softmax scale * log2(e)
 };
@@ -80,21 +88,29 @@ __device__ __forceinline__ int units_of(int len) {
 // units at kPieceCost beyond that, nt'_b = s_pre[b+1] - s_pre[b].
 constexpr int kPieceCost = 3;
 
-// First unit of CTA c.
-__device__ __forceinline__ long long cta_start(int c, long long U, int P) {
-  return (long long)c * U / P;
+struct Plan {
+  long long U;  // virtual units
+  long long A;  // units of the static chunks
+  int P;        // static chunks = CTAs that run
+  int R;        // dynamic chunks after them
+};
+
+// First unit of chunk i (0 <= i <= P + R).
+__device__ __forceinline__ long long chunk_start(const Plan& pl, int i) {
+  return i <= pl.P ? (long long)i * pl.A / pl.P
+                   : pl.A + (long long)(i - pl.P) * (pl.U - pl.A) / pl.R;
 }
 
-// CTA whose range holds unit u (0 <= u < U).
-__device__ __forceinline__ int cta_of(long long u, long long U, int P) {
-  return (int)(((u + 1) * (long long)P - 1) / U);
+// Chunk whose range holds unit u (0 <= u < U).
+__device__ __forceinline__ int chunk_of(const Plan& pl, long long u) {
+  if (u < pl.A) return (int)(((u + 1) * (long long)pl.P - 1) / pl.A);
+  return pl.P + (int)(((u - pl.A + 1) * (long long)pl.R - 1) / (pl.U - pl.A));
 }
 
-// Number of CTAs that touch a segment starting at unit s0 with nt units.
-__device__ __forceinline__ int seg_splits(long long s0, int nt, long long U,
-                                          int P) {
+// Number of chunks that touch a segment starting at unit s0 with nt units.
+__device__ __forceinline__ int seg_splits(const Plan& pl, long long s0, int nt) {
   if (nt <= 0) return 0;
-  return cta_of(s0 + nt - 1, U, P) - cta_of(s0, U, P) + 1;
+  return chunk_of(pl, s0 + nt - 1) - chunk_of(pl, s0) + 1;
 }
 
 // Exclusive prefix of virtual units per request (real units + kPieceCost)
@@ -133,22 +149,35 @@ __device__ __forceinline__ int effective_grid(int grid, long long U) {
   return want < grid ? (int)want : grid;
 }
 
-// Sum of splits of every segment before segment k (the partial-slot base of
-// segment k).  Called by one full warp; all lanes return the same value.
-__device__ __forceinline__ int slot_base_warp(const AttnParams& p,
-                                              const int* s_pre, int k,
-                                              long long U, int P) {
-  const int lane = threadIdx.x & 31;
-  int acc = 0;
-  for (int kk = lane; kk < k; kk += 32) {
-    int b = kk / p.hkv, g = kk - b * p.hkv;
-    int ntv = s_pre[b + 1] - s_pre[b];
-    long long rs = (long long)p.hkv * s_pre[b] + (long long)g * ntv + kPieceCost;
-    acc += seg_splits(rs, ntv - kPieceCost, U, P);
+// The dynamic chunks cover the last U >> kDynShift units (an eighth), when
+// that leaves each of them at least kMinUnitsPerCta units; otherwise the
+// plan is static.  Every static chunk is non-empty: A >= 7U/8 >= P.
+constexpr int kDynShift = 3;
+__device__ __forceinline__ Plan make_plan(const AttnParams& p, long long U) {
+  Plan pl;
+  pl.U = U;
+  pl.P = effective_grid(p.grid, U);
+  pl.A = U;
+  pl.R = 0;
+  if (p.dyn_chunks > 0) {
+    const long long D = U >> kDynShift;
+    const long long R = (long long)p.dyn_chunks * pl.P;
+    if (D >= R * kMinUnitsPerCta) {
+      pl.A = U - D;
+      pl.R = (int)R;
+    }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  return acc;
+  return pl;
+}
+
+// Partial slot of segment k's piece in chunk ch: ch + k.  Chunks are
+// monotone along the unit line and segment k + 1 lies after segment k, so
+// a later segment never touches an earlier chunk: two (segment, chunk)
+// pairs with the same sum would need k1 < k2 and ch1 > ch2, which cannot
+// both touch.  The slots are distinct, those of one segment consecutive
+// (from chunk_of(its first unit) + k), and all below chunks + segments.
+__device__ __forceinline__ int partial_slot(int chunk, int k) {
+  return chunk + k;
 }
 
 // Request owning unit u: the largest b with hkv * s_pre[b] <= u.
@@ -187,6 +216,9 @@ int verify_split_tc_box_rows(int page_size);
 // K and V^T as tensor-memory operands (tensor maps over the byte pools with
 // boxes of 128 bytes x box_rows rows).
 constexpr int kFp8tMaxRows = 64;
+// Dynamic chunks per CTA in the plan of that kernel (its CTAs' KV streaming
+// rates differ by up to ~15% on long mixed-length batches).
+constexpr int kFp8tDynChunks = 2;
 cudaError_t launch_verify_split_fp8t(const AttnParams& p,
                                      const CUtensorMap& tm_k,
                                      const CUtensorMap& tm_v, cudaStream_t s);

@@ -141,12 +141,11 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
   const int g4 = lane >> 2, t4 = lane & 3;
 
   plan_prefix(p, s_pre);
-  const long long U = (long long)p.hkv * s_pre[p.batch];
-  const int P = effective_grid(p.grid, U);
-  const int c = blockIdx.x;
-  if (c >= P) return;  // uniform over the CTA
-  long long u = cta_start(c, U, P);
-  const long long u_end = cta_start(c + 1, U, P);
+  const Plan pl = make_plan(p, (long long)p.hkv * s_pre[p.batch]);
+  const int c = blockIdx.x;  // this kernel runs static plans only
+  if (c >= pl.P) return;     // uniform over the CTA
+  long long u = chunk_start(pl, c);
+  const long long u_end = chunk_start(pl, c + 1);
 
   while (u < u_end) {
     const int b = find_request(s_pre, p.batch, p.hkv, u);
@@ -314,7 +313,7 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
       }
       const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
       const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-      const int S = seg_splits(s0, nt, U, P);
+      const int S = seg_splits(pl, s0, nt);
       if (S == 1) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -334,8 +333,7 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
         }
       } else {
         const int k = b * p.hkv + g;
-        const int slot =
-            slot_base_warp(p, s_pre, k, U, P) + (c - cta_of(s0, U, P));
+        const int slot = partial_slot(c, k);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int r = half ? r1 : r0;
@@ -387,12 +385,12 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
     if (!odd) *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     return;
   }
-  const int P = effective_grid(p.grid, U);
+  const Plan pl = make_plan(p, U);
   const long long s0 =
       (long long)p.hkv * s_pre[b] + (long long)g * ntv + kPieceCost;
-  const int S = seg_splits(s0, nt, U, P);
+  const int S = seg_splits(pl, s0, nt);
   if (S <= 1) return;
-  const int base = slot_base_warp(p, s_pre, k, U, P);
+  const int base = partial_slot(chunk_of(pl, s0), k);
   // launched as a programmatic dependent of the split kernel: everything
   // above overlapped its tail; the partials are read only once it is done
   tc_grid_dependency_wait();

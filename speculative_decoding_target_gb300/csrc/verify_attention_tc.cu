@@ -451,8 +451,8 @@ __device__ __forceinline__ void load_q_tmem(const AttnParams& p, const Piece& pc
 
 template <bool kFp8>
 __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
-                              uint32_t tmem, uint8_t* smem, const int* s_pre,
-                              long long U, int P, int c) {
+                              uint32_t tmem, uint8_t* smem,
+                              const Plan& pl, int c) {
   using C = Cfg<kFp8>;
   const AttnParams& p = *cx.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -464,12 +464,9 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
   const int lim = causal_limit(pc.len, block_rows(p, pc.b), i);
   const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
   const float sl2 = p.scale_log2;
-  // where this piece's result goes (independent of the tiles: worked out
-  // here, off the epilogue's critical path)
-  const int S = seg_splits(pc.s0, pc.nt, U, P);
-  const int slot = S > 1 ? slot_base_warp(p, s_pre, pc.b * p.hkv + pc.g, U, P) +
-                               (c - cta_of(pc.s0, U, P))
-                         : 0;
+  // where this piece's result goes
+  const int S = seg_splits(pl, pc.s0, pc.nt);
+  const int slot = S > 1 ? partial_slot(c, pc.b * p.hkv + pc.g) : 0;
 
   float m = -INFINITY, l = 0.f;
   for (int jt = 0; jt < pc.n_tiles; ++jt) {
@@ -633,10 +630,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   // the merge kernel may be scheduled now; it waits for this grid to finish
   tc_grid_launch_dependents();
   plan_prefix(p, s_pre);
-  const long long U = (long long)p.hkv * s_pre[p.batch];
-  const int P = effective_grid(p.grid, U);
-  const int c = blockIdx.x;
-  if (c >= P) return;  // uniform over the CTA, before any TMEM or barrier use
+  const Plan pl = make_plan(p, (long long)p.hkv * s_pre[p.batch]);
+  const int c = blockIdx.x;  // this kernel runs static plans only
+  if (c >= pl.P) return;  // uniform over the CTA, before any TMEM or barrier use
 
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -669,8 +665,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   const uint32_t tmem = s_tmem;
   Ctx cx{&bars, &s_abort, &p};
 
-  long long u = cta_start(c, U, P);
-  const long long u_end = cta_start(c + 1, U, P);
+  long long u = chunk_start(pl, c);
+  const long long u_end = chunk_start(pl, c + 1);
   int gj0 = 0;
   int last_loaded = -1;  // last tile index the producer loaded
   while (u < u_end) {
@@ -713,7 +709,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         if (lane == 0) mma_piece<kFp8>(cx, pc, gj0, tmem, smem);
         __syncwarp();
       } else {
-        softmax_piece<kFp8>(cx, pc, gj0, tmem, smem, s_pre, U, P, c);
+        softmax_piece<kFp8>(cx, pc, gj0, tmem, smem, pl, c);
       }
       tc::fence_before();
       tc::bar_sync_named(1, kPieceThreads);
