@@ -101,10 +101,8 @@ typedef struct {
  * current device (the split count depends on the SM count).  The workspace
  * holds the split partials: per split and block row an fp32 output row and
  * an fp32 log-sum-exp, plus a 256-byte header whose first 32-bit word is
- * the status word and whose second counts the work chunks claimed at run
- * time (FP8 KV with at most 64 block rows per KV head; the call resets it
- * on its stream before the kernels run).  Returns 0 and sets
- * spec_last_error() on a bad desc or when no CUDA device is usable.
+ * the status word.  Returns 0 and sets spec_last_error() on a bad desc or
+ * when no CUDA device is usable.
  */
 size_t spec_verify_workspace_size(const spec_attn_desc* desc);
 

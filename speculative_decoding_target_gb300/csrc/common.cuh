@@ -2,23 +2,17 @@
 //
 // Work plan of the split-KV verify attention.  The KV of every (request b,
 // KV head g) pair -- a "segment" -- is cut into 64-token units.  Segments are
-// laid end to end in (b, g) order, giving U units in total, and the unit
-// line is cut into contiguous chunks: P static chunks
-// [floor(c*A/P), floor((c+1)*A/P)) over the first A units, one per CTA of
-// the fixed grid (P is the launched grid capped so that no chunk is empty),
-// then R dynamic chunks [A + floor(j*(U-A)/R), A + floor((j+1)*(U-A)/R))
-// over the rest, which CTAs claim one at a time from a counter as they run
-// out of work, so CTAs that stream their KV faster take more of the tail.
-// With R = 0 (A = U) the plan is fully static.  A segment touched by several
-// chunks is "split": each touching chunk writes an fp32 partial (normalised
-// output row and base-2 log-sum-exp per block row) into its own slot and
-// the merge kernel combines them ("Qwen3.8-27B-FP8" page, "Implemented
-// execution path": split-context decode with compact online-softmax
-// partials and a merge).  A segment inside one chunk is written straight to
-// the output.  Every kernel derives the same plan from seq_lens on the
-// device, so the grid never depends on host-side lengths and the launch is
-// graph-capturable; which CTA runs a dynamic chunk changes from call to
-// call, what it computes and where it writes do not.
+// laid end to end in (b, g) order, giving U units in total; CTA c of the
+// fixed grid of P CTAs takes the contiguous unit range ("chunk")
+// [floor(c*U/P), floor((c+1)*U/P)), where P is the launched grid capped so
+// that no chunk is empty.  A segment touched by several chunks is "split":
+// each touching chunk writes an fp32 partial (normalised output row and
+// base-2 log-sum-exp per block row) into its own slot and the merge kernel
+// combines them ("Qwen3.8-27B-FP8" page, "Implemented execution path":
+// split-context decode with compact online-softmax partials and a merge).
+// A segment inside one chunk is written straight to the output.  Every
+// kernel derives the same plan from seq_lens on the device, so the grid
+// never depends on host-side lengths and the launch is graph-capturable.
 #pragma once
 
 #include <cuda.h>
@@ -33,7 +27,7 @@ constexpr int kHeadDim = 256;
 constexpr int kUnit = 64;        // tokens per plan unit
 constexpr int kMaxRows = 128;    // q_len * group rows of one KV head
 constexpr int kMaxBatch = 1024;  // requests per call (shared-memory prefix)
-constexpr int kWsHeader = 256;   // bytes; word 0 = status, word 1 = chunk counter
+constexpr int kWsHeader = 256;   // bytes; word 0 = status
 
 struct AttnParams {
   const __nv_bfloat16* q;
@@ -52,8 +46,6 @@ struct AttnParams {
   int page_size, log2_ps, num_pages, max_pages;
   int max_tokens;     // max_pages * page_size: seq_lens clamp
   int grid;           // P: CTAs of the split kernel
-  int dyn_chunks;     // dynamic chunks per CTA (0: static plan)
-  int* chunk_ctr;     // dynamic chunks claimed so far (zeroed per call)
   int box_rows;       // TMA box height (tcgen05 kernel): min(page_size, 64)
   float scale_log2;   // softmax scale * log2(e)
 };
@@ -90,21 +82,17 @@ constexpr int kPieceCost = 3;
 
 struct Plan {
   long long U;  // virtual units
-  long long A;  // units of the static chunks
-  int P;        // static chunks = CTAs that run
-  int R;        // dynamic chunks after them
+  int P;        // chunks = CTAs that run
 };
 
-// First unit of chunk i (0 <= i <= P + R).
-__device__ __forceinline__ long long chunk_start(const Plan& pl, int i) {
-  return i <= pl.P ? (long long)i * pl.A / pl.P
-                   : pl.A + (long long)(i - pl.P) * (pl.U - pl.A) / pl.R;
+// First unit of chunk c (0 <= c <= P).
+__device__ __forceinline__ long long chunk_start(const Plan& pl, int c) {
+  return (long long)c * pl.U / pl.P;
 }
 
 // Chunk whose range holds unit u (0 <= u < U).
 __device__ __forceinline__ int chunk_of(const Plan& pl, long long u) {
-  if (u < pl.A) return (int)(((u + 1) * (long long)pl.P - 1) / pl.A);
-  return pl.P + (int)(((u - pl.A + 1) * (long long)pl.R - 1) / (pl.U - pl.A));
+  return (int)(((u + 1) * (long long)pl.P - 1) / pl.U);
 }
 
 // Number of chunks that touch a segment starting at unit s0 with nt units.
@@ -149,24 +137,10 @@ __device__ __forceinline__ int effective_grid(int grid, long long U) {
   return want < grid ? (int)want : grid;
 }
 
-// The dynamic chunks cover the last U >> kDynShift units (an eighth), when
-// that leaves each of them at least kMinUnitsPerCta units; otherwise the
-// plan is static.  Every static chunk is non-empty: A >= 7U/8 >= P.
-constexpr int kDynShift = 3;
 __device__ __forceinline__ Plan make_plan(const AttnParams& p, long long U) {
   Plan pl;
   pl.U = U;
   pl.P = effective_grid(p.grid, U);
-  pl.A = U;
-  pl.R = 0;
-  if (p.dyn_chunks > 0) {
-    const long long D = U >> kDynShift;
-    const long long R = (long long)p.dyn_chunks * pl.P;
-    if (D >= R * kMinUnitsPerCta) {
-      pl.A = U - D;
-      pl.R = (int)R;
-    }
-  }
   return pl;
 }
 
@@ -216,9 +190,6 @@ int verify_split_tc_box_rows(int page_size);
 // K and V^T as tensor-memory operands (tensor maps over the byte pools with
 // boxes of 128 bytes x box_rows rows).
 constexpr int kFp8tMaxRows = 64;
-// Dynamic chunks per CTA in the plan of that kernel (its CTAs' KV streaming
-// rates differ by up to ~15% on long mixed-length batches).
-constexpr int kFp8tDynChunks = 2;
 cudaError_t launch_verify_split_fp8t(const AttnParams& p,
                                      const CUtensorMap& tm_k,
                                      const CUtensorMap& tm_v, cudaStream_t s);

@@ -203,7 +203,7 @@ int check_desc(const spec_attn_desc* d) {
 }
 
 struct Layout {
-  int rows, grid, dyn, nslots;
+  int rows, grid, nslots;
   size_t o_off, lse_off, bytes;
 };
 
@@ -212,10 +212,8 @@ int layout(const spec_attn_desc* d, Layout* L) {
   int rc = split_grid(L->rows, use_tc(d), d->kv_dtype == SPEC_KV_FP8_E4M3,
                       &L->grid);
   if (rc) return rc;
-  // partial slots: every chunk of the plan (static and dynamic) starts at
-  // most one split that no earlier chunk started, every segment at most one
-  L->dyn = use_fp8t(d) ? specv::kFp8tDynChunks : 0;
-  L->nslots = L->grid * (1 + L->dyn) + d->batch * d->num_kv_heads;
+  // partial slots: chunk + segment index, below chunks + segments
+  L->nslots = L->grid + d->batch * d->num_kv_heads;
   const size_t o_bytes =
       (size_t)L->nslots * L->rows * specv::kHeadDim * sizeof(float);
   const size_t lse_bytes = (size_t)L->nslots * L->rows * sizeof(float);
@@ -315,8 +313,6 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
   p.max_pages = desc->max_pages_per_seq;
   p.max_tokens = desc->max_pages_per_seq * desc->page_size;
   p.grid = L.grid;
-  p.dyn_chunks = L.dyn;
-  p.chunk_ctr = reinterpret_cast<int*>(ws) + 1;
   p.box_rows = specv::verify_split_tc_box_rows(desc->page_size);
   p.scale_log2 = scale * 1.4426950408889634f;
   const bool tc = use_tc(desc);
@@ -336,17 +332,13 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
     if (rc) return rc;
   }
 
-  cudaError_t e = cudaSuccess;
-  // header words reset per call: the status (checked mode) and the counter
-  // of claimed dynamic chunks (plans with dynamic chunks)
-  const bool checked = desc->flags & SPEC_FLAG_CHECKED;
-  if (checked) p.status = reinterpret_cast<uint32_t*>(ws);
-  if (checked || L.dyn > 0) {  // words [first, last)
-    const int first = checked ? 0 : 1, last = L.dyn > 0 ? 2 : 1;
-    e = cudaMemsetAsync(ws + 4 * first, 0, 4 * (last - first), s);
+  cudaError_t e;
+  if (desc->flags & SPEC_FLAG_CHECKED) {
+    p.status = reinterpret_cast<uint32_t*>(ws);
+    e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess)
+      return fail(SPEC_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
   }
-  if (e != cudaSuccess)
-    return fail(SPEC_ERR_CUDA, "workspace header reset: %s", cudaGetErrorString(e));
   e = fp8t ? specv::launch_verify_split_fp8t(p, tm_k, tm_v, s)
        : tc  ? specv::launch_verify_split_tc(p, tm_k, tm_v, s)
              : specv::launch_verify_split_bf16(p, s);

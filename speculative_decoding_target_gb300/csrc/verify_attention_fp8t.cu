@@ -50,9 +50,7 @@
 //   warp 12       producer: per 128-token tile, lane i loads page run i
 //                 (min(page_size, 64) tokens): 2-D TMA boxes of 128 bytes x
 //                 run with the 128-byte swizzle for each half of the K and V
-//                 rows, and 1-D bulk copies of the run's scales.  After the
-//                 last tile of a chunk of the work plan it claims the next
-//                 dynamic chunk and publishes its id to the other roles.
+//                 rows, and 1-D bulk copies of the run's scales.
 //   warp 13       QK^T issuer (one thread): S^T_j, 16 MMAs, A = K tile in
 //                 TMEM, B = Q from shared memory.
 //   warp 14       PV issuer (one thread): O^T += V^T_j P^T_j per 64-token
@@ -110,11 +108,7 @@ constexpr long long kWaitCycles = 4000000000LL;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kThreads = 512;
 constexpr int kPieceThreads = 6 * 32;       // warps 0..3, 13 and 14
-constexpr int kWarpProducer = 12, kWarpQK = 13, kWarpPV = 14, kWarpIdle = 15;
-// Ring of piece descriptors from the producer (which cuts the chunks it
-// claims into pieces) to the 14 other working warps.
-constexpr int kChunkRing = 4;
-constexpr int kRingReaders = 14;
+constexpr int kWarpProducer = 12, kWarpQK = 13, kWarpPV = 14;
 static_assert(kKSlot % 1024 == 0 && kVSlot % 1024 == 0 && kOffQ % 1024 == 0 &&
                   kOffP % 1024 == 0,
               "swizzled operands need 1024-byte alignment");
@@ -149,8 +143,6 @@ struct Bars {
   uint64_t s_full[2];          // S^T_j complete (also: K tile free again)
   uint64_t p_full[2];          // P^T_j in shared memory (S^T_j consumed)
   uint64_t pv_done[2];         // O^T += V^T_j P^T_j complete
-  uint64_t ch_full[kChunkRing];   // piece published by the producer
-  uint64_t ch_empty[kChunkRing];  // piece read by every other role
   uint64_t drain;
 };
 
@@ -163,7 +155,6 @@ struct Ctx {
 
 struct Piece {
   int b, g, nt, len, tok_begin, tok_end, n_tiles;
-  int S, slot;   // chunks that touch the segment; partial slot when S > 1
   long long s0;
 };
 
@@ -193,13 +184,6 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint64_t* bar,
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
-}
-
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src,
-                                                 uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src),
-               "r"(bytes)
-               : "memory");
 }
 
 // Bulk store of shared-memory bytes to global memory through the async
@@ -843,7 +827,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ Piece s_piece[kChunkRing];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the merge kernel may be scheduled now; it waits for this grid to finish
   tc_grid_launch_dependents();
@@ -871,10 +854,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::bar_init(tc::smem_u32(&bars.p_full[s]), 4);
       tc::bar_init(tc::smem_u32(&bars.pv_done[s]), 1);
     }
-    for (int s = 0; s < kChunkRing; ++s) {
-      tc::bar_init(tc::smem_u32(&bars.ch_full[s]), 1);
-      tc::bar_init(tc::smem_u32(&bars.ch_empty[s]), kRingReaders);
-    }
     tc::bar_init(tc::smem_u32(&bars.drain), 2);
     s_abort = 0;
     tc::bar_fence_init();
@@ -886,125 +865,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s_tmem;
   Ctx cx{&bars, &s_abort, &p, smem};
 
-  // Pieces: the producer walks the CTA's static chunk c, then the dynamic
-  // chunks it claims as it finishes loading the previous one (so the CTAs
-  // that stream fastest take the most), cuts each chunk into pieces and
-  // publishes every piece -- with its output slot -- through a ring in
-  // shared memory, then loads its tiles.  The other roles read the pieces
-  // in order; a piece with b = -1 ends the sequence.  Warp 15 has no role.
+  long long u = chunk_start(pl, c);
+  const long long u_end = chunk_start(pl, c + 1);
   int gj0 = 0;
   int last_loaded = -1;  // last tile index the producer loaded
-  if (warp == kWarpProducer) {
-    int idx = 0;
-    int chunk = c;
-    bool ok = true;
-    while (ok) {
-      long long u = chunk >= 0 ? chunk_start(pl, chunk) : 0;
-      const long long u_end = chunk >= 0 ? chunk_start(pl, chunk + 1) : 0;
-      while (ok) {
-        Piece pc;
-        pc.b = -1;
-        if (u < u_end) {
-          pc.b = find_request(s_pre, p.batch, p.hkv, u);
-          const int ntv = s_pre[pc.b + 1] - s_pre[pc.b];  // virtual units
-          const long long rb = (long long)p.hkv * s_pre[pc.b];
-          pc.g = (int)((u - rb) / ntv);
-          const long long vs = rb + (long long)pc.g * ntv;
-          const int j0v = (int)(u - vs);
-          const int j1v = (int)(u_end - vs < ntv ? u_end - vs : ntv);
-          u = vs + j1v;
-          // real units of the piece; phantom units alone make no piece
-          const int j0 = max(j0v - kPieceCost, 0), j1 = max(j1v - kPieceCost, 0);
-          if (j1 <= j0) continue;
-          pc.nt = ntv - kPieceCost;
-          pc.s0 = vs + kPieceCost;  // the segment's first real unit
-          pc.len = clamp_len(p.seq_lens[pc.b], p.max_tokens);
-          pc.tok_begin = j0 * kUnit;
-          pc.tok_end = min(j1 * kUnit, pc.len);
-          pc.n_tiles = (pc.tok_end - pc.tok_begin + kTile - 1) / kTile;
-          pc.S = seg_splits(pl, pc.s0, pc.nt);
-          pc.slot = pc.S > 1 ? partial_slot(chunk, pc.b * p.hkv + pc.g) : 0;
-        } else if (chunk >= 0) {
-          break;  // chunk done: claim the next one
-        }
-        const int rs = idx % kChunkRing;
-        int okw = 1;
-        if (lane == 0) {
-          if (idx >= kChunkRing)
-            okw = wait_bar(cx, &bars.ch_empty[rs], ((idx / kChunkRing) - 1) & 1);
-          if (okw) {
-            s_piece[rs] = pc;
-            tc::bar_arrive(tc::smem_u32(&bars.ch_full[rs]));
-          }
-        }
-        ++idx;
-        ok = __shfl_sync(0xffffffffu, okw, 0) && pc.b >= 0;
-        if (!ok) break;
-        // the piece's Q rows (one run of group heads per block row) into
-        // L2 now, so the softmax warps find them there tiles later
-        if (lane < min(block_rows(p, pc.b), 32))
-          bulk_prefetch_l2(p.q + (((long long)pc.b * p.q_len + lane) * p.hq +
-                                  pc.g * p.group) * kHeadDim,
-                           (uint32_t)(p.group * kHeadDim * 2));
-        produce(cx, pc, gj0, smem, &tm_k, &tm_v);
-        last_loaded = gj0 + pc.n_tiles - 1;
-        gj0 += pc.n_tiles;
-        __syncwarp();
-      }
-      if (!ok) break;
-      int nx = pl.P + pl.R;
-      if (lane == 0 && pl.R > 0) nx = pl.P + atomicAdd(p.chunk_ctr, 1);
-      nx = __shfl_sync(0xffffffffu, nx, 0);
-      chunk = nx < pl.P + pl.R ? nx : -1;
-    }
-  } else if (warp != kWarpIdle) {
-    for (int idx = 0;; ++idx) {
-      const int rs = idx % kChunkRing;
-      Piece pc;
-      pc.b = -1;
-      if (lane == 0) {
-        if (wait_bar(cx, &bars.ch_full[rs], (idx / kChunkRing) & 1))
-          pc = s_piece[rs];
-        tc::bar_arrive(tc::smem_u32(&bars.ch_empty[rs]));
-      }
-      pc.b = __shfl_sync(0xffffffffu, pc.b, 0);
-      if (pc.b < 0) break;
-      pc.g = __shfl_sync(0xffffffffu, pc.g, 0);
-      pc.nt = __shfl_sync(0xffffffffu, pc.nt, 0);
-      pc.len = __shfl_sync(0xffffffffu, pc.len, 0);
-      pc.tok_begin = __shfl_sync(0xffffffffu, pc.tok_begin, 0);
-      pc.tok_end = __shfl_sync(0xffffffffu, pc.tok_end, 0);
-      pc.n_tiles = __shfl_sync(0xffffffffu, pc.n_tiles, 0);
-      pc.S = __shfl_sync(0xffffffffu, pc.S, 0);
-      pc.slot = __shfl_sync(0xffffffffu, pc.slot, 0);
-      pc.s0 = __shfl_sync(0xffffffffu, pc.s0, 0);
+  while (u < u_end) {
+    Piece pc;
+    pc.b = find_request(s_pre, p.batch, p.hkv, u);
+    const int ntv = s_pre[pc.b + 1] - s_pre[pc.b];  // virtual units
+    const long long rb = (long long)p.hkv * s_pre[pc.b];
+    pc.g = (int)((u - rb) / ntv);
+    const long long vs = rb + (long long)pc.g * ntv;
+    const int j0v = (int)(u - vs);
+    const int j1v = (int)(u_end - vs < ntv ? u_end - vs : ntv);
+    u = vs + j1v;
+    // real units of the piece; a range of phantom units only does nothing
+    const int j0 = max(j0v - kPieceCost, 0), j1 = max(j1v - kPieceCost, 0);
+    if (j1 <= j0) continue;  // the same decision in every warp
+    pc.nt = ntv - kPieceCost;
+    pc.s0 = vs + kPieceCost;  // the segment's first real unit
+    pc.len = clamp_len(p.seq_lens[pc.b], p.max_tokens);
+    pc.tok_begin = j0 * kUnit;
+    pc.tok_end = min(j1 * kUnit, pc.len);
+    pc.n_tiles = (pc.tok_end - pc.tok_begin + kTile - 1) / kTile;
 
-      // The dequant warps run ahead across pieces, gated by the ring and
-      // operand barriers; the MMA issuers and the softmax warps meet around
-      // each piece, so Q is rewritten only after the previous piece's last
-      // MMA and O^T is read before the next piece's first PV.
-      if (warp >= 4 && warp < 12) {
-        dequant_piece<NR>(cx, pc, gj0, smem, tmem, (warp - 4) >> 2);
-      } else {
-        if (warp < 4) load_q<NR>(p, pc, smem, red, pc.slot, pc.S);
-        tc::fence_before();
-        tc::bar_sync_named(1, kPieceThreads);
-        tc::fence_after();
-        if (warp == kWarpQK || warp == kWarpPV) {
-          if (lane == 0) {
-            if (warp == kWarpQK) qk_piece<NR>(cx, pc, gj0, tmem);
-            else pv_piece<NR>(cx, pc, gj0, tmem);
-          }
-          __syncwarp();
-        } else {
-          softmax_piece<NR>(cx, pc, gj0, tmem, smem, red, pc.slot, pc.S);
-        }
-        tc::fence_before();
-        tc::bar_sync_named(1, kPieceThreads);
-        tc::fence_after();
+    // The producer and the dequant warps run ahead across pieces, gated by
+    // the ring and operand barriers; the MMA issuer and the softmax warps
+    // meet around each piece, so Q is rewritten only after the previous
+    // piece's last MMA and O^T is read before the next piece's first PV.
+    if (warp == kWarpProducer) {
+      produce(cx, pc, gj0, smem, &tm_k, &tm_v);
+      last_loaded = gj0 + pc.n_tiles - 1;
+      __syncwarp();
+    } else if (warp >= 4 && warp < 12) {
+      dequant_piece<NR>(cx, pc, gj0, smem, tmem, (warp - 4) >> 2);
+    } else if (warp < 4 || warp == kWarpQK || warp == kWarpPV) {
+      int S = 0, slot = 0;
+      if (warp < 4) {
+        // where this piece's result goes
+        S = seg_splits(pl, pc.s0, pc.nt);
+        slot = S > 1 ? partial_slot(c, pc.b * p.hkv + pc.g) : 0;
+        load_q<NR>(p, pc, smem, red, slot, S);
       }
-      gj0 += pc.n_tiles;
+      tc::fence_before();
+      tc::bar_sync_named(1, kPieceThreads);
+      tc::fence_after();
+      if (warp == kWarpQK || warp == kWarpPV) {
+        if (lane == 0) {
+          if (warp == kWarpQK) qk_piece<NR>(cx, pc, gj0, tmem);
+          else pv_piece<NR>(cx, pc, gj0, tmem);
+        }
+        __syncwarp();
+      } else {
+        softmax_piece<NR>(cx, pc, gj0, tmem, smem, red, slot, S);
+      }
+      tc::fence_before();
+      tc::bar_sync_named(1, kPieceThreads);
+      tc::fence_after();
     }
+    gj0 += pc.n_tiles;
   }
 
   // teardown: no copy, bulk store or MMA may still be in flight

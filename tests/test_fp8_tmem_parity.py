@@ -121,30 +121,3 @@ def test_fp8_repeatable_and_independent_of_workspace():
     assert_attention_close(rows_of(a), oracle_attention(inp), True,
                            "fp8 garbage workspace")
 
-
-def test_fp8_dynamic_chunks_claimed_once_and_repeatable():
-    # enough KV (a plan of more than 32 x 4 x SMs 64-token units) that the
-    # last eighth of the work is cut into two chunks per CTA, claimed at
-    # run time by whichever CTA runs out of work first
-    prefixes = [int(x) for x in np.linspace(2000, 28000, 24)]
-    prefixes[3], prefixes[7] = 0, 5
-    inp = _case(prefixes, 2, 64, seed=2024)      # 12 rows: N = 16
-    ensure_built()
-    desc = sv.desc_for(inp["q"], inp["k_pages"], inp["page_table"])
-    ws = torch.full((sv.verify_workspace_size(desc),), 0xFF,
-                    dtype=torch.uint8, device=DEV)
-    outs = [gpu_attention(inp, workspace=ws) for _ in range(3)]
-    torch.cuda.synchronize()
-    # every CTA claims until the counter passes the last dynamic chunk: the
-    # counter ends at (dynamic chunks + one failed claim per CTA) = 3 x the
-    # CTAs that ran
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert int(ws[4:8].view(torch.int32).item()) == 3 * sms
-    # which CTA runs a dynamic chunk varies; what it computes does not
-    for o in outs[1:]:
-        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
-    chk = gpu_attention(inp, checked=True, workspace=ws)
-    assert sv.verify_status(ws) == 0
-    assert torch.equal(chk.view(torch.int16), outs[0].view(torch.int16))
-    assert_attention_close(rows_of(outs[0]), oracle_attention(inp), True,
-                           "fp8 dynamic chunks")
