@@ -46,6 +46,7 @@ struct AttnParams {
   int page_size, log2_ps, num_pages, max_pages;
   int max_tokens;     // max_pages * page_size: seq_lens clamp
   int grid;           // P: CTAs of the split kernel
+  int piece_cost;     // plan units charged per segment (<= kMaxPieceCost)
   int box_rows;       // TMA box height (tcgen05 kernel): min(page_size, 64)
   float scale_log2;   // softmax scale * log2(e)
 };
@@ -72,13 +73,21 @@ __device__ __forceinline__ int units_of(int len) {
 }
 
 // The plan runs on virtual units: every (request, KV head) segment is
-// charged kPieceCost units in front of its real ones, the fixed cost of a
-// piece (loading Q, the first tile's latency, the epilogue) in 64-token
-// tiles.  CTAs split the virtual units evenly and process the real units in
-// their range, so a CTA that starts a segment owns fewer real units.  In
-// virtual units segment (b, g) starts at hkv s_pre[b] + g nt'_b and its real
-// units at kPieceCost beyond that, nt'_b = s_pre[b+1] - s_pre[b].
-constexpr int kPieceCost = 3;
+// charged piece_cost units in front of its real ones, the fixed cost of a
+// piece (loading Q, the pipeline's fill and drain, the epilogue) in 64-token
+// units of that kernel's streaming time.  Every CTA pays for its first
+// piece; a CTA that crosses into a new segment pays for one more, and the
+// charge at the segment's start bills exactly those.  CTAs split the virtual
+// units evenly and process the real units in their range, so a CTA that
+// starts a segment owns fewer real units.  In virtual units segment (b, g)
+// starts at hkv s_pre[b] + g nt'_b and its real units at piece_cost beyond
+// that, nt'_b = s_pre[b+1] - s_pre[b].  Each kernel's cost was measured as
+// the time a piece boundary adds (clock64 timelines, and calls on equal
+// total KV cut into more or fewer segments).
+constexpr int kMaxPieceCost = 16;
+constexpr int kTcPieceCost = 3;     // bf16/FP8 tcgen05 kernel, Q in TMEM
+constexpr int kFp8tPieceCost = 14;  // FP8 kernel with K and V^T in TMEM
+constexpr int kMmaPieceCost = 3;    // mma.sync kernel (bf16, small pages)
 
 struct Plan {
   long long U;  // virtual units
@@ -101,7 +110,7 @@ __device__ __forceinline__ int seg_splits(const Plan& pl, long long s0, int nt) 
   return chunk_of(pl, s0 + nt - 1) - chunk_of(pl, s0) + 1;
 }
 
-// Exclusive prefix of virtual units per request (real units + kPieceCost)
+// Exclusive prefix of virtual units per request (real units + piece_cost)
 // into s_pre[0..batch] (s_pre[0] = 0).  Called by the whole block; ends
 // with __syncthreads().
 __device__ __forceinline__ void plan_prefix(const AttnParams& p, int* s_pre) {
@@ -112,7 +121,7 @@ __device__ __forceinline__ void plan_prefix(const AttnParams& p, int* s_pre) {
     for (int base = 0; base < p.batch; base += 32) {
       int b = base + lane;
       int v = b < p.batch
-                  ? units_of(clamp_len(p.seq_lens[b], p.max_tokens)) + kPieceCost
+                  ? units_of(clamp_len(p.seq_lens[b], p.max_tokens)) + p.piece_cost
                   : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {

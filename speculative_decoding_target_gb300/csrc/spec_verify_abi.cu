@@ -182,7 +182,7 @@ int check_desc(const spec_attn_desc* d) {
     return fail(SPEC_ERR_ARG, "max_pages_per_seq * page_size exceeds 2^30");
   const long long units = (long long)d->batch * d->num_kv_heads *
                           ((max_tokens + specv::kUnit - 1) / specv::kUnit +
-                           specv::kPieceCost);
+                           specv::kMaxPieceCost);
   if (units > (1LL << 30))
     return fail(SPEC_ERR_ARG, "batch * kv heads * units exceeds 2^30");
   if (d->batch * (long long)d->num_kv_heads > 65535)
@@ -313,6 +313,9 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
   p.max_pages = desc->max_pages_per_seq;
   p.max_tokens = desc->max_pages_per_seq * desc->page_size;
   p.grid = L.grid;
+  p.piece_cost = use_fp8t(desc) ? specv::kFp8tPieceCost
+                 : use_tc(desc) ? specv::kTcPieceCost
+                                : specv::kMmaPieceCost;
   p.box_rows = specv::verify_split_tc_box_rows(desc->page_size);
   p.scale_log2 = scale * 1.4426950408889634f;
   const bool tc = use_tc(desc);

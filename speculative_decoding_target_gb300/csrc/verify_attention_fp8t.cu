@@ -880,10 +880,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j1v = (int)(u_end - vs < ntv ? u_end - vs : ntv);
     u = vs + j1v;
     // real units of the piece; a range of phantom units only does nothing
-    const int j0 = max(j0v - kPieceCost, 0), j1 = max(j1v - kPieceCost, 0);
+    const int j0 = max(j0v - p.piece_cost, 0), j1 = max(j1v - p.piece_cost, 0);
     if (j1 <= j0) continue;  // the same decision in every warp
-    pc.nt = ntv - kPieceCost;
-    pc.s0 = vs + kPieceCost;  // the segment's first real unit
+    pc.nt = ntv - p.piece_cost;
+    pc.s0 = vs + p.piece_cost;  // the segment's first real unit
     pc.len = clamp_len(p.seq_lens[pc.b], p.max_tokens);
     pc.tok_begin = j0 * kUnit;
     pc.tok_end = min(j1 * kUnit, pc.len);

@@ -157,10 +157,10 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
     const int j1v = (int)(u_end - vs < ntv ? u_end - vs : ntv);
     u = vs + j1v;
     // real units of the piece; a range of phantom units only does nothing
-    const int j0 = max(j0v - kPieceCost, 0), j1 = max(j1v - kPieceCost, 0);
+    const int j0 = max(j0v - p.piece_cost, 0), j1 = max(j1v - p.piece_cost, 0);
     if (j1 <= j0) continue;  // uniform over the CTA
-    const int nt = ntv - kPieceCost;
-    const long long s0 = vs + kPieceCost;  // the segment's first real unit
+    const int nt = ntv - p.piece_cost;
+    const long long s0 = vs + p.piece_cost;  // the segment's first real unit
 
     const int len = clamp_len(p.seq_lens[b], p.max_tokens);
     const int qb = block_rows(p, b);
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
   const long long U = (long long)p.hkv * s_pre[p.batch];
   const int k = blockIdx.y, b = k / p.hkv, g = k - b * p.hkv;
   const int ntv = s_pre[b + 1] - s_pre[b];  // virtual units
-  const int nt = ntv - kPieceCost;           // real units
+  const int nt = ntv - p.piece_cost;           // real units
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pr = warp >> 1, odd = warp & 1;  // row of the block, half
   const int r = blockIdx.x * kMergeRowsPerBlock + pr;
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
   }
   const Plan pl = make_plan(p, U);
   const long long s0 =
-      (long long)p.hkv * s_pre[b] + (long long)g * ntv + kPieceCost;
+      (long long)p.hkv * s_pre[b] + (long long)g * ntv + p.piece_cost;
   const int S = seg_splits(pl, s0, nt);
   if (S <= 1) return;
   const int base = partial_slot(chunk_of(pl, s0), k);
