@@ -139,7 +139,12 @@ struct Bars {
   uint64_t v8_empty[kVStages]; // dequant warps done with the V slot
   uint64_t k_full;             // K tile written to TMEM
   uint64_t v_full[3];          // V^T slot written to TMEM
-  uint64_t v_empty[3];         // PV of the slot's 64 tokens complete
+  // PV of the slot's 64 tokens complete, one barrier per slot and dequant
+  // set: PV commits to the set that writes the slot next, so each barrier
+  // has one waiter that consumes every phase in order.  (A barrier shared
+  // by the two sets, which take alternate tiles, can be waited for a phase
+  // two ahead of it, which a parity wait mistakes for complete.)
+  uint64_t v_empty[3][2];
   uint64_t s_full[2];          // S^T_j complete (also: K tile free again)
   uint64_t p_full[2];          // P^T_j in shared memory (S^T_j consumed)
   uint64_t pv_done[2];         // O^T += V^T_j P^T_j complete
@@ -339,7 +344,8 @@ __device__ __forceinline__ uint32_t dup_half(uint32_t h16) {
 
 template <int NR>
 __device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
-                              uint8_t* smem, uint32_t tmem, int set) {
+                              uint8_t* smem, uint32_t tmem, int set,
+                              uint32_t& vpar) {
   constexpr int VS = Cols<NR>::kVSlots;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q4 = warp & 3;              // TMEM lane quarter of this warp
@@ -415,8 +421,12 @@ __device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
 #pragma unroll 1
     for (int sub = 0; sub < 2; ++sub) {
       const int u = 2 * gj + sub, slot = u % VS;
-      if (u >= VS)  // the slot's previous 64 tokens are through PV
-        wait_bar(cx, &cx.bars->v_empty[slot], ((u / VS) - 1) & 1);
+      if (u >= VS) {
+        // the slot's previous 64 tokens are through PV: this set's barrier
+        // of the slot, whose next parity is bit `slot` of vpar
+        wait_bar(cx, &cx.bars->v_empty[slot][set], (vpar >> slot) & 1u);
+        vpar ^= 1u << slot;
+      }
       tc::fence_after();
 #pragma unroll 1
       for (int hg = 0; hg < 4; ++hg) {
@@ -522,7 +532,8 @@ __device__ void pv_piece(const Ctx& cx, const Piece& pc, int gj0,
                 k > 0 ? 1u : acc0);
         }
       }
-      tc::commit(tc::smem_u32(&cx.bars->v_empty[slot]));
+      // the slot's next writer: occurrence u + VS, tile (u + VS) / 2
+      tc::commit(tc::smem_u32(&cx.bars->v_empty[slot][((u + C::kVSlots) >> 1) & 1]));
     }
     tc::commit(tc::smem_u32(&cx.bars->pv_done[gj & 1]));
   }
@@ -847,7 +858,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::bar_init(tc::smem_u32(&bars.k_full), 4);
     for (int s = 0; s < 3; ++s) {
       tc::bar_init(tc::smem_u32(&bars.v_full[s]), 4);
-      tc::bar_init(tc::smem_u32(&bars.v_empty[s]), 1);
+      tc::bar_init(tc::smem_u32(&bars.v_empty[s][0]), 1);
+      tc::bar_init(tc::smem_u32(&bars.v_empty[s][1]), 1);
     }
     for (int s = 0; s < 2; ++s) {
       tc::bar_init(tc::smem_u32(&bars.s_full[s]), 1);
@@ -869,6 +881,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long u_end = chunk_start(pl, c + 1);
   int gj0 = 0;
   int last_loaded = -1;  // last tile index the producer loaded
+  uint32_t vpar = 0;     // dequant warps: parities of their V^T-slot waits
   while (u < u_end) {
     Piece pc;
     pc.b = find_request(s_pre, p.batch, p.hkv, u);
@@ -898,7 +911,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       last_loaded = gj0 + pc.n_tiles - 1;
       __syncwarp();
     } else if (warp >= 4 && warp < 12) {
-      dequant_piece<NR>(cx, pc, gj0, smem, tmem, (warp - 4) >> 2);
+      dequant_piece<NR>(cx, pc, gj0, smem, tmem, (warp - 4) >> 2, vpar);
     } else if (warp < 4 || warp == kWarpQK || warp == kWarpPV) {
       int S = 0, slot = 0;
       if (warp < 4) {

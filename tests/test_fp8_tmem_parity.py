@@ -121,3 +121,18 @@ def test_fp8_repeatable_and_independent_of_workspace():
     assert_attention_close(rows_of(a), oracle_attention(inp), True,
                            "fp8 garbage workspace")
 
+
+
+def test_fp8_two_slot_instance_under_many_short_pieces():
+    # N = 64 keeps two V^T slots, so the two dequant warp sets, which take
+    # alternate tiles, write each slot in turn; many short pieces (short
+    # mixed-length requests over every SM) make one set run far ahead of
+    # the other's PV.  Each set waits on its own slot barriers, so no wait
+    # can be taken for a phase two ahead of the barrier.
+    g = torch.Generator().manual_seed(64)
+    prefixes = torch.randint(60, 900, (24,), generator=g).tolist()
+    for hq, q_len, ps in ((32, 8, 16), (24, 10, 64)):
+        inp = _case(prefixes, q_len, ps, hq=hq, seed=hq + q_len + ps)
+        out = gpu_attention(inp)
+        assert_attention_close(rows_of(out), oracle_attention(inp), True,
+                               f"two-slot instance Hq={hq} q_len={q_len}")
