@@ -373,20 +373,37 @@ def measure_e2e(args, w, inp, desc, attn_ws, acc_ws, out, stream, dev, ws_n,
     the cache state, not a per-step input."""
     from speculative_decoding_target_gb300 import _native
     keys = ("q", "page_table", "seq_lens", "logits", "draft_ids")
-    host = {k: inp[k].cpu().pin_memory() for k in keys}
-    dev_in = [{k: torch.empty_like(inp[k]) for k in keys} for _ in range(2)]
-    i32 = dict(dtype=torch.int32, device=dev)
-    dev_out = [dict(out=torch.empty_like(out),
-                    acc=torch.empty(w.batch, **i32),
-                    nxt=torch.empty(w.batch, **i32),
-                    toks=torch.empty((w.batch, w.q_len), **i32))
-               for _ in range(2)]
-    h_out = [dict(out=torch.empty(out.shape, dtype=out.dtype).pin_memory(),
-                  acc=torch.empty(w.batch, dtype=torch.int32).pin_memory(),
-                  nxt=torch.empty(w.batch, dtype=torch.int32).pin_memory(),
-                  toks=torch.empty((w.batch, w.q_len),
-                                   dtype=torch.int32).pin_memory())
-             for _ in range(2)]
+    # each direction is one contiguous staging buffer (tensors at 256-byte
+    # offsets), so a step costs one host-to-device and one device-to-host
+    # copy call whatever the number of tensors
+    in_specs = [(k, inp[k].dtype, tuple(inp[k].shape)) for k in keys]
+    out_specs = [("out", out.dtype, tuple(out.shape)),
+                 ("acc", torch.int32, (w.batch,)),
+                 ("nxt", torch.int32, (w.batch,)),
+                 ("toks", torch.int32, (w.batch, w.q_len))]
+
+    def packed(specs, device, pin):
+        offs, n = [], 0
+        for _, dt, shape in specs:
+            offs.append(n)
+            nb = torch.Size(shape).numel() * torch.empty((), dtype=dt).element_size()
+            n += (nb + 255) // 256 * 256
+        buf = torch.empty(n, dtype=torch.uint8, device=device)
+        if pin:
+            buf = buf.pin_memory()
+        views = {}
+        for (name, dt, shape), o in zip(specs, offs):
+            nb = torch.Size(shape).numel() * torch.empty((), dtype=dt).element_size()
+            views[name] = buf[o:o + nb].view(dt).view(shape)
+        return buf, views
+
+    h_in_buf, host = packed(in_specs, "cpu", True)
+    for k in keys:
+        host[k].copy_(inp[k].cpu())
+    dev_in_bufs, dev_in = zip(*[packed(in_specs, dev, False) for _ in range(2)])
+    dev_out_bufs, dev_out = zip(*[packed(out_specs, dev, False)
+                                  for _ in range(2)])
+    h_out_bufs, h_out = zip(*[packed(out_specs, "cpu", True) for _ in range(2)])
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
     s_in, s_back = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -401,8 +418,7 @@ def measure_e2e(args, w, inp, desc, attn_ws, acc_ws, out, stream, dev, ws_n,
         with torch.cuda.stream(s_in):
             if used[b]:
                 s_in.wait_event(computed[b])  # the set's last reader is done
-            for name, t in host.items():
-                dev_in[b][name].copy_(t, non_blocking=True)
+            dev_in_bufs[b].copy_(h_in_buf, non_blocking=True)
             copied[b].record(s_in)
 
     def compute(k):
@@ -424,8 +440,7 @@ def measure_e2e(args, w, inp, desc, attn_ws, acc_ws, out, stream, dev, ws_n,
         b = k & 1
         with torch.cuda.stream(s_back):
             s_back.wait_event(computed[b])
-            for name, t in h_out[b].items():
-                t.copy_(dev_out[b][name], non_blocking=True)
+            h_out_bufs[b].copy_(dev_out_bufs[b], non_blocking=True)
             read[b].record(s_back)
 
     def run(n, start_ev=None):
@@ -456,8 +471,9 @@ def measure_e2e(args, w, inp, desc, attn_ws, acc_ws, out, stream, dev, ws_n,
             "note": "KV pool resident in HBM (it is the cache state); every "
                     "step copies its q, page table, seq_lens, logits and "
                     "drafts in from pinned host memory and its out / "
-                    "accept / next / tokens back, double-buffered so that "
-                    "copies overlap the previous step's kernels"}
+                    "accept / next / tokens back (one staging buffer per "
+                    "direction), double-buffered so that copies overlap "
+                    "the previous step's kernels"}
 
 
 # ------------------------------------------------------ block KV append --
