@@ -2,19 +2,27 @@
 """Benchmark of the target-verify step: paged GQA verify attention followed
 by greedy acceptance, on seeded synthetic inputs, through the C ABI.
 
-One step = spec_verify_attention (split-KV kernel + LSE merge) over every
-request's verify block, then spec_greedy_accept over the block's logits.
-Default workload: batch 8, q_len 8, 24/4 heads, head_dim 256, 32,768-token
-prefixes in 64-token pages of a permuted pool, bf16 KV; logits
-[64 x 248,320] fp32 with drafts planted at p = 0.6.
+One step = spec_verify_attention over every request's verify block, then
+spec_greedy_accept over the block's logits.
+
+Headline workload (the largest, long-context configuration): batch 4, q_len
+8, 24/4 heads, head_dim 256, 524,288-token prefixes in 64-token pages of a
+permuted pool, bf16 KV (8.59 GB read per step); logits [32 x 248,320] fp32
+with drafts planted at p = 0.5.  The same run times the four other verify
+configurations (the "configs" key), each with its own roofline block: the
+batch-1 4K-token and 256K-token cases both with a 512 MB L2 flush before
+every step ("cold") and back to back ("warm"), the others (inputs larger
+than L2) back to back.
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own
-replica of the workload on its own GPU (the step has no cross-GPU exchange),
-timing is the max over ranks, and value counts the steps of all ranks.
+replica of the headline workload on its own GPU (the step has no cross-GPU
+exchange), timing is the max over ranks, and value counts the steps of all
+ranks; only rank 0 times the other configurations.
 
 --impl reference times the CPU float64 oracle on the host cores instead
-(rank 0 only), on a bounded sample of rows per step, extrapolated to the
-whole workload.
+(rank 0 only): the K timed steps each compute a different 1/K of the
+headline workload's attention rows and accept requests, so that together
+they compute one whole verify step; value is whole steps per second.
 """
 from __future__ import annotations
 
@@ -38,24 +46,31 @@ from speculative_decoding_target_gb300 import workloads as wl  # noqa: E402
 METRIC = ("verify steps/s and KV-read GB/s (fraction of GB300 HBM peak) at "
           "1 GPU")
 UNIT = "steps/s"
-DEFAULT_WORKLOAD = "b8_q8_p32k"
-KERNEL_LAUNCHES_PER_STEP = 3   # split, merge, argmax (its last CTA per request finalises)
+DEFAULT_WORKLOAD = "b4_q8_p512k"
+# our kernels per verify step: the split-KV attention kernel, the LSE merge
+# kernel, the argmax/accept kernel (its last CTA per request finalises)
+KERNEL_LAUNCHES_PER_STEP = 3
+L2_FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 << 20           # GB300 L2 (upper bound used for labels)
+# configurations timed cold (L2 flushed before each step) and warm
+COLD_AND_WARM = ("b1_q8_p4k_ps16", "b1_q16_p256k")
 
-# DRAM traffic of one launch of the dominant kernel (the split-KV attention
-# kernel), dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture
-# (profiles/verify_split_*.md), keyed by workload and valid only while that
-# kernel's sources still hash to the recorded value.
+# DRAM traffic of the dominant kernel (the split-KV attention kernel):
+# dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture, per
+# algorithmic KV byte, keyed by the kernel and valid only while that
+# kernel's sources still hash to the recorded value.  A workload other than
+# the captured one gets the capture's bytes scaled by its algorithmic bytes
+# (the traffic follows them: every KV byte is read once, and the partials
+# are a small fixed share).
 NCU_TRAFFIC = {
-    "b8_q8_p32k": {"kernel": "tc", "source_hash": "82f85a10d3d072aa",
-                   "bytes_per_launch": 1077388032 + 4466944},
-    # captured on the smaller FP8 case b8_q8_p16k_fp8 (276.95 MB
-    # algorithmic: 279.21 MB read + 4.59 MB written) and scaled to a full
-    # launch by the algorithmic bytes, which the traffic follows
-    "b32_q8_p1k128k_fp8": {"kernel": "fp8t", "source_hash": "70ac74e863844017",
-                           "per_algorithmic_byte": (279210496 + 4592896)
-                           / (8 * 16392 * 4 * 528)},
+    "tc": {"source_hash": "82f85a10d3d072aa", "captured_on": "b8_q8_p32k",
+           "read": 1077388032, "write": 4466944,
+           "algorithmic": 1074003968},
+    "fp8t": {"source_hash": "70ac74e863844017",
+             "captured_on": "b8_q8_p16k_fp8",
+             "read": 279210496, "write": 4592896,
+             "algorithmic": 8 * 16392 * 4 * 528},
 }
-NCU_TRAFFIC["b8_q8_p16k_fp8"] = NCU_TRAFFIC["b32_q8_p1k128k_fp8"]
 
 # Sources of each split kernel: bf16 KV and FP8 blocks of more than 64 rows
 # per KV head take the tcgen05 kernel with Q in tensor memory; FP8 blocks of
@@ -79,6 +94,19 @@ def kernel_source_hash(kind: str = "tc") -> str:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def traffic_per_launch(w, kv_b: int):
+    """ncu DRAM bytes of one split-kernel launch on workload w (None when
+    the kernel changed since the capture)."""
+    kind = split_kernel_of(w)
+    rec = NCU_TRAFFIC.get(kind)
+    if not rec or rec["source_hash"] != kernel_source_hash(kind):
+        return None, None
+    per = (rec["read"] + rec["write"]) / rec["algorithmic"]
+    how = ("captured on this workload" if rec["captured_on"] == w.name else
+           f"captured on {rec['captured_on']}, scaled by algorithmic bytes")
+    return int(round(per * kv_b)), how
 
 
 def measured_peaks():
@@ -174,17 +202,211 @@ def job_throughput(world: int, steps: int, elapsed_ms: float) -> float:
     return world * steps / (elapsed_ms / 1e3)
 
 
-def algorithmic_bytes(w: wl.VerifyWorkload, seq_lens):
+def algorithmic_bytes(w: wl.VerifyWorkload, seq_lens=None):
+    if seq_lens is None:
+        seq_lens = [p + w.q_len for p in wl.prefix_lengths(w)]
     kv = wl.kv_bytes(seq_lens, w.num_kv_heads, w.head_dim, w.kv_dtype)
     logits = w.batch * w.q_len * w.vocab * 4
     return kv, logits
 
 
+def config_of(w: wl.VerifyWorkload, ws_n: int, graph: bool = False) -> dict:
+    """The workload description both arms print (identical dicts)."""
+    kv_b, logit_b = algorithmic_bytes(w)
+    return {
+        "workload": w.name, "batch": w.batch, "q_len": w.q_len,
+        "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+        "head_dim": w.head_dim, "prefix": w.prefix or "U[1024,131072]",
+        "page_size": w.page_size, "kv_dtype": w.kv_dtype,
+        "vocab": w.vocab, "accept_p": w.accept_p, "seed": w.seed,
+        "kv_bytes_per_step": kv_b, "logits_bytes_per_step": logit_b,
+        "l2": (f"inputs larger than L2 ({(kv_b + logit_b) / 1e9:.3f} GB "
+               "read per step), no flush" if kv_b + logit_b > L2_BYTES else
+               f"inputs fit in L2 ({(kv_b + logit_b) / 1e9:.3f} GB read per "
+               "step), steps back to back, no flush (warm)"),
+        "parallelism": f"replicas x{ws_n}",
+        "cuda_graph": bool(graph),
+    }
+
+
+def accept_statistics(accept_len, w: wl.VerifyWorkload) -> dict:
+    """Mean accepted drafts and per-position survival of the synthetic
+    logits.  Survival at position j is the share of requests that accepted
+    at least j drafts; the survival rates sum to the mean accepted length
+    ("Laguna S 2.1 DFlash accepting and FP8-KV result", acceptance and
+    per-position survival).  Drafts are planted independently with
+    probability p, so the expected accepted length is sum_j p^j."""
+    a = [int(x) for x in accept_len]
+    k = w.q_len - 1
+    n = max(1, len(a))
+    survival = [sum(1 for x in a if x >= j) / n for j in range(1, k + 1)]
+    mean = sum(a) / n
+    return {
+        "requests": len(a), "mean_accept": round(mean, 6),
+        "survival": [round(x, 6) for x in survival],
+        "survival_sum": round(sum(survival), 6),
+        "survival_sum_equals_mean": abs(sum(survival) - mean) < 1e-9,
+        "expected_mean_accept": round(sum(w.accept_p ** j
+                                          for j in range(1, k + 1)), 6),
+        "commit_tokens_mean": round(mean + 1, 6),
+    }
+
+
+def tensor_digest(t) -> str:
+    """sha256 of a tensor's bytes (small tensors), or of the int64 sums of
+    its 32-bit words in 64 MiB chunks, computed where the tensor lives."""
+    if t is None:
+        return None
+    b = t.detach().contiguous().view(-1).view(torch.uint8)
+    h = hashlib.sha256()
+    if b.numel() <= (64 << 20):
+        h.update(b.cpu().numpy().tobytes())
+        return h.hexdigest()[:16]
+    words = b[: b.numel() // 4 * 4].view(torch.int32)
+    chunk = 1 << 24
+    full = words.numel() // chunk * chunk
+    sums = words[:full].view(-1, chunk).sum(dim=1, dtype=torch.int64)
+    h.update(sums.cpu().numpy().tobytes())
+    h.update(words[full:].cpu().numpy().tobytes())
+    h.update(b[words.numel() * 4:].cpu().numpy().tobytes())
+    return "sum:" + h.hexdigest()[:16]
+
+
+def input_digests(inp) -> dict:
+    keys = ("q", "k_pages", "v_pages", "k_scales", "v_scales", "page_table",
+            "seq_lens", "logits", "draft_ids")
+    return {k: tensor_digest(inp.get(k)) for k in keys if inp.get(k) is not None}
+
+
 # ----------------------------------------------------------------- GPU arm --
+
+class VerifyStep:
+    """Buffers and the step function of one workload on one device."""
+
+    def __init__(self, w: wl.VerifyWorkload, inp: dict, dev):
+        import speculative_decoding_target_gb300 as sv
+        self.w, self.inp, self.dev = w, inp, dev
+        self.desc = sv.desc_for(inp["q"], inp["k_pages"], inp["page_table"])
+        self.attn_ws = sv.alloc_workspace(sv.verify_workspace_size(self.desc),
+                                          dev)
+        rows = w.batch * w.q_len
+        self.acc_ws = sv.alloc_workspace(
+            sv.accept_workspace_size(rows, w.vocab), dev)
+        self.out = torch.empty_like(inp["q"])
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.acc = torch.empty(w.batch, **i32)
+        self.nxt = torch.empty(w.batch, **i32)
+        self.toks = torch.empty((w.batch, w.q_len), **i32)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def attention(self, stream=None):
+        from speculative_decoding_target_gb300 import _native
+        i = self.inp
+        _native.verify_attention_into(
+            self.desc, i["q"], i["k_pages"], i["v_pages"], i["k_scales"],
+            i["v_scales"], i["page_table"], i["seq_lens"], i["scale"],
+            self.out, self.attn_ws, stream or self.stream)
+
+    def accept(self, stream=None):
+        from speculative_decoding_target_gb300 import _native
+        _native.greedy_accept_into(self.inp["logits"], self.inp["draft_ids"],
+                                   self.acc, self.nxt, self.toks, self.acc_ws,
+                                   stream or self.stream)
+
+    def step(self, ev=None):
+        if ev is not None:
+            ev[0].record(self.stream)
+        self.attention()
+        if ev is not None:
+            ev[1].record(self.stream)
+        self.accept()
+        if ev is not None:
+            ev[2].record(self.stream)
+
+    def timed(self, steps: int, flush=None):
+        """Per-step (attention ms, accept ms, step ms) lists and the total
+        ms of the loop.  With `flush` (a device buffer larger than L2) the
+        buffer is rewritten before every step, outside its events."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+               for _ in range(steps)]
+        torch.cuda.synchronize(self.dev)
+        for k in range(steps):
+            if flush is not None:
+                flush.fill_(k & 0xFF)
+            self.step(evs[k])
+        torch.cuda.synchronize(self.dev)
+        attn = [e[0].elapsed_time(e[1]) for e in evs]
+        acc = [e[1].elapsed_time(e[2]) for e in evs]
+        step = [e[0].elapsed_time(e[2]) for e in evs]
+        total = evs[0][0].elapsed_time(evs[-1][2])
+        return attn, acc, step, total
+
+
+def roofline_block(w, kv_b: int, attn_ms: float, peak: float,
+                   peak_kind: str) -> dict:
+    achieved = kv_b / (attn_ms * 1e-3) / 1e9
+    traffic, how = traffic_per_launch(w, kv_b)
+    blk = {
+        "kernel": "verify attention (split-KV kernel + LSE merge, one C-ABI "
+                  "call)",
+        "split_kernel": split_kernel_of(w),
+        "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+        "peak_kind": peak_kind, "unit": "GB/s",
+        "frac": round(achieved / peak, 4), "traffic": traffic,
+        "algorithmic_bytes_per_launch": kv_b,
+        "avg_launch_ms": round(attn_ms, 5),
+    }
+    if how:
+        blk["traffic_note"] = how
+    return blk
+
+
+def measure_config(w: wl.VerifyWorkload, dev, steps: int, warmup: int,
+                   peak: float, peak_kind: str, flush) -> dict:
+    """Time one more configuration in the same run (rank 0): attention,
+    accept and the whole step, cold (L2 flushed before each step) and warm
+    for the batch-1 cases, back to back for the others."""
+    inp = wl.workload_inputs(w, device=dev)
+    vs = VerifyStep(w, inp, dev)
+    for _ in range(warmup):
+        vs.step()
+    kv_b, logit_b = algorithmic_bytes(w, inp["seq_lens"].tolist())
+    modes = ("cold", "warm") if w.name in COLD_AND_WARM else ("large",)
+    rec = {"workload": w.name, "batch": w.batch, "q_len": w.q_len,
+           "prefix": w.prefix or "U[1024,131072]", "page_size": w.page_size,
+           "kv_dtype": w.kv_dtype, "seed": w.seed,
+           "kv_bytes_per_step": kv_b, "logits_bytes_per_step": logit_b}
+    for mode in modes:
+        attn, acc, step, total = vs.timed(
+            steps, flush if mode == "cold" else None)
+        a, c = statistics.mean(attn), statistics.mean(acc)
+        st = statistics.mean(step) if mode == "cold" else total / steps
+        rec[mode] = {
+            "l2": {"cold": f"{L2_FLUSH_BYTES >> 20} MB written before every "
+                           "step, outside its events",
+                   "warm": "steps back to back, no flush (KV and logits "
+                           "partly or wholly L2-resident)",
+                   "large": "inputs larger than L2, steps back to back, no "
+                            "flush"}[mode],
+            "steps_per_s": round(1e3 / st, 3), "step_ms": round(st, 5),
+            "attention_ms": round(a, 5), "accept_ms": round(c, 5),
+            "kv_read_gbs": round(kv_b / (a * 1e-3) / 1e9, 1),
+            "frac": round(kv_b / (a * 1e-3) / 1e9 / peak, 4),
+            "logits_gbs": round(logit_b / (c * 1e-3) / 1e9, 1),
+        }
+    main_mode = modes[0]
+    rec["roofline"] = roofline_block(w, kv_b, rec[main_mode]["attention_ms"],
+                                     peak, peak_kind)
+    rec["roofline"]["l2"] = main_mode
+    rec["acceptance"] = accept_statistics(vs.acc.cpu().tolist(), w)
+    rec["input_digest"] = input_digests(inp)
+    rec["gpu_launches"] = KERNEL_LAUNCHES_PER_STEP * (steps * len(modes) +
+                                                      warmup)
+    return rec, inp
+
 
 def run_gpu(args, w: wl.VerifyWorkload):
     import speculative_decoding_target_gb300 as sv
-    from speculative_decoding_target_gb300 import _native
 
     ws_n, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -196,69 +418,47 @@ def run_gpu(args, w: wl.VerifyWorkload):
 
     inp = wl.workload_inputs(w, device=dev)
     seq_lens = inp["seq_lens"].tolist()
-    desc = sv.desc_for(inp["q"], inp["k_pages"], inp["page_table"])
-    attn_ws = sv.alloc_workspace(sv.verify_workspace_size(desc), dev)
-    rows = w.batch * w.q_len
-    acc_ws = sv.alloc_workspace(sv.accept_workspace_size(rows, w.vocab), dev)
-    out = torch.empty_like(inp["q"])
-    acc = torch.empty(w.batch, dtype=torch.int32, device=dev)
-    nxt = torch.empty(w.batch, dtype=torch.int32, device=dev)
-    toks = torch.empty((w.batch, w.q_len), dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step(ev_a=None, ev_b=None):
-        if ev_a is not None:
-            ev_a.record(stream)
-        _native.verify_attention_into(
-            desc, inp["q"], inp["k_pages"], inp["v_pages"], inp["k_scales"],
-            inp["v_scales"], inp["page_table"], inp["seq_lens"], inp["scale"],
-            out, attn_ws, stream)
-        if ev_b is not None:
-            ev_b.record(stream)
-        _native.greedy_accept_into(inp["logits"], inp["draft_ids"], acc, nxt,
-                                   toks, acc_ws, stream)
+    vs = VerifyStep(w, inp, dev)
+    stream = vs.stream
 
     def barrier():
         if ws_n > 1:
             import torch.distributed as dist
             dist.barrier()
 
+    step = vs.step
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     if args.graph:
         # one CUDA graph per C-ABI call, replayed in the timed loop: the
         # same kernels without the per-call host overhead
-        eager_step = step
         g_attn, g_acc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         with torch.cuda.stream(side):
             with torch.cuda.graph(g_attn, stream=side):
-                _native.verify_attention_into(
-                    desc, inp["q"], inp["k_pages"], inp["v_pages"],
-                    inp["k_scales"], inp["v_scales"], inp["page_table"],
-                    inp["seq_lens"], inp["scale"], out, attn_ws, side)
+                vs.attention(side)
             with torch.cuda.graph(g_acc, stream=side):
-                _native.greedy_accept_into(inp["logits"], inp["draft_ids"],
-                                           acc, nxt, toks, acc_ws, side)
+                vs.accept(side)
         torch.cuda.synchronize(dev)
 
-        def step(ev_a=None, ev_b=None):
-            if ev_a is not None:
-                ev_a.record(stream)
+        def step(ev=None):
+            if ev is not None:
+                ev[0].record(stream)
             g_attn.replay()
-            if ev_b is not None:
-                ev_b.record(stream)
+            if ev is not None:
+                ev[1].record(stream)
             g_acc.replay()
+            if ev is not None:
+                ev[2].record(stream)
 
         for _ in range(args.warmup):
             step()
         torch.cuda.synchronize(dev)
-        del eager_step
 
-    evs = [(torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+           for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -268,33 +468,28 @@ def run_gpu(args, w: wl.VerifyWorkload):
     torch.cuda.synchronize(dev)
     t0.record(stream)
     for k in range(args.steps):
-        step(*evs[k])
+        step(evs[k])
     t1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
-    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    acc_ms = [e[1].elapsed_time(e[2]) for e in evs]
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     # end to end through the public API with host buffers: every step copies
     # its inputs from pinned host memory and reads its results back
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(args, w, inp, desc, attn_ws, acc_ws, out, stream,
-                          dev, ws_n, barrier)
+        e2e = measure_e2e(args, w, inp, vs.desc, vs.attn_ws, vs.acc_ws,
+                          vs.out, stream, dev, ws_n, barrier)
 
     kv_b, logit_b = algorithmic_bytes(w, seq_lens)
-    attn_avg_s = statistics.mean(attn_ms) / 1e3
+    attn_avg_ms = statistics.mean(attn_ms)
+    acc_avg_ms = statistics.mean(acc_ms)
     peak, peak_kind = measured_peaks()
-    achieved = kv_b / attn_avg_s / 1e9
-    src_hash = kernel_source_hash(split_kernel_of(w))
-    traffic = None
-    rec = NCU_TRAFFIC.get(w.name)
-    if rec and rec.get("source_hash") == src_hash:
-        traffic = rec.get("bytes_per_launch")
-        if traffic is None:
-            traffic = int(rec["per_algorithmic_byte"] * kv_b)
+    roof = roofline_block(w, kv_b, attn_avg_ms, peak, peak_kind)
     result = {
         "metric": METRIC,
         "value": round(job_throughput(ws_n, args.steps, elapsed_ms), 3),
@@ -309,52 +504,69 @@ def run_gpu(args, w: wl.VerifyWorkload):
         "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8_e4m3",
         "data": "synthetic (seeded; random bf16 Q/K/V ~N(0,1), fp32 logits "
                 "~N(0,4), planted drafts)",
-        "config": {
-            "workload": w.name, "batch": w.batch, "q_len": w.q_len,
-            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
-            "head_dim": w.head_dim, "prefix": w.prefix or "U[1024,131072]",
-            "page_size": w.page_size, "kv_dtype": w.kv_dtype,
-            "vocab": w.vocab, "accept_p": w.accept_p,
-            "kv_bytes_per_step": kv_b, "logits_bytes_per_step": logit_b,
-            "l2": f"inputs larger than L2 ({(kv_b + logit_b) / 1e9:.3f} GB "
-                  "read per step), no flush",
-            "parallelism": f"replicas x{ws_n}",
-            "cuda_graph": bool(args.graph),
-        },
-        "kv_read_gbs": round(achieved, 1),
-        "roofline": {
-            "kernel": "verify attention (split-KV kernel + LSE merge, one "
-                      "C-ABI call)",
-            "bound": "hbm", "achieved": round(achieved, 1),
-            "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": traffic,
-            "algorithmic_bytes_per_launch": kv_b,
-            "avg_launch_ms": round(attn_avg_s * 1e3, 5),
-        },
+        "config": config_of(w, ws_n, args.graph),
+        "kv_read_gbs": roof["achieved"],
+        "accept_ms": round(acc_avg_ms, 5),
+        "logits_gbs": round(logit_b / (acc_avg_ms * 1e-3) / 1e9, 1),
+        "roofline": roof,
         "gpu_launches": KERNEL_LAUNCHES_PER_STEP * args.steps,
-        "kernel_source_hash": src_hash,
+        "kernel_source_hash": kernel_source_hash(split_kernel_of(w)),
         "clocks": clk,
     }
     if e2e is not None:
         result["e2e"] = e2e
-    if not args.no_append:
-        result["kv_append"] = measure_kv_append(w, dev, args.steps,
-                                                args.warmup)
-    if not args.no_ragged:
-        result["ragged"] = measure_ragged(w, inp, dev, args.steps,
-                                          args.warmup, attn_avg_s)
-    if not args.no_stochastic:
-        result["stochastic"] = measure_stochastic(w, inp, dev, args.steps,
-                                                  args.warmup, peak)
-    if not args.no_select:
-        result["dflash2_select"] = measure_select(w, dev, args.steps,
-                                                  args.warmup, peak)
+    result["acceptance"] = accept_statistics(vs.acc.cpu().tolist(), w)
+    result["input_digest"] = input_digests(inp)
+    host_inp = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         host_inp = {k: (v.cpu() if torch.is_tensor(v) else v)
                     for k, v in inp.items()}
+    if not args.main_only and rank == 0:
+        del vs
+        inp = None
+        torch.cuda.empty_cache()
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        configs = {}
+        extras_w = wl.WORKLOADS[args.extras_workload]
+        extras_inp = None
+        for name in wl.WORKLOAD_ORDER:
+            if name == w.name:
+                continue
+            cw = wl.WORKLOADS[name]
+            rec, cinp = measure_config(cw, dev, args.steps, args.warmup,
+                                       peak, peak_kind, flush)
+            configs[name] = rec
+            if name == extras_w.name:
+                extras_inp = cinp
+            del cinp
+            torch.cuda.empty_cache()
+        result["configs"] = configs
+        if extras_inp is None and extras_w.name == w.name:
+            extras_inp = wl.workload_inputs(w, device=dev)
+        ex = {"workload": extras_w.name}
+        if not args.no_append:
+            ex["kv_append"] = measure_kv_append(extras_w, dev, args.steps,
+                                                args.warmup)
+        if not args.no_ragged:
+            full = configs.get(extras_w.name, {}).get("large", {}).get(
+                "attention_ms")
+            ex["ragged"] = measure_ragged(extras_w, extras_inp, dev,
+                                          args.steps, args.warmup, full)
+        if not args.no_stochastic:
+            ex["stochastic"] = measure_stochastic(extras_w, extras_inp, dev,
+                                                  args.steps, args.warmup,
+                                                  peak)
+        if not args.no_select:
+            ex["dflash2_select"] = measure_select(extras_w, dev, args.steps,
+                                                  args.warmup, peak)
+        result["next_rows"] = ex
+        del extras_inp
+        torch.cuda.empty_cache()
+    if host_inp is not None:
         result["cpu_baseline"] = cpu_baseline(w, host_inp, args.cpu_seconds)
     if ws_n > 1:
         import torch.distributed as dist
+        dist.barrier()
         dist.destroy_process_group()
     return result, rank
 
@@ -552,7 +764,7 @@ def measure_kv_append(w: wl.VerifyWorkload, dev, iters: int, warmup: int):
 # ------------------------------------------------ per-request verify widths --
 
 def measure_ragged(w: wl.VerifyWorkload, inp, dev, steps: int, warmup: int,
-                   full_attn_s: float):
+                   full_attn_ms=None):
     """One verify step with per-request widths q_b ~ U[1, q_len] (seeded):
     attention over the padded block, accept with commit lengths (only the
     q_b logits rows of each request are read), and the next block's
@@ -619,7 +831,8 @@ def measure_ragged(w: wl.VerifyWorkload, inp, dev, steps: int, warmup: int,
                   "EWMA policy prepares the next block",
         "mean_width": round(rows / w.batch, 3),
         "attention_ms": round(part[0], 5),
-        "attention_full_width_ms": round(full_attn_s * 1e3, 5),
+        "attention_full_width_ms": (None if full_attn_ms is None
+                                    else round(full_attn_ms, 5)),
         "accept_commit_ms": round(part[1], 5),
         "logits_bytes_read": rows * w.vocab * 4,
         "prepare_ms": round(part[2], 5),
@@ -764,92 +977,120 @@ def measure_select(w: wl.VerifyWorkload, dev, steps: int, warmup: int,
 
 # ----------------------------------------------------------- CPU baseline --
 
-def _oracle_step_estimate(w, host_inp, n_rows: int, n_acc_rows: int, rng):
-    """Time the oracle on n_rows attention rows and n_acc_rows accept rows;
-    return the extrapolated seconds of one full step."""
+def _oracle_rows(w, host_inp, rows):
+    """The oracle's attention over the given flat rows (b*q_len + i)*Hq + h."""
     import oracle
     bits = wl.to_numpy_bits
-    total_rows = w.batch * w.q_len * w.num_q_heads
-    rows = np.sort(rng.choice(total_rows, size=min(n_rows, total_rows),
-                              replace=False)).astype(np.int64)
     fp8 = host_inp["k_scales"] is not None
-    args = (bits(host_inp["q"]), bits(host_inp["k_pages"]),
-            bits(host_inp["v_pages"]), host_inp["page_table"].numpy(),
-            host_inp["seq_lens"].numpy())
-    t = time.perf_counter()
-    oracle.verify_attention(
-        *args, num_kv_heads=w.num_kv_heads, scale=host_inp["scale"],
+    return oracle.verify_attention(
+        bits(host_inp["q"]), bits(host_inp["k_pages"]),
+        bits(host_inp["v_pages"]), host_inp["page_table"].numpy(),
+        host_inp["seq_lens"].numpy(), num_kv_heads=w.num_kv_heads,
+        scale=host_inp["scale"],
         k_scales=bits(host_inp["k_scales"]) if fp8 else None,
-        v_scales=bits(host_inp["v_scales"]) if fp8 else None, rows=rows)
-    t_attn = time.perf_counter() - t
-    acc_total = w.batch * w.q_len
-    nb = max(1, min(w.batch, n_acc_rows // w.q_len))
-    lg = host_inp["logits"].numpy()[:nb * w.q_len]
-    dr = host_inp["draft_ids"].numpy()[:nb]
-    t = time.perf_counter()
-    oracle.greedy_accept(lg, dr)
-    t_acc = time.perf_counter() - t
-    return (t_attn * total_rows / rows.size
-            + t_acc * acc_total / (nb * w.q_len)), rows.size, nb * w.q_len
+        v_scales=bits(host_inp["v_scales"]) if fp8 else None,
+        rows=np.asarray(rows, np.int64))
+
+
+def _oracle_accept(w, host_inp, requests):
+    import oracle
+    if len(requests) == 0:
+        return
+    lo, hi = int(requests[0]), int(requests[-1]) + 1
+    lg = host_inp["logits"].numpy()[lo * w.q_len:hi * w.q_len]
+    oracle.greedy_accept(lg, host_inp["draft_ids"].numpy()[lo:hi])
 
 
 def cpu_baseline(w, host_inp, budget_s: float):
+    """The oracle as it stands on a bounded sample of one step: a growing
+    random sample of attention rows (and the accept of a proportional share
+    of the requests) until about budget_s seconds are spent, extrapolated to
+    the whole step by row count."""
     import oracle
     rng = np.random.default_rng(w.seed)
-    n = 8
-    t0 = time.perf_counter()
+    total = w.batch * w.q_len * w.num_q_heads
+    perm = rng.permutation(total)
+    n, spent, t_rows, n_done = 8, 0.0, 0.0, 0
     while True:
-        est, nr, na = _oracle_step_estimate(w, host_inp, n, 2 * w.q_len, rng)
-        spent = time.perf_counter() - t0
-        total = w.batch * w.q_len * w.num_q_heads
-        if spent > budget_s / 3 or nr >= total:
+        rows = np.sort(perm[n_done:n_done + n])
+        t = time.perf_counter()
+        _oracle_rows(w, host_inp, rows)
+        dt = time.perf_counter() - t
+        t_rows += dt
+        n_done += rows.size
+        spent += dt
+        per_row = t_rows / n_done
+        left = total - n_done
+        if left == 0 or spent + per_row * min(left, 4 * n) > budget_s:
             break
-        n = min(total, n * 4)
+        n = min(left, 4 * n)
+    nreq = max(1, round(w.batch * n_done / total))
+    t = time.perf_counter()
+    _oracle_accept(w, host_inp, np.arange(nreq))
+    t_acc = time.perf_counter() - t
+    est = per_row * total + t_acc * w.batch / nreq
     return {"value": round(1.0 / est, 6), "unit": UNIT,
             "cores": oracle.default_threads(), "kind": "oracle",
-            "sample": f"{nr} of {w.batch * w.q_len * w.num_q_heads} attention "
-                      f"rows and {na} of {w.batch * w.q_len} logits rows of "
-                      f"one step, extrapolated by row count "
-                      f"({spent:.1f} s of CPU time)"}
+            "sample": f"{n_done} of {total} attention rows (random) and the "
+                      f"accept of {nreq} of {w.batch} requests of one step, "
+                      f"extrapolated by row count ({spent + t_acc:.1f} s of "
+                      f"oracle time)"}
 
 
 # ------------------------------------------------------- reference arm --
 
 def run_reference(args, w):
+    """The CPU float64 oracle as the reference arm.  The K timed steps each
+    compute a different 1/K of the workload's attention rows and accept
+    requests (contiguous slices), so together they compute one whole verify
+    step: ms_per_step is the time of one slice, value is whole verify steps
+    per second (1 / the sum of the K slice times).  Warm-up steps compute a
+    few rows each.  Inputs are drawn on the host with the workload's recipe
+    and seed (the random values differ from the device-side draw)."""
     ws_n, rank, _ = dist_env()
     if rank != 0:
         return None, rank
     import oracle
-    host_inp = wl.workload_inputs(w, device="cpu")
-    rng = np.random.default_rng(w.seed + 1)
-    n_rows = max(1, args.ref_rows)
-    for _ in range(args.warmup):
-        _oracle_step_estimate(w, host_inp, n_rows, w.q_len, rng)
-    ests = []
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        est, nr, na = _oracle_step_estimate(w, host_inp, n_rows, w.q_len, rng)
-        ests.append(est)
-    spent = time.perf_counter() - t0
-    value = 1.0 / statistics.mean(ests)
-    sample = (f"{nr} of {w.batch * w.q_len * w.num_q_heads} attention rows "
-              f"and {na} logits rows per step, extrapolated by row count")
+    t_gen = time.perf_counter()
+    host_inp = wl.workload_inputs(w, device="cpu", fast_host=True)
+    t_gen = time.perf_counter() - t_gen
+    total = w.batch * w.q_len * w.num_q_heads
+    K = max(1, args.steps)
+    row_slices = np.array_split(np.arange(total, dtype=np.int64), K)
+    req_slices = np.array_split(np.arange(w.batch, dtype=np.int64), K)
+    for k in range(args.warmup):
+        _oracle_rows(w, host_inp, row_slices[k % K][:8])
+    times = []
+    for k in range(K):
+        t = time.perf_counter()
+        if row_slices[k].size:
+            _oracle_rows(w, host_inp, row_slices[k])
+        _oracle_accept(w, host_inp, req_slices[k])
+        times.append(time.perf_counter() - t)
+    whole = sum(times)
+    value = 1.0 / whole
+    sample = (f"each of the {K} timed steps computes 1/{K} of the "
+              f"{total} attention rows and of the {w.batch} accept requests; "
+              f"the {K} together compute one whole verify step in "
+              f"{whole:.2f} s")
     return {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 6), "unit": UNIT,
         "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(1e3 / value, 3), "higher_is_better": True,
+        "ms_per_step": round(1e3 * whole / K, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded, generated on the host)",
-        "config": {"workload": w.name, "batch": w.batch, "q_len": w.q_len,
-                   "prefix": w.prefix or "U[1024,131072]",
-                   "page_size": w.page_size, "kv_dtype": w.kv_dtype},
+        "config": config_of(w, ws_n, args.graph),
+        "step_fraction": round(1.0 / K, 6),
+        "value_basis": "whole verify steps per second: 1 / (sum of the K "
+                       "slice times)",
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT,
                          "cores": oracle.default_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT,
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "wall_s": round(spent, 2),
+        "input_generation_s": round(t_gen, 2),
+        "timed_s": round(whole, 2),
     }, rank
 
 
@@ -861,6 +1102,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=list(wl.ALL_WORKLOADS))
+    ap.add_argument("--main-only", action="store_true",
+                    help="time only --workload (no other configurations, "
+                         "no next-row timings)")
+    ap.add_argument("--extras-workload", default="b8_q8_p32k",
+                    choices=list(wl.WORKLOADS),
+                    help="workload whose shapes the next-row timings use")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="replay each C-ABI call from a CUDA graph")
@@ -874,7 +1121,6 @@ def main():
     ap.add_argument("--no-select", action="store_true",
                     help="skip the DFlash2 candidate selector timing")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
-    ap.add_argument("--ref-rows", type=int, default=48)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -463,9 +463,12 @@ int spec_prepare_next_block(const spec_width_policy* pol, int32_t batch,
  *     SPEC_NOALLOC_SCRATCH_BYTES is rejected with SPEC_ERR_WORKSPACE.
  *   - SPEC_FLAG_CHECKED is rejected with SPEC_ERR_UNSUPPORTED (its status
  *     word lives in a caller workspace).
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, which may load the library's GPU code on that
- *     device); make that first call before any stream capture.
+ *   - The array's device address is looked up (cudaGetSymbolAddress) on
+ *     the first call in each CUDA context and cached under that context's
+ *     process-unique id, so a caller that runs in a driver context of its
+ *     own, and the new primary context after a device reset, each get their
+ *     own lookup, never a stale address.  The first call in a context may
+ *     load the library's GPU code there; make it before any stream capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; nothing in it needs to start at zero.  Calls whose kernels
  *     overlap on the GPU (on different streams, or from different threads)

@@ -23,32 +23,96 @@ namespace {
 static __device__ __align__(256) unsigned char
     g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch
+// The array's device address belongs to the CUDA context that loaded this
+// module, not to the device: a caller may run in a context of its own (an
+// engine that creates and owns its driver context), and a device reset
+// replaces the primary context.  So the address is cached per context,
+// keyed by the context's process-unique id (cuCtxGetId; a handle value can
+// be reused by a later context, an id is never reused).
+using PFN_ctx_get_current = CUresult (*)(CUcontext*);
+using PFN_ctx_get_id = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device, looked up once
-// per device.  In host code g_noalloc_scratch names a host-side stand-in,
-// never the device array, so it is never passed to a kernel directly.
-int scratch_address(void** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess)
-    return specv::set_error(SPEC_ERR_CUDA, "cudaGetDevice: %s",
+constexpr int kMaxContexts = 64;
+std::mutex g_mu;
+PFN_ctx_get_current g_get_current = nullptr;
+PFN_ctx_get_id g_get_id = nullptr;
+struct Entry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+Entry g_cache[kMaxContexts];
+int g_cached = 0, g_next = 0;
+
+int driver_entry(const char* name, int version, void** fn) {
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion(name, fn, version,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !*fn)
+    return specv::set_error(SPEC_ERR_CUDA, "%s unavailable: %s", name,
                             cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices)
-    return specv::set_error(SPEC_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  return SPEC_OK;
+}
+
+// Id of the calling thread's current context, or 0 when none is current.
+int current_context_id(unsigned long long* id) {
+  *id = 0;
+  CUcontext ctx = nullptr;
+  CUresult r = g_get_current(&ctx);
+  if (r != CUDA_SUCCESS)
+    return specv::set_error(SPEC_ERR_CUDA, "cuCtxGetCurrent failed (%d)",
+                            (int)r);
+  if (!ctx) return SPEC_OK;
+  r = g_get_id(ctx, id);
+  if (r != CUDA_SUCCESS)
+    return specv::set_error(SPEC_ERR_CUDA, "cuCtxGetId failed (%d)", (int)r);
+  return SPEC_OK;
+}
+
+int symbol_address(void** out) {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p)
+    return specv::set_error(SPEC_ERR_CUDA,
+                            "cudaGetSymbolAddress of the scratch: %s",
+                            cudaGetErrorString(e));
+  *out = p;
+  return SPEC_OK;
+}
+
+// Device address of the scratch array in the current context, looked up
+// once per context.  In host code g_noalloc_scratch names a host-side
+// stand-in, never the device array, so it is never passed to a kernel.
+int scratch_address(void** out) {
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p)
-      return specv::set_error(SPEC_ERR_CUDA,
-                              "cudaGetSymbolAddress of the scratch: %s",
-                              cudaGetErrorString(e));
-    g_scratch_addr[dev] = p;
+  int rc;
+  if (!g_get_current || !g_get_id) {
+    void *f1 = nullptr, *f2 = nullptr;
+    if ((rc = driver_entry("cuCtxGetCurrent", 4000, &f1))) return rc;
+    if ((rc = driver_entry("cuCtxGetId", 12000, &f2))) return rc;
+    g_get_current = reinterpret_cast<PFN_ctx_get_current>(f1);
+    g_get_id = reinterpret_cast<PFN_ctx_get_id>(f2);
   }
-  *out = g_scratch_addr[dev];
+  unsigned long long id = 0;
+  if ((rc = current_context_id(&id))) return rc;
+  void* addr = nullptr;
+  if (id == 0) {
+    // no context is current yet: the runtime makes the current device's
+    // primary context current while it looks the symbol up
+    if ((rc = symbol_address(&addr))) return rc;
+    if ((rc = current_context_id(&id))) return rc;
+  }
+  for (int i = 0; i < g_cached; ++i)
+    if (id != 0 && g_cache[i].ctx_id == id) {
+      *out = g_cache[i].addr;
+      return SPEC_OK;
+    }
+  if (!addr && (rc = symbol_address(&addr))) return rc;
+  if (id != 0) {  // remember it (the oldest entry makes room)
+    const int slot = g_cached < kMaxContexts ? g_cached++ : g_next;
+    if (g_cached == kMaxContexts) g_next = (slot + 1) % kMaxContexts;
+    g_cache[slot] = {id, addr};
+  }
+  *out = addr;
   return SPEC_OK;
 }
 

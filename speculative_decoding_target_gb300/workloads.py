@@ -30,8 +30,11 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from typing import List, Optional, Sequence
 
+import numpy as np
 import torch
 
 VOCAB = 248_320
@@ -133,7 +136,8 @@ def make_attention_inputs(*, batch: int, q_len: int, num_q_heads: int,
                           seed: int = 0, device="cpu", spare_pages: int = -1,
                           shuffle: bool = True, poison: bool = True,
                           max_pages: Optional[int] = None,
-                          value_std: float = 1.0) -> dict:
+                          value_std: float = 1.0,
+                          fast_host: bool = False) -> dict:
     """Random verify-attention inputs in a paged pool.
 
     Returns a dict of tensors on ``device``:
@@ -141,6 +145,12 @@ def make_attention_inputs(*, batch: int, q_len: int, num_q_heads: int,
       or uint8 (E4M3 bytes); k_scales/v_scales [num_pages, Hkv, ps, D/64]
       fp16 (FP8 only, else None); page_table int32 [B, max_pages] (-1 where
       unused); seq_lens int32 [B] = prefix + q_len; scale = 1/sqrt(D).
+
+    fast_host: on the host, draw the K/V pools with numpy generators in
+    threads (one stream per chunk of the pool) instead of torch's
+    single-stream CPU generator, which takes minutes for pools of several
+    GB.  The recipe (distribution, quantisation rule, layout, poisoning) is
+    the same; the random values differ from a device-side draw.
     """
     device = torch.device(device)
     assert len(prefix_lens) == batch
@@ -170,11 +180,15 @@ def make_attention_inputs(*, batch: int, q_len: int, num_q_heads: int,
          ).to(torch.bfloat16)
     shape = (num_pages, num_kv_heads, page_size, head_dim)
     k_scales = v_scales = None
+    host_fast = fast_host and device.type == "cpu"
     if kv_dtype == "bf16":
         k_pages = torch.empty(shape, dtype=torch.bfloat16, device=device)
         v_pages = torch.empty(shape, dtype=torch.bfloat16, device=device)
-        for dst in (k_pages, v_pages):
-            _fill_randn_bf16(dst, gdev, value_std)
+        for n, dst in enumerate((k_pages, v_pages)):
+            if host_fast:
+                _fill_randn_bf16_host(dst, seed * 4 + n, value_std)
+            else:
+                _fill_randn_bf16(dst, gdev, value_std)
     elif kv_dtype == "fp8_e4m3":
         assert head_dim % 64 == 0
         k_pages = torch.empty(shape, dtype=torch.uint8, device=device)
@@ -182,8 +196,12 @@ def make_attention_inputs(*, batch: int, q_len: int, num_q_heads: int,
         sshape = (num_pages, num_kv_heads, page_size, head_dim // 64)
         k_scales = torch.empty(sshape, dtype=torch.float16, device=device)
         v_scales = torch.empty(sshape, dtype=torch.float16, device=device)
-        for dst, sc in ((k_pages, k_scales), (v_pages, v_scales)):
-            _fill_randn_fp8(dst, sc, gdev, value_std)
+        for n, (dst, sc) in enumerate(((k_pages, k_scales),
+                                       (v_pages, v_scales))):
+            if host_fast:
+                _fill_randn_fp8_host(dst, sc, seed * 4 + n, value_std)
+            else:
+                _fill_randn_fp8(dst, sc, gdev, value_std)
     else:
         raise ValueError(kv_dtype)
 
@@ -231,6 +249,78 @@ def _fill_randn_fp8(dst: torch.Tensor, scales: torch.Tensor,
         dst[s:e] = y.to(torch.float8_e4m3fn).view(torch.uint8).view(
             (e - s,) + tuple(inner))
         scales[s:e] = sc
+
+
+def _host_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+_HOST_CHUNK = 1 << 22
+
+
+def _host_chunks(n: int, seed: int):
+    """Chunks of a flat pool of n elements, each with its own numpy stream."""
+    nch = (n + _HOST_CHUNK - 1) // _HOST_CHUNK
+    return nch, np.random.SeedSequence(seed).spawn(max(1, nch))
+
+
+def _fill_randn_bf16_host(dst: torch.Tensor, seed: int, std: float):
+    """N(0, std^2) into a host bf16 tensor: float32 normals from numpy,
+    rounded to bf16 to nearest-even on their bit patterns (finite values)."""
+    out = dst.view(-1).view(torch.int16).numpy().view(np.uint16)
+    nch, seqs = _host_chunks(out.size, seed)
+
+    def work(c):
+        s, e = c * _HOST_CHUNK, min(out.size, (c + 1) * _HOST_CHUNK)
+        x = np.random.default_rng(seqs[c]).standard_normal(e - s,
+                                                           dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        u = x.view(np.uint32)
+        u += np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+        out[s:e] = u >> np.uint32(16)
+
+    with ThreadPoolExecutor(_host_threads()) as ex:
+        list(ex.map(work, range(nch)))
+
+
+def _fill_randn_fp8_host(dst: torch.Tensor, scales: torch.Tensor, seed: int,
+                         std: float):
+    """The FP8 rule of _fill_randn_fp8 on the host, a chunk of pages per
+    numpy stream; torch converts to E4M3 (one intra-op thread per worker)."""
+    npg = dst.shape[0]
+    inner = tuple(dst.shape[1:])
+    per_page = dst[0].numel()
+    step = max(1, _HOST_CHUNK // max(1, per_page))
+    nch = (npg + step - 1) // step
+    seqs = np.random.SeedSequence(seed).spawn(max(1, nch))
+    blocks = inner[-1] // 64
+
+    def work(c):
+        s, e = c * step, min(npg, (c + 1) * step)
+        x = torch.from_numpy(np.random.default_rng(seqs[c]).standard_normal(
+            (e - s,) + inner, dtype=np.float32))
+        if std != 1.0:
+            x *= std
+        xb = x.view(e - s, inner[0], inner[1], blocks, 64)
+        amax = xb.abs().amax(dim=-1)
+        sc = torch.where(amax > 0, amax / E4M3_MAX,
+                         torch.ones_like(amax)).to(torch.float16)
+        y = (xb / sc.float().unsqueeze(-1)).clamp(-E4M3_MAX, E4M3_MAX)
+        dst[s:e] = y.to(torch.float8_e4m3fn).view(torch.uint8).view(
+            (e - s,) + inner)
+        scales[s:e] = sc
+
+    prev = torch.get_num_threads()
+    torch.set_num_threads(1)
+    try:
+        with ThreadPoolExecutor(_host_threads()) as ex:
+            list(ex.map(work, range(nch)))
+    finally:
+        torch.set_num_threads(prev)
 
 
 def _poison(k_pages, v_pages, k_scales, v_scales, page_table, seq_lens,
@@ -284,13 +374,14 @@ def make_accept_inputs(*, batch: int, q_len: int, vocab: int, accept_p: float,
     return {"logits": logits, "draft_ids": drafts.contiguous()}
 
 
-def workload_inputs(w: VerifyWorkload, device="cpu", with_accept: bool = True):
-    """Inputs for one named workload."""
+def workload_inputs(w: VerifyWorkload, device="cpu", with_accept: bool = True,
+                    fast_host: bool = False):
+    """Inputs for one named workload (fast_host: see make_attention_inputs)."""
     attn = make_attention_inputs(
         batch=w.batch, q_len=w.q_len, num_q_heads=w.num_q_heads,
         num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
         page_size=w.page_size, prefix_lens=prefix_lengths(w),
-        kv_dtype=w.kv_dtype, seed=w.seed, device=device)
+        kv_dtype=w.kv_dtype, seed=w.seed, device=device, fast_host=fast_host)
     if with_accept:
         attn.update(make_accept_inputs(batch=w.batch, q_len=w.q_len,
                                        vocab=w.vocab, accept_p=w.accept_p,
