@@ -134,9 +134,12 @@ __device__ __forceinline__ void chunk_argmax(const AcceptParams& p, int chunk,
 // Request b's accepted prefix and bonus token from its rows' chunk pairs,
 // by one CTA (the pairs are read past L1: other CTAs wrote them).
 __device__ __forceinline__ void finalize_request(const AcceptParams& p, int b) {
-  __shared__ int s_t[16];
+  __shared__ int s_t[16], s_d[16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qb = p.q_lens ? min(max(p.q_lens[b], 0), p.q_len) : p.q_len;
+  // the drafts, loaded side by side rather than one by one in the walk
+  if (threadIdx.x < p.q_len)
+    s_d[threadIdx.x] = p.draft_ids[(long long)b * p.q_len + threadIdx.x];
   for (int j = warp; j < qb; j += kAcceptThreads / 32) {
     const long long row = (long long)b * p.q_len + j;
     float bv = -INFINITY;
@@ -149,7 +152,7 @@ __device__ __forceinline__ void finalize_request(const AcceptParams& p, int b) {
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    const int32_t* d = p.draft_ids + (long long)b * p.q_len;
+    const int* d = s_d;
     int a = 0;
     while (a + 1 < qb && d[a + 1] == s_t[a]) ++a;
     // an idle request (no rows) commits nothing

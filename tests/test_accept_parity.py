@@ -30,6 +30,7 @@ def _run_both(logits: torch.Tensor, drafts: torch.Tensor):
 @pytest.mark.parametrize("B,q_len,vocab,p", [
     (1, 8, 248320, 0.5), (3, 16, 100003, 0.7), (5, 1, 4096, 0.5),
     (2, 5, 8191, 0.9), (4, 8, 8193, 1.0), (2, 8, 7, 0.5), (1, 2, 1, 1.0),
+    (6, 8, 1023, 0.6), (6, 8, 1024, 0.6), (6, 8, 1025, 0.6), (9, 3, 2052, 0.8),
 ])
 def test_random_planted(B, q_len, vocab, p):
     inp = wl.make_accept_inputs(batch=B, q_len=q_len, vocab=vocab,
