@@ -163,6 +163,24 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
                           size_t workspace_bytes, void* stream);
 
 /*
+ * Test hook for the failure path: the main-loop bound, in SM clock cycles,
+ * of every mbarrier wait of the split kernels in calls made with
+ * SPEC_FLAG_CHECKED.  0 (the default) restores the normal bound of about
+ * two seconds (4e9 cycles), the largest value accepted.  Calls without
+ * SPEC_FLAG_CHECKED always use the normal bound.
+ *
+ * A wait that runs past its bound is a bug, not a data condition: the CTA
+ * records SPEC_STATUS_TIMEOUT in the status word, makes its other waits
+ * return at once, stops issuing loads, then waits (with the normal bound)
+ * for the loads, bulk stores and MMAs it already issued, frees its tensor
+ * memory and exits.  The output of that call is invalid; the device and the
+ * stream stay usable.  A short bound therefore lets a test make the waits
+ * run out on purpose and check the status without hanging the GPU.  The
+ * setting is process-wide; returns SPEC_ERR_ARG outside [0, 4e9].
+ */
+int spec_verify_set_wait_limit(int64_t cycles);
+
+/*
  * Read (and optionally clear) the status word of a verify workspace.
  * Synchronises `stream`, copies 4 bytes to *status_out (host pointer).
  * Meaningful for calls made with SPEC_FLAG_CHECKED.

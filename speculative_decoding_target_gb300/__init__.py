@@ -9,7 +9,7 @@ from ._native import (SpecError, accept_workspace_size, alloc_workspace,
                       desc_for, dflash2_select, dflash2_select_into, greedy_accept, greedy_accept_commit,
                       greedy_accept_commit_into, greedy_accept_into,
                       kv_append, load, make_desc, prepare_next_block,
-                      prepare_next_block_into, stochastic_accept,
+                      prepare_next_block_into, set_wait_limit, stochastic_accept,
                       stochastic_accept_into, stochastic_workspace_size,
                       verify_attention,
                       verify_attention_into, verify_status,
@@ -20,7 +20,8 @@ __all__ = [
     "dflash2_select", "dflash2_select_into",
     "greedy_accept", "greedy_accept_commit", "greedy_accept_commit_into",
     "greedy_accept_into", "kv_append", "load", "make_desc",
-    "prepare_next_block", "prepare_next_block_into", "stochastic_accept",
+    "prepare_next_block", "prepare_next_block_into", "set_wait_limit",
+    "stochastic_accept",
     "stochastic_accept_into", "stochastic_workspace_size", "verify_attention",
     "verify_attention_into", "verify_status", "verify_workspace_size",
     "width_policy",

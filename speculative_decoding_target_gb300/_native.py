@@ -37,6 +37,7 @@ EXPORTED = (
     "spec_kv_append", "spec_greedy_accept_commit", "spec_prepare_next_block",
     "spec_stochastic_workspace_size", "spec_stochastic_accept",
     "spec_select_workspace_size", "spec_dflash2_select",
+    "spec_verify_set_wait_limit",
 )
 SELECT_MODES = {"greedy": 0, "map": 1}
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -98,6 +99,8 @@ def load(path: str = LIB_PATH):
     lib.spec_kv_append.argtypes = [ctypes.POINTER(AttnDesc), P, P, P, P, P,
                                    P, P, P, P, P, P, P]
     lib.spec_kv_append.restype = ctypes.c_int
+    lib.spec_verify_set_wait_limit.argtypes = [ctypes.c_int64]
+    lib.spec_verify_set_wait_limit.restype = ctypes.c_int
     lib.spec_verify_status.argtypes = [P, ctypes.POINTER(u32), i32, P]
     lib.spec_verify_status.restype = ctypes.c_int
     lib.spec_accept_workspace_size.argtypes = [i32, i32]
@@ -248,6 +251,13 @@ def kv_append(k_new, v_new, k_pages, v_pages, page_table, seq_lens, *,
         _ptr(v_pages), _ptr(k_scales), _ptr(v_scales), _ptr(page_table),
         _ptr(seq_lens), _ptr(positions), _ptr(cache_loc), _ptr(workspace),
         _stream(stream)))
+
+
+def set_wait_limit(cycles: int) -> None:
+    """Main-loop wait bound (SM clock cycles) of the split kernels for calls
+    with checked=True; 0 restores the default.  A test hook for the timeout
+    path."""
+    _check(load().spec_verify_set_wait_limit(int(cycles)))
 
 
 def verify_status(workspace: torch.Tensor, clear: bool = True,

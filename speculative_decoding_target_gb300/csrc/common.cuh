@@ -49,7 +49,12 @@ struct AttnParams {
   int piece_cost;     // plan units charged per segment (<= kMaxPieceCost)
   int box_rows;       // TMA box height (tcgen05 kernel): min(page_size, 64)
   float scale_log2;   // softmax scale * log2(e)
+  // clock cycles a main-loop wait of the split kernels may last before the
+  // CTA gives up (sets SPEC_STATUS_TIMEOUT and drains); the teardown's
+  // drain of copies and MMAs already issued always uses kDrainWaitCycles
+  long long wait_cycles;
 };
+constexpr long long kDrainWaitCycles = 4000000000LL;  // about two seconds
 
 __device__ __forceinline__ int clamp_len(int len, int cap) {
   return len < 0 ? 0 : (len > cap ? cap : len);

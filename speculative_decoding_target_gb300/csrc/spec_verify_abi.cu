@@ -3,6 +3,7 @@
 // enqueued, except a failed launch (SPEC_ERR_CUDA).
 #include <cstdarg>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -41,6 +42,9 @@ int g_occ[kMaxDevices][12];  // split-kernel CTAs per SM: [w] mma.sync with w
                              // compute warps, [9] tcgen05 bf16, [10] tcgen05
                              // FP8, [11] tcgen05 FP8 with TMEM KV operands
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+// main-loop wait bound of the split kernels for SPEC_FLAG_CHECKED calls
+// (spec_verify_set_wait_limit); 0 = the default bound
+std::atomic<long long> g_checked_wait_cycles{0};
 
 bool use_tc(const spec_attn_desc* d) {
   return d->page_size >= specv::kTcMinPageSize;
@@ -318,6 +322,11 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
                                 : specv::kMmaPieceCost;
   p.box_rows = specv::verify_split_tc_box_rows(desc->page_size);
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_cycles = specv::kDrainWaitCycles;
+  if (desc->flags & SPEC_FLAG_CHECKED) {
+    const long long w = g_checked_wait_cycles.load(std::memory_order_relaxed);
+    if (w > 0) p.wait_cycles = w;
+  }
   const bool tc = use_tc(desc);
   const bool fp8t = use_fp8t(desc);
   CUtensorMap tm_k, tm_v;
@@ -350,6 +359,15 @@ int spec_verify_attention(const spec_attn_desc* desc, const void* q,
   e = specv::launch_verify_merge(p, s);
   if (e != cudaSuccess)
     return fail(SPEC_ERR_CUDA, "merge kernel launch: %s", cudaGetErrorString(e));
+  return SPEC_OK;
+}
+
+int spec_verify_set_wait_limit(int64_t cycles) {
+  g_err[0] = 0;
+  if (cycles < 0 || cycles > specv::kDrainWaitCycles)
+    return fail(SPEC_ERR_ARG, "wait limit %lld outside [0, %lld]",
+                (long long)cycles, specv::kDrainWaitCycles);
+  g_checked_wait_cycles.store(cycles, std::memory_order_relaxed);
   return SPEC_OK;
 }
 

@@ -58,9 +58,12 @@
 //   The two issuers wait (bounded) for their own inputs in tile order, so a
 //   ready PV never waits behind a QK^T issue.
 //
-// Every wait is bounded (about two seconds of clock); a wait that runs out
-// sets SPEC_STATUS_TIMEOUT in the status word (checked mode) and makes every
-// later wait of the CTA return at once, so the kernel always finishes.
+// Every wait is bounded (AttnParams::wait_cycles, about two seconds by
+// default); a wait that runs out sets SPEC_STATUS_TIMEOUT in the status word
+// (checked mode) and makes every later wait of the CTA return at once, so
+// the kernel always finishes.  The producer then issues no further loads,
+// and the teardown waits (with the long bound) for the loads, bulk stores
+// and MMAs already issued before it frees tensor memory.
 #include <cuda_fp8.h>
 
 #include <cstddef>
@@ -104,7 +107,6 @@ struct Cols {
   static_assert(kS + 2 * NR <= 512, "tensor memory holds 512 columns");
 };
 constexpr uint32_t kTmemCols = 512;
-constexpr long long kWaitCycles = 4000000000LL;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kThreads = 512;
 constexpr int kPieceThreads = 6 * 32;       // warps 0..3, 13 and 14
@@ -165,13 +167,13 @@ struct Piece {
 
 __device__ __noinline__ bool wait_slow(uint32_t a, uint32_t parity,
                                        volatile int* abort, uint32_t* status,
-                                       bool ignore_abort) {
+                                       bool ignore_abort, long long bound) {
   if (!ignore_abort && *abort) return false;
   const long long t0 = clock64();
   while (true) {
     if (tc::bar_try_wait(a, parity)) return true;
     if (!ignore_abort && *abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > bound) {
       *abort = 1;
       if (status) atomicOr(status, SPEC_STATUS_TIMEOUT);
       return false;
@@ -183,7 +185,11 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint64_t* bar,
                                          bool ignore_abort = false) {
   const uint32_t a = tc::smem_u32(bar);
   if (tc::bar_try_wait(a, parity)) return true;
-  return wait_slow(a, parity, cx.abort, cx.p->status, ignore_abort);
+  // the teardown's drain (ignore_abort) keeps the long bound whatever the
+  // main-loop bound is: copies and MMAs already issued must land before the
+  // CTA frees its tensor memory and exits
+  return wait_slow(a, parity, cx.abort, cx.p->status, ignore_abort,
+                   ignore_abort ? kDrainWaitCycles : cx.p->wait_cycles);
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -235,8 +241,14 @@ __device__ __forceinline__ int box_page(const AttnParams& p, const Piece& pc,
   return page;
 }
 
-__device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
-                        const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
+// Returns false once the CTA gave up (a wait ran out): from then on no load
+// is issued, and *last_k / *last_v hold the last tiles whose K / V loads
+// were issued, so that the teardown waits for exactly the loads in flight.
+// A slot is refilled only once its previous tile's bytes have landed and
+// been consumed, so at most one load per slot is ever in flight.
+__device__ bool produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
+                        const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                        int* last_k, int* last_v) {
   const AttnParams& p = *cx.p;
   const int lane = threadIdx.x & 31;
   const int rpb = p.box_rows;
@@ -259,7 +271,8 @@ __device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
       const int S = kv ? kVStages : kKStages, st = gj % S;
       uint64_t* empty = kv ? cx.bars->v8_empty : cx.bars->k8_empty;
       uint64_t* fullb = kv ? cx.bars->v8_full : cx.bars->k8_full;
-      if (gj >= S) wait_bar(cx, &empty[st], ((gj / S) - 1) & 1);
+      const bool ok = gj < S || wait_bar(cx, &empty[st], ((gj / S) - 1) & 1);
+      if (!__all_sync(0xffffffffu, ok && !*cx.abort)) return false;
       const uint32_t full = tc::smem_u32(&fullb[st]);
       if (lane == 0) tc::bar_arrive_expect_tx(full, bytes);
       __syncwarp();
@@ -271,9 +284,11 @@ __device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
         tc::tma_load_2d(base + kHalf + o * 128, tm, full, 128, (int)row);
         bulk_copy(base + kOffKS + o * 8, (kv ? vsb : ksb) + row * 8, rpb * 8, full);
       }
+      *(kv ? last_v : last_k) = gj;
     }
     page = next_page;
   }
+  return true;
 }
 
 // ---- warps 6..9: FP8 -> fp16 into the TMEM operand tiles -------------------
@@ -880,7 +895,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long u = chunk_start(pl, c);
   const long long u_end = chunk_start(pl, c + 1);
   int gj0 = 0;
-  int last_loaded = -1;  // last tile index the producer loaded
+  int last_k = -1, last_v = -1;  // last tiles whose K / V loads were issued
+  bool producing = true;         // producer: cleared once it stopped issuing
   uint32_t vpar = 0;     // dequant warps: parities of their V^T-slot waits
   while (u < u_end) {
     Piece pc;
@@ -907,8 +923,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // meet around each piece, so Q is rewritten only after the previous
     // piece's last MMA and O^T is read before the next piece's first PV.
     if (warp == kWarpProducer) {
-      produce(cx, pc, gj0, smem, &tm_k, &tm_v);
-      last_loaded = gj0 + pc.n_tiles - 1;
+      if (producing)
+        producing = produce(cx, pc, gj0, smem, &tm_k, &tm_v, &last_k, &last_v);
       __syncwarp();
     } else if (warp >= 4 && warp < 12) {
       dequant_piece<NR>(cx, pc, gj0, smem, tmem, (warp - 4) >> 2, vpar);
@@ -942,9 +958,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // teardown: no copy, bulk store or MMA may still be in flight
   if (warp < 4 && tid < kRowsMax) bulk_store_wait<true>();
   if (warp == kWarpProducer && lane == 0) {
-    for (int gj = max(0, last_loaded - kKStages + 1); gj <= last_loaded; ++gj)
+    for (int gj = max(0, last_k - kKStages + 1); gj <= last_k; ++gj)
       wait_bar(cx, &bars.k8_full[gj % kKStages], (gj / kKStages) & 1, true);
-    for (int gj = max(0, last_loaded - kVStages + 1); gj <= last_loaded; ++gj)
+    for (int gj = max(0, last_v - kVStages + 1); gj <= last_v; ++gj)
       wait_bar(cx, &bars.v8_full[gj % kVStages], (gj / kVStages) & 1, true);
   }
   if ((warp == kWarpQK || warp == kWarpPV) && lane == 0) {  // both issuers

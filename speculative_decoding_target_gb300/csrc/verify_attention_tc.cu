@@ -45,9 +45,12 @@
 // per tile whatever its width, so 64-token tiles halve the instructions per
 // KV byte of 32-token tiles.
 //
-// Every wait is bounded (about two seconds of clock); a wait that runs out
-// sets SPEC_STATUS_TIMEOUT in the status word (checked mode) and makes every
-// later wait of the CTA return at once, so the kernel always finishes.
+// Every wait is bounded (AttnParams::wait_cycles, about two seconds by
+// default); a wait that runs out sets SPEC_STATUS_TIMEOUT in the status word
+// (checked mode) and makes every later wait of the CTA return at once, so
+// the kernel always finishes.  The producer then issues no further loads,
+// and the teardown waits (with the long bound) for the loads and MMAs
+// already issued before it frees tensor memory.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -64,7 +67,6 @@ constexpr int kPreBytes = ((kMaxBatch + 1) * 4 + 127) / 128 * 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;               // S/P buffers: columns 256, 320
 constexpr uint32_t kColQ = 384;               // Q: columns 384..511
-constexpr long long kWaitCycles = 4000000000LL;
 constexpr float kRescaleLog2 = 8.0f;          // rescale O when m grows > 2^8
 // FP8 staging: K bytes, V bytes, K scales, V scales of one tile
 constexpr int kS8K = 0;
@@ -125,13 +127,13 @@ struct Ctx {
 // the CTA) when the bound runs out or another wait of the CTA already did.
 __device__ __noinline__ bool wait_slow(uint32_t a, uint32_t parity,
                                        volatile int* abort, uint32_t* status,
-                                       bool ignore_abort) {
+                                       bool ignore_abort, long long bound) {
   if (!ignore_abort && *abort) return false;
   const long long t0 = clock64();
   while (true) {
     if (tc::bar_try_wait(a, parity)) return true;
     if (!ignore_abort && *abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > bound) {
       *abort = 1;
       if (status) atomicOr(status, SPEC_STATUS_TIMEOUT);
       return false;
@@ -143,7 +145,11 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint64_t* bar,
                                          bool ignore_abort = false) {
   const uint32_t a = tc::smem_u32(bar);
   if (tc::bar_try_wait(a, parity)) return true;
-  return wait_slow(a, parity, cx.abort, cx.p->status, ignore_abort);
+  // the teardown's drain (ignore_abort) keeps the long bound whatever the
+  // main-loop bound is: copies and MMAs already issued must land before the
+  // CTA frees its tensor memory and exits
+  return wait_slow(a, parity, cx.abort, cx.p->status, ignore_abort,
+                   ignore_abort ? kDrainWaitCycles : cx.p->wait_cycles);
 }
 
 struct Piece {
@@ -179,9 +185,14 @@ __device__ __forceinline__ int box_page(const AttnParams& p, const Piece& pc,
   return page;
 }
 
+// Returns the number of tiles whose loads were issued: all of the piece's,
+// unless the CTA gave up (a wait ran out), after which nothing more is
+// issued, so that the teardown can wait for exactly the loads in flight.
+// A stage is refilled only once its previous tile's data has landed and
+// been consumed, so at most one load per stage is ever in flight.
 template <bool kFp8>
-__device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
-                        const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
+__device__ int produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
+                       const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
   using C = Cfg<kFp8>;
   const AttnParams& p = *cx.p;
   const int lane = threadIdx.x & 31;
@@ -199,8 +210,9 @@ __device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
         ((long long)(page * p.hkv + pc.g) << p.log2_ps) + (t & (p.page_size - 1));
     if constexpr (!kFp8) {
       const int st = gj % C::kStages;
-      if (gj >= C::kStages)
-        wait_bar(cx, &cx.bars->kv_empty[st], ((gj / C::kStages) - 1) & 1);
+      bool ok = gj < C::kStages ||
+                wait_bar(cx, &cx.bars->kv_empty[st], ((gj / C::kStages) - 1) & 1);
+      if (!__all_sync(0xffffffffu, ok && !*cx.abort)) return jt;
       const uint32_t full = tc::smem_u32(&cx.bars->kv_full[st]);
       if (lane == 0)
         tc::bar_arrive_expect_tx(full, (uint32_t)(nbox * rpb * 128 * 4 * 2));
@@ -217,8 +229,9 @@ __device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
       }
     } else {
       const int s8 = gj % C::kStages8;
-      if (gj >= C::kStages8)
-        wait_bar(cx, &cx.bars->f8_empty[s8], ((gj / C::kStages8) - 1) & 1);
+      bool ok = gj < C::kStages8 ||
+                wait_bar(cx, &cx.bars->f8_empty[s8], ((gj / C::kStages8) - 1) & 1);
+      if (!__all_sync(0xffffffffu, ok && !*cx.abort)) return jt;
       const uint32_t full = tc::smem_u32(&cx.bars->f8_full[s8]);
       if (lane == 0)
         tc::bar_arrive_expect_tx(full, (uint32_t)(nbox * rpb * (2 * 256 + 2 * 8)));
@@ -238,6 +251,7 @@ __device__ void produce(const Ctx& cx, const Piece& pc, int gj0, uint8_t* smem,
     }
     page = next_page;
   }
+  return pc.n_tiles;
 }
 
 // ---- warps 6..9 (FP8): dequantise a staged tile into the fp16 K/V slots -----
@@ -390,7 +404,7 @@ __device__ void mma_piece(const Ctx& cx, const Piece& pc, int gj0, uint32_t tmem
       last = clock64();
     } else if (*cx.abort) {
       break;
-    } else if (clock64() - last > kWaitCycles) {
+    } else if (clock64() - last > cx.p->wait_cycles) {
       *cx.abort = 1;
       if (cx.p->status) atomicOr(cx.p->status, SPEC_STATUS_TIMEOUT);
       break;
@@ -669,6 +683,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   const long long u_end = chunk_start(pl, c + 1);
   int gj0 = 0;
   int last_loaded = -1;  // last tile index the producer loaded
+  bool producing = true;  // producer: cleared once it stopped issuing
   while (u < u_end) {
     Piece pc;
     pc.b = find_request(s_pre, p.batch, p.hkv, u);
@@ -695,8 +710,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     // after the previous piece's last MMA and read after it is complete.
     if (warp == 0) {
       // the whole warp: lanes issue the copies of their pages
-      produce<kFp8>(cx, pc, gj0, smem, &tm_k, &tm_v);
-      last_loaded = gj0 + pc.n_tiles - 1;
+      if (producing) {
+        const int n = produce<kFp8>(cx, pc, gj0, smem, &tm_k, &tm_v);
+        if (n > 0) last_loaded = gj0 + n - 1;
+        producing = n == pc.n_tiles;
+      }
       __syncwarp();
     } else if (warp >= 6) {
       if (kFp8) dequant_piece(cx, pc, gj0, smem);

@@ -247,3 +247,11 @@ def test_select_argument_checks(lib):
     assert call(d(), hidden=ctypes.c_void_p(0x100002)) == _native.SPEC_ERR_ALIGN
     assert call(d(), ws=None) == _native.SPEC_ERR_WORKSPACE
     assert call(d(), ws_bytes=16) == _native.SPEC_ERR_WORKSPACE
+
+
+def test_wait_limit_hook_range(lib):
+    # the checked-mode wait bound: [0, 4e9] cycles, 0 = the default
+    assert lib.spec_verify_set_wait_limit(-1) == _native.SPEC_ERR_ARG
+    assert lib.spec_verify_set_wait_limit(5_000_000_000) == _native.SPEC_ERR_ARG
+    assert lib.spec_verify_set_wait_limit(1000) == _native.SPEC_OK
+    assert lib.spec_verify_set_wait_limit(0) == _native.SPEC_OK
