@@ -139,7 +139,17 @@ struct Bars {
   uint64_t k8_empty[kKStages]; // dequant warps done with the K slot
   uint64_t v8_full[kVStages];  // staged V bytes landed
   uint64_t v8_empty[kVStages]; // dequant warps done with the V slot
-  uint64_t k_full;             // K tile written to TMEM
+  // The K tile in two channel halves, so the next tile's first half is
+  // written while the last eight MMAs of QK^T read the second half:
+  uint64_t k_full_a;           // channels 0..127 of K written to TMEM
+  uint64_t k_full;             // channels 128..255 written (the whole tile)
+  // QK^T's first eight MMAs (channels 0..127) of tile j done: that half
+  // may be rewritten.  One barrier per dequant set: QK^T of tile j commits
+  // to the barrier of the set that writes tile j + 1, so each barrier has
+  // one waiter that consumes its phases in order (a barrier shared by the
+  // two sets could be waited for a phase it has not reached, which a
+  // parity wait mistakes for complete).
+  uint64_t k_free_a[2];
   uint64_t v_full[3];          // V^T slot written to TMEM
   // PV of the slot's 64 tokens complete, one barrier per slot and dequant
   // set: PV commits to the set that writes the slot next, so each barrier
@@ -165,17 +175,22 @@ struct Piece {
   long long s0;
 };
 
-__device__ __noinline__ bool wait_slow(uint32_t a, uint32_t parity,
-                                       volatile int* abort, uint32_t* status,
-                                       bool ignore_abort, long long bound) {
+// The teardown's drain (ignore_abort) keeps the long bound whatever the
+// main-loop bound is: copies and MMAs already issued must land before the
+// CTA frees its tensor memory and exits.  Inlined: a call would make the
+// softmax warps save their live registers around every wait.
+__device__ __forceinline__ bool wait_slow(uint32_t a, uint32_t parity,
+                                       volatile int* abort,
+                                       const AttnParams* p, bool ignore_abort) {
   if (!ignore_abort && *abort) return false;
+  const long long bound = ignore_abort ? kDrainWaitCycles : p->wait_cycles;
   const long long t0 = clock64();
   while (true) {
     if (tc::bar_try_wait(a, parity)) return true;
     if (!ignore_abort && *abort) return false;
     if (clock64() - t0 > bound) {
       *abort = 1;
-      if (status) atomicOr(status, SPEC_STATUS_TIMEOUT);
+      if (p->status) atomicOr(p->status, SPEC_STATUS_TIMEOUT);
       return false;
     }
   }
@@ -185,11 +200,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint64_t* bar,
                                          bool ignore_abort = false) {
   const uint32_t a = tc::smem_u32(bar);
   if (tc::bar_try_wait(a, parity)) return true;
-  // the teardown's drain (ignore_abort) keeps the long bound whatever the
-  // main-loop bound is: copies and MMAs already issued must land before the
-  // CTA frees its tensor memory and exits
-  return wait_slow(a, parity, cx.abort, cx.p->status, ignore_abort,
-                   ignore_abort ? kDrainWaitCycles : cx.p->wait_cycles);
+  return wait_slow(a, parity, cx.abort, cx.p, ignore_abort);
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -379,40 +390,55 @@ __device__ void dequant_piece(const Ctx& cx, const Piece& pc, int gj0,
     uint8_t* vp = smem + kOffVR + sv * kVSlot;
     wait_bar(cx, &cx.bars->k8_full[sk], (gj / kKStages) & 1);
 
-    // ---- K: token L -> lane L.  The K tile is free once S^T_{j-1} is done.
-    if (gj > 0) wait_bar(cx, &cx.bars->s_full[(gj - 1) & 1], ((gj - 1) >> 1) & 1);
-    tc::fence_after();
-    if (32 * q4 < ntok) {  // warp-uniform; lanes past the tile are masked
-      const uint2 k4 = *reinterpret_cast<const uint2*>(kp + kOffKS + L * 8);
-      const uint32_t ksc[4] = {dup_half(k4.x), dup_half(k4.x >> 16),
-                               dup_half(k4.y), dup_half(k4.y >> 16)};
-      uint4 raw[16];  // the whole row: every load in flight at once
-#pragma unroll
-      for (int cc = 0; cc < 16; ++cc)
-        raw[cc] = *reinterpret_cast<const uint4*>(
-            kp + (cc >> 3) * kHalf + L * 128 + (((cc & 7) ^ kswz) << 4));
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-        uint32_t o[32];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const uint4 r4 = raw[blk * 4 + cc];
-          const uint32_t w[4] = {r4.x, r4.y, r4.z, r4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            e4m3x4_scaled(w[e], ksc[blk], ksc[blk], o[cc * 8 + 2 * e],
-                          o[cc * 8 + 2 * e + 1]);
-        }
-        tc::tmem_st_cols<32>(lane_base + kColK + blk * 32, o);
+    // ---- K: token L -> lane L, in two halves of 128 channels (TMEM columns
+    // 0..63 and 64..127).  The first half is free once the first eight MMAs
+    // of S^T_{j-1} are done, the second once S^T_{j-1} is complete, so the
+    // first half of this tile is written while S^T_{j-1} still runs.
+    const bool has = 32 * q4 < ntok;  // warp-uniform; lanes past the tile
+                                      // are masked by the softmax
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      if (gj > 0) {
+        if (half == 0)  // QK^T of tile gj-1, committed to this set's barrier
+          wait_bar(cx, &cx.bars->k_free_a[gj & 1], ((gj - 1) >> 1) & 1);
+        else
+          wait_bar(cx, &cx.bars->s_full[(gj - 1) & 1], ((gj - 1) >> 1) & 1);
       }
+      tc::fence_after();
+      if (has) {
+        // the half row (8 x 16 bytes) and its two scales, all in flight
+        uint4 raw[8];
+        uint32_t ksc[2];
+        const uint32_t k2 =
+            *reinterpret_cast<const uint32_t*>(kp + kOffKS + L * 8 + 4 * half);
+        ksc[0] = dup_half(k2);
+        ksc[1] = dup_half(k2 >> 16);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          raw[cc] = *reinterpret_cast<const uint4*>(
+              kp + half * kHalf + L * 128 + ((cc ^ kswz) << 4));
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          uint32_t o[32];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const uint4 r4 = raw[bb * 4 + cc];
+            const uint32_t w[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              e4m3x4_scaled(w[e], ksc[bb], ksc[bb], o[cc * 8 + 2 * e],
+                            o[cc * 8 + 2 * e + 1]);
+          }
+          tc::tmem_st_cols<32>(lane_base + kColK + (2 * half + bb) * 32, o);
+        }
+      }
+      tc::tmem_wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0)
+        tc::bar_arrive(tc::smem_u32(half ? &cx.bars->k_full : &cx.bars->k_full_a));
     }
-    tc::tmem_wait_st();
-    tc::fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      tc::bar_arrive(tc::smem_u32(&cx.bars->k_full));
-      tc::bar_arrive(tc::smem_u32(&cx.bars->k8_empty[sk]));
-    }
+    if (lane == 0) tc::bar_arrive(tc::smem_u32(&cx.bars->k8_empty[sk]));
 
     // V scales of token L, transposed to [block][token] for the V^T pass
     wait_bar(cx, &cx.bars->v8_full[sv], (gj / kVStages) & 1);
@@ -491,8 +517,9 @@ __device__ void qk_piece(const Ctx& cx, const Piece& pc, int gj0,
       tc::smem_u32(reinterpret_cast<uint8_t*>(cx.smem) + kOffQ), 16, 1024);
   for (int jt = 0; jt < pc.n_tiles; ++jt) {
     const int gj = gj0 + jt;
-    wait_bar(cx, &cx.bars->k_full, gj & 1);
-    // the S^T buffer of tile gj is free once softmax consumed tile gj-2
+    // first half of K (channels 0..127) written, and the S^T buffer of tile
+    // gj free (softmax consumed tile gj-2)
+    wait_bar(cx, &cx.bars->k_full_a, gj & 1);
     if (gj >= 2) wait_bar(cx, &cx.bars->p_full[gj & 1], ((gj >> 1) - 1) & 1);
     tc::fence_after();
     const uint32_t d = tmem + Cols<NR>::kS + (gj & 1) * NR;
@@ -500,10 +527,19 @@ __device__ void qk_piece(const Ctx& cx, const Piece& pc, int gj0,
     // (address field = byte address / 16; every operand lies below 256 KB,
     // so the field never carries)
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
+    for (int k = 0; k < 8; ++k)
       tc::mma_bf16_ta(d, tmem + kColK + k * 8,
                       qdesc + (uint64_t)(((k >> 2) * (NR * 128) + (k & 3) * 32) >> 4),
                       kIdQK, k > 0 ? 1u : 0u);
+    // after those eight MMAs, to the barrier of tile gj+1's dequant set
+    tc::commit(tc::smem_u32(&cx.bars->k_free_a[(gj + 1) & 1]));
+    wait_bar(cx, &cx.bars->k_full, gj & 1);        // second half written
+    tc::fence_after();
+#pragma unroll
+    for (int k = 8; k < 16; ++k)
+      tc::mma_bf16_ta(d, tmem + kColK + k * 8,
+                      qdesc + (uint64_t)(((k >> 2) * (NR * 128) + (k & 3) * 32) >> 4),
+                      kIdQK, 1u);
     tc::commit(tc::smem_u32(&cx.bars->s_full[gj & 1]));
   }
 }
@@ -870,7 +906,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::bar_init(tc::smem_u32(&bars.v8_full[s]), 1);
       tc::bar_init(tc::smem_u32(&bars.v8_empty[s]), 4);
     }
+    tc::bar_init(tc::smem_u32(&bars.k_full_a), 4);
     tc::bar_init(tc::smem_u32(&bars.k_full), 4);
+    tc::bar_init(tc::smem_u32(&bars.k_free_a[0]), 1);
+    tc::bar_init(tc::smem_u32(&bars.k_free_a[1]), 1);
     for (int s = 0; s < 3; ++s) {
       tc::bar_init(tc::smem_u32(&bars.v_full[s]), 4);
       tc::bar_init(tc::smem_u32(&bars.v_empty[s][0]), 1);

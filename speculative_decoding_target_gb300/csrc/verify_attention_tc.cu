@@ -125,17 +125,21 @@ struct Ctx {
 
 // Bounded wait on phase `parity` of an mbarrier.  Returns false (and flags
 // the CTA) when the bound runs out or another wait of the CTA already did.
+// The teardown's drain (ignore_abort) keeps the long bound whatever the
+// main-loop bound is: copies and MMAs already issued must land before the
+// CTA frees its tensor memory and exits.
 __device__ __noinline__ bool wait_slow(uint32_t a, uint32_t parity,
-                                       volatile int* abort, uint32_t* status,
-                                       bool ignore_abort, long long bound) {
+                                       volatile int* abort,
+                                       const AttnParams* p, bool ignore_abort) {
   if (!ignore_abort && *abort) return false;
+  const long long bound = ignore_abort ? kDrainWaitCycles : p->wait_cycles;
   const long long t0 = clock64();
   while (true) {
     if (tc::bar_try_wait(a, parity)) return true;
     if (!ignore_abort && *abort) return false;
     if (clock64() - t0 > bound) {
       *abort = 1;
-      if (status) atomicOr(status, SPEC_STATUS_TIMEOUT);
+      if (p->status) atomicOr(p->status, SPEC_STATUS_TIMEOUT);
       return false;
     }
   }
@@ -145,11 +149,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint64_t* bar,
                                          bool ignore_abort = false) {
   const uint32_t a = tc::smem_u32(bar);
   if (tc::bar_try_wait(a, parity)) return true;
-  // the teardown's drain (ignore_abort) keeps the long bound whatever the
-  // main-loop bound is: copies and MMAs already issued must land before the
-  // CTA frees its tensor memory and exits
-  return wait_slow(a, parity, cx.abort, cx.p->status, ignore_abort,
-                   ignore_abort ? kDrainWaitCycles : cx.p->wait_cycles);
+  return wait_slow(a, parity, cx.abort, cx.p, ignore_abort);
 }
 
 struct Piece {
