@@ -63,12 +63,12 @@ COLD_AND_WARM = ("b1_q8_p4k_ps16", "b1_q16_p256k")
 # (the traffic follows them: every KV byte is read once, and the partials
 # are a small fixed share).
 NCU_TRAFFIC = {
-    "tc": {"source_hash": "82f85a10d3d072aa", "captured_on": "b8_q8_p32k",
-           "read": 1077388032, "write": 4466944,
-           "algorithmic": 1074003968},
-    "fp8t": {"source_hash": "70ac74e863844017",
+    "tc": {"source_hash": "f495f72252f1c31d", "captured_on": "b1_q16_p256k",
+           "read": 1074337280, "write": 3843328,
+           "algorithmic": 262160 * 4 * 1024},
+    "fp8t": {"source_hash": "74b0213517cf9098",
              "captured_on": "b8_q8_p16k_fp8",
-             "read": 279210496, "write": 4592896,
+             "read": 279201536, "write": 4579328,
              "algorithmic": 8 * 16392 * 4 * 528},
 }
 
