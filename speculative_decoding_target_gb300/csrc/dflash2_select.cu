@@ -24,6 +24,7 @@
 //      walks the chain, greedy or MAP, with one warp.
 #include <climits>
 
+#include "common.cuh"
 #include "selector.cuh"
 
 namespace specv {
@@ -66,6 +67,9 @@ __global__ void __launch_bounds__(kSelThreads, 3)
   __shared__ float s_pv[kSelPool];
   __shared__ int s_pi[kSelPool];
   __shared__ int s_n;
+  // the projection kernel may start now: it reads none of this kernel's
+  // output and runs alongside it
+  tc_grid_launch_dependents();
   const int chunk = blockIdx.x, row = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* x = p.cand_logits + (long long)row * p.vocab;
@@ -207,6 +211,7 @@ constexpr int kProjMTiles = 4;  // 64 rows of h per CTA
 // D / 128 slices in a fixed order.
 __global__ void __launch_bounds__(256) project_kernel(const SelectParams p) {
   __shared__ float s_acc[8][kProjMTiles * 16][8];
+  tc_grid_launch_dependents();  // the table kernel may be scheduled now
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int n0 = blockIdx.x * 8, m0 = blockIdx.y * kProjMTiles * 16;
@@ -259,6 +264,10 @@ __global__ void __launch_bounds__(256) project_kernel(const SelectParams p) {
     if (m0 + r < rows && n0 + c < p.rank)
       p.proj[((long long)blockIdx.z * rows + m0 + r) * p.rank + n0 + c] = s;
   }
+  // launched as a programmatic dependent of the top-K pass, which it does
+  // not read: it waits for that grid only here, so that this grid completes
+  // after it and the table kernel (waiting for this grid) sees both
+  tc_grid_dependency_wait();
 }
 
 // ---- 3. transition tables ---------------------------------------------------
@@ -371,6 +380,9 @@ __global__ void __launch_bounds__(256) table_kernel(const SelectParams p) {
   // H_t = the sum of the projection's k slices in slice order (warps 2..7)
   const int warp = threadIdx.x >> 5;
   const int rows = p.batch * P1;
+  // a programmatic dependent of the projection kernel, whose completion
+  // follows the top-K pass's: both grids' outputs are read after this
+  tc_grid_dependency_wait();
   if (warp == 0) {
     merge_candidates(p, row, s_ids[1], s_vals[1]);
   } else if (warp == 1) {
@@ -449,14 +461,24 @@ cudaError_t launch_dflash2_select(const SelectParams& p, cudaStream_t s) {
   topk_partial_kernel<<<dim3(p.chunks, rows), kSelThreads, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  project_kernel<<<dim3((p.rank + 7) / 8,
-                        (rows + kProjMTiles * 16 - 1) / (kProjMTiles * 16),
-                        (p.dim + 127) / 128),
-                   256, 0, s>>>(p);
-  e = cudaGetLastError();
+  // the projection and the table kernel are programmatic dependents of the
+  // launch before them: the projection overlaps the top-K pass, the table
+  // kernel is scheduled while the projection runs
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((p.rank + 7) / 8,
+                     (rows + kProjMTiles * 16 - 1) / (kProjMTiles * 16),
+                     (p.dim + 127) / 128);
+  e = cudaLaunchKernelEx(&cfg, project_kernel, p);
   if (e != cudaSuccess) return e;
-  table_kernel<<<dim3(p.positions - 1, p.batch), 256, 0, s>>>(p);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(p.positions - 1, p.batch);
+  return cudaLaunchKernelEx(&cfg, table_kernel, p);
 }
 
 }  // namespace specv

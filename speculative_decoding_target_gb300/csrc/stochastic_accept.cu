@@ -17,11 +17,14 @@
 //      the request), then the chunk's total draw weight;
 //   3. sample_finalize_kernel, one CTA per request: the tests again, the
 //      chunk that holds u * W, and a block scan of that chunk alone.
+// The second and third launches are programmatic dependents of the one
+// before them (scheduled while it runs, waiting for it in the kernel).
 // Every float step that decides an integer goes through the same device
 // functions in kernels 2 and 3 with explicitly rounded operations, so both
 // see bit-identical weights.
 #include <climits>
 
+#include "common.cuh"
 #include "stochastic.cuh"
 
 namespace specv {
@@ -53,6 +56,8 @@ __global__ void __launch_bounds__(kSampleThreads)
     softmax_partial_kernel(const StochasticParams p) {
   constexpr int kVec = kSampleChunk / 4 / kSampleThreads;
   __shared__ float red[kSampleThreads / 32];
+  // the residual kernel may be scheduled now; it waits for this grid
+  tc_grid_launch_dependents();
   const int chunk = blockIdx.x, row = blockIdx.y;
   const int b = row / p.q_len;
   if (row - b * p.q_len >= rows_of(p, b)) return;  // uniform per CTA
@@ -231,6 +236,10 @@ __global__ void __launch_bounds__(kSampleThreads)
   __shared__ float red[kSampleThreads / 32];
   __shared__ WalkSmem sm;
   const int chunk = blockIdx.x, b = blockIdx.y;
+  tc_grid_launch_dependents();  // the draw kernel may be scheduled now
+  // a programmatic dependent of the softmax pass: its partials are read
+  // only once that grid is complete
+  tc_grid_dependency_wait();
   decide(p, b, &sm);
   const Walk w = sm.walk;
   if (w.qb == 0 || !w.rejected) return;  // only a rejection needs W_c
@@ -273,6 +282,9 @@ __global__ void __launch_bounds__(kSampleThreads)
   __shared__ float s_base, s_target;
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // a programmatic dependent of the residual kernel (itself one of the
+  // softmax pass): everything either wrote is read after this
+  tc_grid_dependency_wait();
   decide(p, b, &sm);
   const Walk w = sm.walk;
   if (w.qb == 0) {
@@ -451,11 +463,21 @@ cudaError_t launch_stochastic_accept(const StochasticParams& p,
   softmax_partial_kernel<<<dim3(p.chunks, rows), kSampleThreads, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  residual_chunk_kernel<<<dim3(p.chunks, p.batch), kSampleThreads, 0, s>>>(p);
-  e = cudaGetLastError();
+  // the second and third launches are programmatic dependents of the one
+  // before: they are scheduled while it runs and wait for it in the kernel
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kSampleThreads);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(p.chunks, p.batch);
+  e = cudaLaunchKernelEx(&cfg, residual_chunk_kernel, p);
   if (e != cudaSuccess) return e;
-  sample_finalize_kernel<<<p.batch, kSampleThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(p.batch);
+  return cudaLaunchKernelEx(&cfg, sample_finalize_kernel, p);
 }
 
 }  // namespace specv
