@@ -189,6 +189,25 @@ __device__ __forceinline__ void tc_grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Launch configuration of a programmatic dependent launch: the grid may be
+// scheduled while the kernel before it on the stream runs (once that one
+// has executed griddepcontrol.launch_dependents in every CTA, or exited),
+// and waits for it with griddepcontrol.wait before touching memory that
+// kernel writes or reads.  `attr` must outlive the launch call.
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t s, cudaLaunchAttribute* attr) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 // Record an error message for spec_last_error() and return `code`.
 int set_error(int code, const char* fmt, ...);
 

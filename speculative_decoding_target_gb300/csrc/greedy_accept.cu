@@ -174,6 +174,9 @@ __device__ __forceinline__ void finalize_request(const AcceptParams& p, int b) {
 // request's last CTA to finish reduces its rows.
 __global__ void __launch_bounds__(kAcceptThreads)
     argmax_partial_kernel(const AcceptParams p) {
+  // a following attention call may be scheduled now (it waits for this
+  // grid before touching memory)
+  tc_grid_launch_dependents();
   const int chunk = blockIdx.x, row = blockIdx.y;
   const int b = row / p.q_len;
   // uniform per CTA: a row past its block is not read, only counted

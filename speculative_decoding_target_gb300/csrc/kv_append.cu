@@ -23,6 +23,9 @@ constexpr int kWarps = 4;
 
 __global__ void __launch_bounds__(kWarps * 32)
     kv_append_kernel(const AppendParams p) {
+  // the attention call that follows may be scheduled now (it waits for
+  // this grid before touching memory)
+  specv::tc_grid_launch_dependents();
   const int w = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= p.batch * p.q_len * p.hkv) return;  // uniform per warp

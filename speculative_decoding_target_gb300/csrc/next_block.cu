@@ -7,6 +7,7 @@
 // One warp per request.  Lane 0 applies the width policy to the request's
 // accept count (the float32 steps rounded one at a time, as stated in
 // spec_verify.h); lanes 0 .. q_max-1 then write one block row each.
+#include "common.cuh"
 #include "next_block.cuh"
 #include "spec_verify.h"
 
@@ -41,6 +42,9 @@ __device__ int next_width(const NextBlockParams& p, int b, int qb, int a) {
 
 __global__ void __launch_bounds__(kWarps * 32)
     prepare_next_block_kernel(const NextBlockParams p) {
+  // the attention call that follows may be scheduled now (it waits for
+  // this grid before touching memory)
+  specv::tc_grid_launch_dependents();
   const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= p.batch) return;  // uniform per warp

@@ -892,6 +892,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the merge kernel may be scheduled now; it waits for this grid to finish
   tc_grid_launch_dependents();
+  // launched as a programmatic dependent of the kernel before it on the
+  // stream (it was scheduled while that one ran): every input and output
+  // is touched only once that grid is complete
+  tc_grid_dependency_wait();
   plan_prefix(p, s_pre);
   const Plan pl = make_plan(p, (long long)p.hkv * s_pre[p.batch]);
   const int c = blockIdx.x;
@@ -1017,8 +1021,10 @@ cudaError_t launch(const AttnParams& p, const CUtensorMap& tm_k,
                    const CUtensorMap& tm_v, cudaStream_t s) {
   // the shared-memory attribute was set by verify_split_fp8t_ctas_per_sm(),
   // which sizing the grid always runs first
-  verify_split_fp8t_kernel<NR><<<p.grid, kThreads, kSmem, s>>>(p, tm_k, tm_v);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      pdl_config(dim3(p.grid), dim3(kThreads), kSmem, s, attr);
+  return cudaLaunchKernelEx(&cfg, verify_split_fp8t_kernel<NR>, p, tm_k, tm_v);
 }
 
 template <int NR>

@@ -139,6 +139,9 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
   const int mi = lane >> 3, lr = lane & 7;
   tc_grid_launch_dependents();  // the merge kernel may be scheduled now
   const int g4 = lane >> 2, t4 = lane & 3;
+  // a programmatic dependent of the kernel before it on the stream: inputs
+  // and outputs are touched only once that grid is complete
+  tc_grid_dependency_wait();
 
   plan_prefix(p, s_pre);
   const Plan pl = make_plan(p, (long long)p.hkv * s_pre[p.batch]);
@@ -368,6 +371,8 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
 constexpr int kMergeRowsPerBlock = 4;
 __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
   __shared__ int s_pre[kMaxBatch + 1];
+  // a following attention call's split kernel may be scheduled now
+  tc_grid_launch_dependents();
   __shared__ float s_acc[kMergeRowsPerBlock][32][9];  // the odd warp's sums
   plan_prefix(p, s_pre);
   const long long U = (long long)p.hkv * s_pre[p.batch];
@@ -461,8 +466,10 @@ cudaError_t launch_split(const AttnParams& p, cudaStream_t s) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;
-  verify_split_bf16_kernel<kWarps><<<p.grid, C::kThreads, C::kSmem, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      pdl_config(dim3(p.grid), dim3(C::kThreads), C::kSmem, s, attr);
+  return cudaLaunchKernelEx(&cfg, verify_split_bf16_kernel<kWarps>, p);
 }
 
 template <int kWarps>

@@ -643,6 +643,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the merge kernel may be scheduled now; it waits for this grid to finish
   tc_grid_launch_dependents();
+  // launched as a programmatic dependent of the kernel before it on the
+  // stream (it was scheduled while that one ran): every input and output
+  // is touched only once that grid is complete
+  tc_grid_dependency_wait();
   plan_prefix(p, s_pre);
   const Plan pl = make_plan(p, (long long)p.hkv * s_pre[p.batch]);
   const int c = blockIdx.x;  // this kernel runs static plans only
@@ -763,8 +767,10 @@ cudaError_t launch(const AttnParams& p, const CUtensorMap& tm_k,
   // the shared-memory attribute was set on this device by ctas_per_sm(),
   // which sizing the grid always runs first (an attribute call per launch
   // costs microseconds of host time)
-  verify_split_tc_kernel<kFp8><<<p.grid, C::kThreads, C::kSmem, s>>>(p, tm_k, tm_v);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      pdl_config(dim3(p.grid), dim3(C::kThreads), C::kSmem, s, attr);
+  return cudaLaunchKernelEx(&cfg, verify_split_tc_kernel<kFp8>, p, tm_k, tm_v);
 }
 
 template <bool kFp8>
