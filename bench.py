@@ -889,9 +889,11 @@ def measure_stochastic(w: wl.VerifyWorkload, inp, dev, steps: int,
             logit_bytes / (out["greedy_drafts_ms"] * 1e-3) / 1e9, 1),
         "frac_of_peak_greedy_drafts": round(
             logit_bytes / (out["greedy_drafts_ms"] * 1e-3) / 1e9 / peak, 4),
-        "gpu_launches": 3 * 2 * steps,
-        "note": "three launches per call: one streaming pass over the logits "
-                "(softmax statistics), per-chunk draw weights, the draw; "
+        "gpu_launches": (2 + 3) * steps,
+        "note": "one streaming pass over the logits (softmax statistics), "
+                "then the draw; with full draft distributions a pass over "
+                "the rejection row's chunks (residual weights) in between "
+                "(a greedy drafter's residual follows from the statistics); "
                 "temperature 1, seeded uniforms",
     })
     return out

@@ -12,9 +12,13 @@
 //   1. softmax_partial_kernel, CTA (chunk, row): the chunk's maximum M and
 //      sum exp2((x - M) k), k = log2(e) / T, in one streaming pass over the
 //      logits (rows past a request's width are skipped unread);
-//   2. residual_chunk_kernel, CTA (chunk, request): the accept tests (one
-//      warp per block row, all rows side by side; repeated by every CTA of
-//      the request), then the chunk's total draw weight;
+//   2. residual_chunk_kernel, CTA (chunk, request), only with draft
+//      distributions: the accept tests (one warp per block row, all rows
+//      side by side; repeated by every CTA of the request), then the
+//      chunk's total draw weight max(0, p - q).  A greedy drafter (q
+//      one-hot at its draft) needs no second pass: the residual is p
+//      without the rejected token, whose chunk weights follow from the
+//      softmax statistics;
 //   3. sample_finalize_kernel, one CTA per request: the tests again, the
 //      chunk that holds u * W, and a block scan of that chunk alone.
 // The second and third launches are programmatic dependents of the one
@@ -283,7 +287,8 @@ __global__ void __launch_bounds__(kSampleThreads)
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // a programmatic dependent of the residual kernel (itself one of the
-  // softmax pass): everything either wrote is read after this
+  // softmax pass), or of the softmax pass for a greedy drafter: everything
+  // they wrote is read after this
   tc_grid_dependency_wait();
   decide(p, b, &sm);
   const Walk w = sm.walk;
@@ -299,28 +304,53 @@ __global__ void __launch_bounds__(kSampleThreads)
     return;
   }
   const long long frow = (long long)b * p.q_len + w.a;
-  // chunk weights in shared memory: the residual's (from kernel 2), else
-  // p's from the row statistics; a zero residual (p == q) falls back to p
+  // chunk weights in shared memory: with draft distributions, the
+  // residual's (from kernel 2); otherwise p's from the row statistics, and
+  // after a rejection by a greedy drafter (q one-hot at the rejected draft)
+  // the residual max(0, p - q) is p without the rejected token, so its
+  // chunk loses that token's probability.  A zero residual (p == q) falls
+  // back to p.
   const float* pm = p.part_max + frow * p.chunks;
   const float* ps = p.part_sum + frow * p.chunks;
+  const bool from_kernel2 = w.rejected && p.draft_probs;
   for (int c = threadIdx.x; c < kMaxSampleChunks; c += kSampleThreads)
-    s_cw[c] = w.rejected && c < p.chunks ? p.chunk_w[(long long)b * p.chunks + c]
-                                          : 0.f;
+    s_cw[c] = from_kernel2 && c < p.chunks
+                  ? p.chunk_w[(long long)b * p.chunks + c] : 0.f;
   __syncthreads();
   if (warp == 0) {
-    float W = chunk_total(s_cw, lane);
-    bool residual = w.rejected && W > 0.f;
+    float W = 0.f;
+    bool residual = false;
+    if (from_kernel2) {
+      W = chunk_total(s_cw, lane);
+      residual = W > 0.f;
+    }
     if (!residual) {
+      // the rejected draft's probability, for a greedy drafter's residual
+      const bool greedy_rej = w.rejected && !p.draft_probs && w.drej >= 0 &&
+                              w.drej < p.vocab;
+      const float pd =
+          greedy_rej ? prob(w.fin, p.logits[frow * p.vocab + w.drej]) : 0.f;
+      const int cd = greedy_rej ? w.drej / kSampleChunk : -1;
       for (int c = lane; c < kMaxSampleChunks; c += 32) {
         float v = 0.f;
         if (c < p.chunks && ps[c] > 0.f)
           v = __fmul_rn(__fmul_rn(ps[c], exp2f(__fmul_rn(__fsub_rn(pm[c], w.fin.m),
                                                          w.fin.k))),
                         w.fin.inv_z);
+        if (c == cd) v = v > pd ? __fsub_rn(v, pd) : 0.f;
         s_cw[c] = v;
       }
       __syncwarp();
       W = chunk_total(s_cw, lane);
+      if (greedy_rej) {
+        residual = W > 0.f;
+        if (!residual) {  // p is one-hot at the rejected draft: fall back to p
+          for (int c = lane; c < kMaxSampleChunks; c += 32)
+            if (c == cd) s_cw[c] = pd;
+          __syncwarp();
+          W = chunk_total(s_cw, lane);
+        }
+      }
     }
     // the first chunk whose running sum exceeds u * W: lane l scans chunks
     // 4l .. 4l+3 after an exclusive warp scan of the lanes' sums
@@ -473,9 +503,11 @@ cudaError_t launch_stochastic_accept(const StochasticParams& p,
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3(p.chunks, p.batch);
-  e = cudaLaunchKernelEx(&cfg, residual_chunk_kernel, p);
-  if (e != cudaSuccess) return e;
+  if (p.draft_probs) {  // a greedy drafter's residual needs no second pass
+    cfg.gridDim = dim3(p.chunks, p.batch);
+    e = cudaLaunchKernelEx(&cfg, residual_chunk_kernel, p);
+    if (e != cudaSuccess) return e;
+  }
   cfg.gridDim = dim3(p.batch);
   return cudaLaunchKernelEx(&cfg, sample_finalize_kernel, p);
 }
