@@ -63,12 +63,12 @@ COLD_AND_WARM = ("b1_q8_p4k_ps16", "b1_q16_p256k")
 # (the traffic follows them: every KV byte is read once, and the partials
 # are a small fixed share).
 NCU_TRAFFIC = {
-    "tc": {"source_hash": "f495f72252f1c31d", "captured_on": "b1_q16_p256k",
-           "read": 1074337280, "write": 3843328,
+    "tc": {"source_hash": "27357d13b41597cd", "captured_on": "b1_q16_p256k",
+           "read": 1074340608, "write": 3459840,
            "algorithmic": 262160 * 4 * 1024},
-    "fp8t": {"source_hash": "74b0213517cf9098",
+    "fp8t": {"source_hash": "81b730fd84eb99fd",
              "captured_on": "b8_q8_p16k_fp8",
-             "read": 279201536, "write": 4579328,
+             "read": 279184640, "write": 4232448,
              "algorithmic": 8 * 16392 * 4 * 528},
 }
 
@@ -529,8 +529,10 @@ def run_gpu(args, w: wl.VerifyWorkload):
         configs = {}
         extras_w = wl.WORKLOADS[args.extras_workload]
         extras_inp = None
+        only = None if args.configs == "all" else {
+            c for c in args.configs.split(",") if c and c != "none"}
         for name in wl.WORKLOAD_ORDER:
-            if name == w.name:
+            if name == w.name or (only is not None and name not in only):
                 continue
             cw = wl.WORKLOADS[name]
             rec, cinp = measure_config(cw, dev, args.steps, args.warmup,
@@ -555,10 +557,10 @@ def run_gpu(args, w: wl.VerifyWorkload):
         if not args.no_stochastic:
             ex["stochastic"] = measure_stochastic(extras_w, extras_inp, dev,
                                                   args.steps, args.warmup,
-                                                  peak)
+                                                  peak, flush)
         if not args.no_select:
             ex["dflash2_select"] = measure_select(extras_w, dev, args.steps,
-                                                  args.warmup, peak)
+                                                  args.warmup, peak, flush)
         result["next_rows"] = ex
         del extras_inp
         torch.cuda.empty_cache()
@@ -845,8 +847,39 @@ def measure_ragged(w: wl.VerifyWorkload, inp, dev, steps: int, warmup: int,
 
 # ------------------------------------------------------ stochastic verify --
 
+def time_cold_calls(call, dev, steps: int, warmup: int, flush):
+    """Device time of one call, cold: the call captured in a CUDA graph
+    (eager calls would time the host's submission rate, since each call is
+    shorter than its Python and ctypes overhead), replayed `steps` times
+    with the L2 flushed before each replay, outside the replay's events.
+    Returns (mean, median) in ms."""
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        call(stream)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            call(side)
+    torch.cuda.synchronize(dev)
+    for _ in range(warmup):
+        graph.replay()
+    evs = [(torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for k, (a, b) in enumerate(evs):
+        flush.fill_(k & 0xFF)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = [a.elapsed_time(b) for a, b in evs]
+    return statistics.mean(ms), statistics.median(ms)
+
+
 def measure_stochastic(w: wl.VerifyWorkload, inp, dev, steps: int,
-                       warmup: int, peak: float):
+                       warmup: int, peak: float, flush):
     """Rejection-sampling accept on the workload's logits: greedy drafts
     (no draft probabilities) and drafts with full draft distributions
     (B x (q_len - 1) x V fp32, the residual row read at a rejection).
@@ -863,25 +896,15 @@ def measure_stochastic(w: wl.VerifyWorkload, inp, dev, steps: int,
     i32 = dict(dtype=torch.int32, device=dev)
     acc, nxt = torch.empty(B, **i32), torch.empty(B, **i32)
     toks = torch.empty((B, q), **i32)
-    stream = torch.cuda.current_stream(dev)
     out = {}
     for name, dp in (("greedy_drafts", None), ("draft_probs", probs)):
-        def call():
+        def call(st, dp=dp):
             sv.stochastic_accept_into(inp["logits"], inp["draft_ids"], dp,
                                       None, temp, ua, us, None, None, acc,
-                                      nxt, toks, ws, stream)
-        for _ in range(warmup):
-            call()
-        torch.cuda.synchronize(dev)
-        evs = [(torch.cuda.Event(enable_timing=True),
-                torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for a, b in evs:
-            a.record(stream)
-            call()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-        out[name + "_ms"] = round(ms, 5)
+                                      nxt, toks, ws, st)
+        mean, med = time_cold_calls(call, dev, steps, warmup, flush)
+        out[name + "_ms"] = round(mean, 5)
+        out[name + "_median_ms"] = round(med, 5)
     logit_bytes = B * q * V * 4
     out.update({
         "logits_bytes": logit_bytes,
@@ -890,6 +913,8 @@ def measure_stochastic(w: wl.VerifyWorkload, inp, dev, steps: int,
         "frac_of_peak_greedy_drafts": round(
             logit_bytes / (out["greedy_drafts_ms"] * 1e-3) / 1e9 / peak, 4),
         "gpu_launches": (2 + 3) * steps,
+        "timing": "per call: CUDA graph replay, L2 flushed (512 MB written) "
+                  "before each call outside its events",
         "note": "one streaming pass over the logits (softmax statistics), "
                 "then the draw; with full draft distributions a pass over "
                 "the rejection row's chunks (residual weights) in between "
@@ -914,7 +939,7 @@ def select_bytes(w: wl.VerifyWorkload) -> int:
 
 
 def measure_select(w: wl.VerifyWorkload, dev, steps: int, warmup: int,
-                   peak: float):
+                   peak: float, flush):
     """The DFlash2 selector on the workload's draft block (B requests, q_len
     positions, top 16 of the vocabulary, rank 256, hidden 5,120), random
     weights; greedy and MAP walks, CUDA events per call."""
@@ -936,29 +961,19 @@ def measure_select(w: wl.VerifyWorkload, dev, steps: int, warmup: int,
     code_b = (torch.randn((V, R), generator=g, device=dev) * 0.3).to(
         torch.bfloat16)
     out = torch.empty((B, P), dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
     res = {}
     for mode in ("greedy", "map"):
         desc = sv._native.select_desc(logits, code_a, hidden,
                                       top=SELECT_TOP, mode=mode)
         ws = sv.alloc_workspace(sv._native.select_workspace_size(desc), dev)
 
-        def call():
+        def call(st, desc=desc, ws=ws):
             sv.dflash2_select_into(desc, logits, boundary, hidden, w_h,
                                    code_a, code_b, out, None, None, None, ws,
-                                   stream)
-        for _ in range(warmup):
-            call()
-        torch.cuda.synchronize(dev)
-        evs = [(torch.cuda.Event(enable_timing=True),
-                torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for a, b in evs:
-            a.record(stream)
-            call()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        res[mode + "_ms"] = round(statistics.mean(a.elapsed_time(b)
-                                                  for a, b in evs), 5)
+                                   st)
+        mean, med = time_cold_calls(call, dev, steps, warmup, flush)
+        res[mode + "_ms"] = round(mean, 5)
+        res[mode + "_median_ms"] = round(med, 5)
     nbytes = select_bytes(w)
     res.update({
         "shape": f"{B} requests x {P} positions, top {SELECT_TOP} of {V}, "
@@ -969,6 +984,8 @@ def measure_select(w: wl.VerifyWorkload, dev, steps: int, warmup: int,
         "frac_of_peak_greedy": round(
             nbytes / (res["greedy_ms"] * 1e-3) / 1e9 / peak, 4),
         "gpu_launches": 3 * 2 * steps,
+        "timing": "per call: CUDA graph replay, L2 flushed (512 MB written) "
+                  "before each call outside its events",
         "note": "three launches per call (after a counter reset): chunked "
                 "top-K over the candidate logits (the streaming pass), the "
                 "rank projection, the transition tables with the walk in "
@@ -1110,6 +1127,10 @@ def main():
     ap.add_argument("--extras-workload", default="b8_q8_p32k",
                     choices=list(wl.WORKLOADS),
                     help="workload whose shapes the next-row timings use")
+    ap.add_argument("--configs", default="all",
+                    help="comma list of the other configurations to time "
+                         "after the headline ('all', or 'none' for the "
+                         "widened rows alone)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="replay each C-ABI call from a CUDA graph")

@@ -185,14 +185,18 @@ __global__ void __launch_bounds__(kAcceptThreads)
   __shared__ int s_last;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();  // this CTA's pair before its count
-    s_last = atomicAdd(p.counters + b, 1) == p.q_len * p.chunks - 1;
+    // thread 0 wrote this CTA's pair: a release add orders it before the
+    // count, and the acquire side makes every counted pair visible to the
+    // last CTA (its other threads through the barrier below)
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(p.counters + b)
+                 : "memory");
+    s_last = old == p.q_len * p.chunks - 1;
   }
   __syncthreads();
-  if (s_last) {
-    __threadfence();
-    finalize_request(p, b);
-  }
+  if (s_last) finalize_request(p, b);
 }
 
 }  // namespace
