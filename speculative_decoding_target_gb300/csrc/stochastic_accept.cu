@@ -116,27 +116,33 @@ struct RowStats {
 
 // (max, normaliser) of a row from its chunk partials; one warp, fixed
 // order, identical on every lane and in every kernel.  Lane l holds chunks
-// l, l + 32, ... (at most kMaxSampleChunks / 32 of them), loaded in one go.
-__device__ RowStats row_stats(const StochasticParams& p, int row, float k) {
-  constexpr int kPerLane = kMaxSampleChunks / 32;
+// l, l + 32, ... (at most kMaxSampleChunks / 32 of them): row_partials
+// issues their loads, row_stats reduces them.
+constexpr int kStatsPerLane = kMaxSampleChunks / 32;
+
+__device__ __forceinline__ void row_partials(const StochasticParams& p, int row,
+                                             float* cm, float* cs) {
   const int lane = threadIdx.x & 31;
   const float* pm = p.part_max + (long long)row * p.chunks;
   const float* ps = p.part_sum + (long long)row * p.chunks;
-  float cm[kPerLane], cs[kPerLane];
 #pragma unroll
-  for (int i = 0; i < kPerLane; ++i) {
+  for (int i = 0; i < kStatsPerLane; ++i) {
     const int c = lane + 32 * i;
     cm[i] = c < p.chunks ? pm[c] : -INFINITY;
     cs[i] = c < p.chunks ? ps[c] : 0.f;
   }
+}
+
+__device__ __forceinline__ RowStats row_stats(const float* cm, const float* cs,
+                                              float k) {
   float m = cm[0];
 #pragma unroll
-  for (int i = 1; i < kPerLane; ++i) m = fmaxf(m, cm[i]);
+  for (int i = 1; i < kStatsPerLane; ++i) m = fmaxf(m, cm[i]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float z = 0.f;
 #pragma unroll
-  for (int i = 0; i < kPerLane; ++i)
+  for (int i = 0; i < kStatsPerLane; ++i)
     if (cs[i] > 0.f)
       z = __fadd_rn(z, __fmul_rn(cs[i], exp2f(__fmul_rn(__fsub_rn(cm[i], m), k))));
 #pragma unroll
@@ -156,6 +162,8 @@ struct Walk {
 struct WalkSmem {
   RowStats stats[16];
   int ok[16];
+  int d[16];      // the request's block ids: d[j + 1] is scored by row j
+  float xd[16];   // row j's logit of d[j + 1] (when row j tests a draft)
   Walk walk;
 };
 
@@ -163,39 +171,50 @@ struct WalkSmem {
 // w, w + warps, ... (their statistics and the test of the draft each row
 // scores), then thread 0 counts the leading accepted drafts.  Every test is
 // independent of the others, so they run side by side; the result is the
-// same in every kernel that calls this.  Ends with the CTA synchronised and
-// the walk in sm->walk.
-__device__ void decide(const StochasticParams& p, int b, WalkSmem* sm) {
+// same in every kernel that calls this.  Each row's loads that do not
+// depend on its draft (the uniform, the chunk partials) are issued with the
+// draft id, so a test costs two rounds of loads.  With `part` (a
+// [16][kMaxSampleChunks] array) the rows' chunk partials are kept there for
+// the draw.  Ends with the CTA synchronised and the walk in sm->walk.
+__device__ void decide(const StochasticParams& p, int b, WalkSmem* sm,
+                       float2* part) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
-  const bool live = p.temperature[b] > 0.f;
-  const int qb = live ? rows_of(p, b) : 0;
   const long long row0 = (long long)b * p.q_len;
   const int32_t* dr = p.draft_ids + row0;
+  if (threadIdx.x < p.q_len) sm->d[threadIdx.x] = dr[threadIdx.x];
+  const bool live = p.temperature[b] > 0.f;
+  const int qb = live ? rows_of(p, b) : 0;
   if (qb > 0) {
     const float k = k_of(p, b);
     for (int j = warp; j < qb; j += nw) {
-      // the inputs of the test are independent of the statistics: load first
-      float x = 0.f, qd = 1.f, u = 0.f;
-      int d = -1;
-      if (j + 1 < qb) {
-        d = dr[j + 1];
-        u = p.u_accept[(long long)b * (p.q_len - 1) + j];
-        if (d >= 0 && d < p.vocab) {
-          x = p.logits[(row0 + j) * p.vocab + d];
-          if (p.draft_probs)
-            qd = p.draft_probs[((long long)b * (p.q_len - 1) + j) * p.vocab + d];
-        }
+      const bool test = j + 1 < qb;
+      const int d = test ? dr[j + 1] : -1;
+      const float u = test ? p.u_accept[(long long)b * (p.q_len - 1) + j] : 0.f;
+      float cm[kStatsPerLane], cs[kStatsPerLane];
+      row_partials(p, (int)(row0 + j), cm, cs);
+      float x = 0.f, qd = 1.f;
+      const bool in = test && d >= 0 && d < p.vocab;
+      if (in) {
+        x = p.logits[(row0 + j) * p.vocab + d];
+        if (p.draft_probs)
+          qd = p.draft_probs[((long long)b * (p.q_len - 1) + j) * p.vocab + d];
       }
-      const RowStats r = row_stats(p, (int)(row0 + j), k);
+      const RowStats r = row_stats(cm, cs, k);
       int ok = 1;
-      if (j + 1 < qb) {
-        const float pd = (d >= 0 && d < p.vocab) ? prob(r, x) : 0.f;
+      if (test) {
+        const float pd = in ? prob(r, x) : 0.f;
         ok = __fmul_rn(u, qd) < pd;   // accept draft j + 1
+      }
+      if (part) {
+#pragma unroll
+        for (int i = 0; i < kStatsPerLane; ++i)
+          part[j * kMaxSampleChunks + lane + 32 * i] = make_float2(cm[i], cs[i]);
       }
       if (lane == 0) {
         sm->stats[j] = r;
         sm->ok[j] = ok;
+        sm->xd[j] = x;
       }
     }
   }
@@ -209,7 +228,7 @@ __device__ void decide(const StochasticParams& p, int b, WalkSmem* sm) {
     if (qb > 0) {
       while (w.a + 1 < qb && sm->ok[w.a]) ++w.a;
       w.rejected = w.a + 1 < qb;
-      if (w.rejected) w.drej = dr[w.a + 1];
+      if (w.rejected) w.drej = sm->d[w.a + 1];
       w.fin = sm->stats[w.a];
     }
     sm->walk = w;
@@ -244,7 +263,7 @@ __global__ void __launch_bounds__(kSampleThreads)
   // a programmatic dependent of the softmax pass: its partials are read
   // only once that grid is complete
   tc_grid_dependency_wait();
-  decide(p, b, &sm);
+  decide(p, b, &sm, nullptr);
   const Walk w = sm.walk;
   if (w.qb == 0 || !w.rejected) return;  // only a rejection needs W_c
   constexpr int kPer = kSampleChunk / kSampleThreads;
@@ -279,7 +298,13 @@ __global__ void __launch_bounds__(kSampleThreads)
   constexpr int kWarps = kSampleThreads / 32;
   __shared__ WalkSmem sm;
   __shared__ float s_cw[kMaxSampleChunks];
-  __shared__ float s_w[kSampleThreads * (kPer + 1)];
+  // the rows' chunk partials until the chunk weights are taken, then the
+  // chosen chunk's draw weights
+  __shared__ union {
+    float2 part[16 * kMaxSampleChunks];
+    float w[kSampleThreads * (kPer + 1)];
+  } s_u;
+  float* s_w = s_u.w;
   __shared__ float s_warp[kWarps];
   __shared__ int s_found[kWarps], s_last[kWarps];
   __shared__ int s_chunk, s_residual;
@@ -290,7 +315,7 @@ __global__ void __launch_bounds__(kSampleThreads)
   // softmax pass), or of the softmax pass for a greedy drafter: everything
   // they wrote is read after this
   tc_grid_dependency_wait();
-  decide(p, b, &sm);
+  decide(p, b, &sm, s_u.part);
   const Walk w = sm.walk;
   if (w.qb == 0) {
     if (threadIdx.x == 0) {
@@ -310,8 +335,7 @@ __global__ void __launch_bounds__(kSampleThreads)
   // the residual max(0, p - q) is p without the rejected token, so its
   // chunk loses that token's probability.  A zero residual (p == q) falls
   // back to p.
-  const float* pm = p.part_max + frow * p.chunks;
-  const float* ps = p.part_sum + frow * p.chunks;
+  const float2* fpart = s_u.part + w.a * kMaxSampleChunks;  // (max, sum)
   const bool from_kernel2 = w.rejected && p.draft_probs;
   for (int c = threadIdx.x; c < kMaxSampleChunks; c += kSampleThreads)
     s_cw[c] = from_kernel2 && c < p.chunks
@@ -328,13 +352,14 @@ __global__ void __launch_bounds__(kSampleThreads)
       // the rejected draft's probability, for a greedy drafter's residual
       const bool greedy_rej = w.rejected && !p.draft_probs && w.drej >= 0 &&
                               w.drej < p.vocab;
-      const float pd =
-          greedy_rej ? prob(w.fin, p.logits[frow * p.vocab + w.drej]) : 0.f;
+      // (the rejecting row scored it: its logit is that row's test input)
+      const float pd = greedy_rej ? prob(w.fin, sm.xd[w.a]) : 0.f;
       const int cd = greedy_rej ? w.drej / kSampleChunk : -1;
       for (int c = lane; c < kMaxSampleChunks; c += 32) {
         float v = 0.f;
-        if (c < p.chunks && ps[c] > 0.f)
-          v = __fmul_rn(__fmul_rn(ps[c], exp2f(__fmul_rn(__fsub_rn(pm[c], w.fin.m),
+        const float2 mc = fpart[c];
+        if (c < p.chunks && mc.y > 0.f)
+          v = __fmul_rn(__fmul_rn(mc.y, exp2f(__fmul_rn(__fsub_rn(mc.x, w.fin.m),
                                                          w.fin.k))),
                         w.fin.inv_z);
         if (c == cd) v = v > pd ? __fsub_rn(v, pd) : 0.f;
@@ -397,7 +422,7 @@ __global__ void __launch_bounds__(kSampleThreads)
     }
     if (first != INT_MAX && cs == first) s_base = base;
   }
-  __syncthreads();
+  __syncthreads();  // the partials are read: s_u holds the weights now
   const int cs = s_chunk;
   const bool residual = s_residual;
   const float* x = p.logits + frow * p.vocab;
@@ -473,13 +498,12 @@ __global__ void __launch_bounds__(kSampleThreads)
     }
     if (pick == INT_MAX)  // rounding between the two sums: last nonzero
       pick = last >= 0 ? last : begin;
-    const int32_t* dr = p.draft_ids + (long long)b * p.q_len;
     p.accept_len[b] = w.a;
     p.next_token[b] = pick;
     if (p.out_tokens) {
       int32_t* o = p.out_tokens + (long long)b * p.q_len;
       for (int j = 0; j < p.q_len; ++j)
-        o[j] = j < w.a ? dr[j + 1] : (j == w.a ? pick : -1);
+        o[j] = j < w.a ? sm.d[j + 1] : (j == w.a ? pick : -1);
     }
     if (p.new_seq_lens) p.new_seq_lens[b] = p.seq_lens[b] - w.qb + w.a + 1;
   }

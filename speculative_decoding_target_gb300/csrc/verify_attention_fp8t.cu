@@ -658,6 +658,42 @@ __device__ __forceinline__ void load_scores16(uint32_t taddr, int c0,
   }
 }
 
+// P^T_j = 2^(s - m) for this token: its row of the MN-major B operand, 16
+// rows (two 16-byte chunks) at a time, with the base-2 maxima `mu` (-inf
+// replaced by 0).  Returns whether a score passed its row's maximum by more
+// than 2^8 (then P^T_j must be recomputed after raising it; the values
+// written may be as large as inf meanwhile, and are never published).
+template <int NR>
+__device__ __forceinline__ bool write_p(uint32_t sbuf, bool masked, bool in,
+                                        int t, const Red* red, const float* mu,
+                                        float sl2, uint8_t* prow, int L) {
+  const float4* mu4 = reinterpret_cast<const float4*>(mu);
+  bool need = false;
+#pragma unroll 1
+  for (int c0 = 0; c0 < NR; c0 += 16) {
+    float v[16];
+    load_scores16(sbuf + c0, c0, masked, in, t, red, v);
+    uint32_t pk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float4 m = mu4[(c0 >> 2) + (e >> 1)];
+      const float m0 = (e & 1) ? m.z : m.x, m1 = (e & 1) ? m.w : m.y;
+      const float a0 = fmaf(v[2 * e], sl2, -m0);
+      const float a1 = fmaf(v[2 * e + 1], sl2, -m1);
+      need |= a0 > kRescaleLog2;
+      need |= a1 > kRescaleLog2;
+      const __half2 hh = __floats2half2_rn(exp2f(a0), exp2f(a1));
+      pk[e] = *reinterpret_cast<const uint32_t*>(&hh);
+    }
+    const int n8 = c0 >> 3;
+    *reinterpret_cast<uint4*>(prow + ((n8 ^ (L & 7)) << 4)) =
+        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    *reinterpret_cast<uint4*>(prow + (((n8 + 1) ^ (L & 7)) << 4)) =
+        make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  }
+  return need;
+}
+
 template <int NR>
 __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
                               uint32_t tmem, uint8_t* smem, Red* red, int slot,
@@ -687,115 +723,97 @@ __device__ void softmax_piece(const Ctx& cx, const Piece& pc, int gj0,
     const int t = t0 + L;
     wait_bar(cx, &cx.bars->s_full[gj & 1], (gj >> 1) & 1);
     tc::fence_after();
-    // raise m when a score passes it by more than 2^8 (always on the
-    // piece's first tile); the decision is shared by the four warps
-    bool slow = jt == 0;
-    if (!slow) {
-      const float4* mu4 = reinterpret_cast<const float4*>(red->mu[mi]);
-      bool need = false;
+    // P^T_j goes to the buffer of tile gj, free once PV of tile gj-2 is done
+    if (gj >= 2) wait_bar(cx, &cx.bars->pv_done[gj & 1], ((gj >> 1) - 1) & 1);
+    uint8_t* prow = smem + kOffP + (gj & 1) * kPBytes + L * 128;
+    // Past the piece's first tile, P^T_j is written at once with the running
+    // maxima, and the same pass notes a score that passes its row's maximum
+    // by more than 2^8; the four warps then vote.  Only then (rarely) is m
+    // raised and P^T_j written again, so a tile costs one pass over S^T.
+    // Nothing is published before the vote.
+    bool raise = jt == 0;  // the piece's first tile sets m from its scores
+    for (;;) {
+      if (raise) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < NR; c0 += 16) {
-        float v[16];
-        load_scores16(sbuf + c0, c0, masked, in, t, red, v);
+        for (int c0 = 0; c0 < NR; c0 += 16) {
+          float v[16];
+          load_scores16(sbuf + c0, c0, masked, in, t, red, v);
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const float4 m = mu4[(c0 >> 2) + k4];
-          need |= fmaf(v[4 * k4], sl2, -m.x) > kRescaleLog2;
-          need |= fmaf(v[4 * k4 + 1], sl2, -m.y) > kRescaleLog2;
-          need |= fmaf(v[4 * k4 + 2], sl2, -m.z) > kRescaleLog2;
-          need |= fmaf(v[4 * k4 + 3], sl2, -m.w) > kRescaleLog2;
+          for (int k = 0; k < 16; ++k) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+              v[k] = fmaxf(v[k], __shfl_xor_sync(0xffffffffu, v[k], o));
+          }
+          if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) red->colmax[q4][c0 + k] = v[k];
+          }
+        }
+        tc::bar_sync_named(2, 128);
+        if (L < NR) {
+          // scale > 0, so the max of the raw scores gives the max of the scaled
+          const float cm = fmaxf(fmaxf(red->colmax[0][L], red->colmax[1][L]),
+                                 fmaxf(red->colmax[2][L], red->colmax[3][L])) * sl2;
+          const float mo = red->m[mi][L];
+          float mn = mo, al = 1.f;
+          if (jt == 0) {
+            mn = cm;
+          } else if (mo != -INFINITY && cm > mo + kRescaleLog2) {
+            mn = cm;
+            al = exp2f(mo - mn);
+          }
+          red->m[mi ^ 1][L] = mn;
+          red->mu[mi ^ 1][L] = mn == -INFINITY ? 0.f : mn;
+          red->alpha[L] = al;
+        }
+        tc::bar_sync_named(2, 128);
+        mi ^= 1;
+        if (jt > 0) {
+#pragma unroll
+          for (int r = 0; r < NR; ++r) lp[r] *= red->alpha[r];
+          // O^T must be final for tile gj-1 before it is rescaled
+          wait_bar(cx, &cx.bars->pv_done[(gj - 1) & 1], ((gj - 1) >> 1) & 1);
+          tc::fence_after();
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < NR; c0 += 16) {
+              uint32_t o[16];
+              const uint32_t ta = lane_base + Cols<NR>::kO + h * NR + c0;
+              tc::tmem_ld_cols<16>(ta, o);
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                o[k] = __float_as_uint(__uint_as_float(o[k]) * red->alpha[c0 + k]);
+              tc::tmem_st16(ta, o);
+            }
+          }
+          tc::tmem_wait_st();
         }
       }
+      const bool need =
+          write_p<NR>(sbuf, masked, in, t, red, red->mu[mi], sl2, prow, L);
+      if (raise) break;  // written with the raised maxima
       const bool any = __any_sync(0xffffffffu, need);
       if (lane == 0) red->flag[gj & 1][q4] = any ? 1 : 0;
       tc::bar_sync_named(2, 128);
-      slow = (red->flag[gj & 1][0] | red->flag[gj & 1][1] |
-              red->flag[gj & 1][2] | red->flag[gj & 1][3]) != 0;
+      raise = (red->flag[gj & 1][0] | red->flag[gj & 1][1] |
+               red->flag[gj & 1][2] | red->flag[gj & 1][3]) != 0;
+      if (!raise) break;
     }
-    if (slow) {
-#pragma unroll 1
-      for (int c0 = 0; c0 < NR; c0 += 16) {
-        float v[16];
-        load_scores16(sbuf + c0, c0, masked, in, t, red, v);
+    // this token's share of the row sums, from the fp16 P^T row it wrote:
+    // the same values the PV MMAs multiply
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+    for (int n8 = 0; n8 < NR / 8; ++n8) {
+      const uint4 w4 =
+          *reinterpret_cast<const uint4*>(prow + ((n8 ^ (L & 7)) << 4));
+      const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1)
-            v[k] = fmaxf(v[k], __shfl_xor_sync(0xffffffffu, v[k], o));
-        }
-        if (lane == 0) {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) red->colmax[q4][c0 + k] = v[k];
-        }
+      for (int k = 0; k < 4; ++k) {
+        const float2 f =
+            __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        lp[8 * n8 + 2 * k] += f.x;
+        lp[8 * n8 + 2 * k + 1] += f.y;
       }
-      tc::bar_sync_named(2, 128);
-      if (L < NR) {
-        // scale > 0, so the max of the raw scores gives the max of the scaled
-        const float cm = fmaxf(fmaxf(red->colmax[0][L], red->colmax[1][L]),
-                               fmaxf(red->colmax[2][L], red->colmax[3][L])) * sl2;
-        const float mo = red->m[mi][L];
-        float mn = mo, al = 1.f;
-        if (jt == 0) {
-          mn = cm;
-        } else if (mo != -INFINITY && cm > mo + kRescaleLog2) {
-          mn = cm;
-          al = exp2f(mo - mn);
-        }
-        red->m[mi ^ 1][L] = mn;
-        red->mu[mi ^ 1][L] = mn == -INFINITY ? 0.f : mn;
-        red->alpha[L] = al;
-      }
-      tc::bar_sync_named(2, 128);
-      mi ^= 1;
-      if (jt > 0) {
-#pragma unroll
-        for (int r = 0; r < NR; ++r) lp[r] *= red->alpha[r];
-        // O^T must be final for tile gj-1 before it is rescaled
-        wait_bar(cx, &cx.bars->pv_done[(gj - 1) & 1], ((gj - 1) >> 1) & 1);
-        tc::fence_after();
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll 1
-          for (int c0 = 0; c0 < NR; c0 += 16) {
-            uint32_t o[16];
-            const uint32_t ta = lane_base + Cols<NR>::kO + h * NR + c0;
-            tc::tmem_ld_cols<16>(ta, o);
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-              o[k] = __float_as_uint(__uint_as_float(o[k]) * red->alpha[c0 + k]);
-            tc::tmem_st16(ta, o);
-          }
-        }
-        tc::tmem_wait_st();
-      }
-    }
-    // P^T_j = 2^(s - m): this token's row of the MN-major B operand, 16 rows
-    // (two 16-byte chunks) at a time.  The P^T buffer of tile gj is free
-    // once PV of tile gj-2 is done.
-    if (gj >= 2) wait_bar(cx, &cx.bars->pv_done[gj & 1], ((gj >> 1) - 1) & 1);
-    const float4* mu4 = reinterpret_cast<const float4*>(red->mu[mi]);
-    uint8_t* prow = smem + kOffP + (gj & 1) * kPBytes + L * 128;
-#pragma unroll
-    for (int c0 = 0; c0 < NR; c0 += 16) {
-      float v[16];
-      load_scores16(sbuf + c0, c0, masked, in, t, red, v);
-      uint32_t pk[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float4 m = mu4[(c0 >> 2) + (e >> 1)];
-        const float m0 = (e & 1) ? m.z : m.x, m1 = (e & 1) ? m.w : m.y;
-        const float x0 = exp2f(fmaf(v[2 * e], sl2, -m0));
-        const float x1 = exp2f(fmaf(v[2 * e + 1], sl2, -m1));
-        lp[c0 + 2 * e] += x0;
-        lp[c0 + 2 * e + 1] += x1;
-        const __half2 hh = __floats2half2_rn(x0, x1);
-        pk[e] = *reinterpret_cast<const uint32_t*>(&hh);
-      }
-      const int n8 = c0 >> 3;
-      *reinterpret_cast<uint4*>(prow + ((n8 ^ (L & 7)) << 4)) =
-          make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<uint4*>(prow + (((n8 + 1) ^ (L & 7)) << 4)) =
-          make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
     tc::fence_proxy_async_smem();
     tc::fence_before();
