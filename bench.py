@@ -66,9 +66,9 @@ NCU_TRAFFIC = {
     "tc": {"source_hash": "27357d13b41597cd", "captured_on": "b1_q16_p256k",
            "read": 1074340608, "write": 3459840,
            "algorithmic": 262160 * 4 * 1024},
-    "fp8t": {"source_hash": "81b730fd84eb99fd",
+    "fp8t": {"source_hash": "d9f64cbfec5bded7",
              "captured_on": "b8_q8_p16k_fp8",
-             "read": 279184640, "write": 4232448,
+             "read": 279188992, "write": 4164352,
              "algorithmic": 8 * 16392 * 4 * 528},
 }
 
