@@ -62,6 +62,28 @@ def test_fp8_running_max_jumps_mid_sequence():
                            "fp8 running max jump")
 
 
+@pytest.mark.parametrize("lane,mult", [(40, 256.0), (127, 256.0), (5, 4.0)])
+def test_fp8_single_token_spike(lane, mult):
+    # One cached token, lane `lane` of a tile in the middle of each request's
+    # prefix, gets keys `mult` times larger, so only the warp holding that
+    # lane sees its scores pass the running maxima.  The four softmax warps
+    # must agree to raise them for that tile.  At 256x the scores pass the
+    # maxima by far more than fp16 and fp32 exp2 can hold, so the first P^T
+    # written for the tile overflows and must be replaced before PV reads
+    # it.  At 4x the jump lands near the rescale threshold: past it for some
+    # rows, short of it for others.
+    inp = _case([3000, 6000, 1500], 8, 64, seed=91 + lane)
+    ks = inp["k_scales"]
+    pt = inp["page_table"].cpu()
+    for b, n in enumerate(inp["seq_lens"].cpu().tolist()):
+        t = (n // 2) // 128 * 128 + lane
+        ks[int(pt[b, t // 64]), :, t % 64, :] *= mult
+    out = gpu_attention(inp)
+    assert torch.isfinite(out.float()).all()
+    assert_attention_close(rows_of(out), oracle_attention(inp), True,
+                           f"fp8 spike lane {lane} x{mult}")
+
+
 def test_fp8_ragged_widths():
     inp = _case([700, 70, 1500, 5, 333], 8, 64, seed=48)
     ql = torch.tensor([8, 5, 1, 0, 3], dtype=torch.int32, device=DEV)
