@@ -363,17 +363,20 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
   }
 }
 
-// One warp per block row: out = sum_s 2^(lse_s - lse) o_s for split
-// segments; segments with no cached token get zero rows.
-// Two warps per block row: they take alternate batches of eight splits and
-// combine their sums through shared memory, so a long list of splits costs
-// half the rounds of dependent loads without more registers per thread.
+// out = sum_s 2^(lse_s - lse) o_s over the splits of a segment; segments
+// with no cached token get zero rows.  Two warps per block row take
+// alternate batches of eight splits, every load of a batch (the partial
+// rows and their log-sum-exps) issued before any is used, and keep a
+// running maximum over their batches (rescaling their sums when it grows),
+// so no pass over the log-sum-exps has to come first: up to 16 splits cost
+// one round of dependent loads.  The odd warp hands its maximum and sums to
+// the even one through shared memory.
 constexpr int kMergeRowsPerBlock = 4;
 __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
   __shared__ int s_pre[kMaxBatch + 1];
   // a following attention call's split kernel may be scheduled now
   tc_grid_launch_dependents();
-  __shared__ float s_acc[kMergeRowsPerBlock][32][9];  // the odd warp's sums
+  __shared__ float s_acc[kMergeRowsPerBlock][32][10];  // the odd warp's sums
   plan_prefix(p, s_pre);
   const long long U = (long long)p.hkv * s_pre[p.batch];
   const int k = blockIdx.y, b = k / p.hkv, g = k - b * p.hkv;
@@ -400,56 +403,63 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
   // above overlapped its tail; the partials are read only once it is done
   tc_grid_dependency_wait();
   const float* lse = p.part_lse + (long long)base * p.rows + r;
-  float mx = -INFINITY;
-  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lse[(long long)s * p.rows]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float* o = p.part_o + ((long long)base * p.rows + r) * kHeadDim + lane * 8;
+  const long long stride = (long long)p.rows * kHeadDim;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float den = 0.f;
-  if (mx != -INFINITY) {
-    const float* o =
-        p.part_o + ((long long)base * p.rows + r) * kHeadDim + lane * 8;
-    const long long stride = (long long)p.rows * kHeadDim;
-    // eight splits at a time, every load issued before any is used; the
-    // two warps of the pair take alternate batches
-    for (int sb = 8 * odd; sb < S; sb += 16) {
-      float lv[8];
-      float4 x0[8], x1[8];
+  float den = 0.f, mx = -INFINITY;
+  for (int sb = 8 * odd; sb < S; sb += 16) {
+    float lv[8];
+    float4 x0[8], x1[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int s = sb + j;
-        if (s < S) {
-          lv[j] = lse[(long long)s * p.rows];
-          x0[j] = *reinterpret_cast<const float4*>(o + s * stride);
-          x1[j] = *reinterpret_cast<const float4*>(o + s * stride + 4);
-        } else {
-          lv[j] = -INFINITY;
-          x0[j] = x1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (sb + j >= S) break;
-        const float w = exp2f(lv[j] - mx);
-        den += w;
-        acc[0] += w * x0[j].x; acc[1] += w * x0[j].y; acc[2] += w * x0[j].z;
-        acc[3] += w * x0[j].w; acc[4] += w * x1[j].x; acc[5] += w * x1[j].y;
-        acc[6] += w * x1[j].z; acc[7] += w * x1[j].w;
+    for (int j = 0; j < 8; ++j) {
+      const int s = sb + j;
+      if (s < S) {
+        lv[j] = lse[(long long)s * p.rows];
+        x0[j] = *reinterpret_cast<const float4*>(o + s * stride);
+        x1[j] = *reinterpret_cast<const float4*>(o + s * stride + 4);
+      } else {
+        lv[j] = -INFINITY;
+        x0[j] = x1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
+    float bm = lv[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) bm = fmaxf(bm, lv[j]);
+    if (bm == -INFINITY) continue;  // no split of this batch saw a key
+    if (bm > mx) {  // the running maximum grows: rescale what is summed
+      const float c = exp2f(mx - bm);  // 0 while nothing was summed
+      den *= c;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] *= c;
+      mx = bm;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float w = exp2f(lv[j] - mx);  // 0 for an empty split
+      den += w;
+      acc[0] += w * x0[j].x; acc[1] += w * x0[j].y; acc[2] += w * x0[j].z;
+      acc[3] += w * x0[j].w; acc[4] += w * x1[j].x; acc[5] += w * x1[j].y;
+      acc[6] += w * x1[j].z; acc[7] += w * x1[j].w;
+    }
   }
-  // the odd warp hands its sums to the even one (named barrier of the pair)
+  // the odd warp hands its maximum and sums to the even one (named barrier
+  // of the pair)
   if (odd) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) s_acc[pr][lane][e] = acc[e];
     s_acc[pr][lane][8] = den;
+    s_acc[pr][lane][9] = mx;
   }
   asm volatile("bar.sync %0, 64;" ::"r"(1 + pr) : "memory");
   if (odd) return;
+  const float m1 = s_acc[pr][lane][9];
+  const float M = fmaxf(mx, m1);
+  if (M != -INFINITY) {
+    const float c0 = exp2f(mx - M), c1 = exp2f(m1 - M);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] += s_acc[pr][lane][e];
-  den += s_acc[pr][lane][8];
+    for (int e = 0; e < 8; ++e) acc[e] = acc[e] * c0 + s_acc[pr][lane][e] * c1;
+    den = den * c0 + s_acc[pr][lane][8] * c1;
+  }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint4 v;
   v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
