@@ -311,19 +311,38 @@ __device__ void merge_candidates(const SelectParams& p, int row, int* ids,
 
 // ---- 4. the walk -------------------------------------------------------------
 
+// Request b's tables and candidates into shared memory (s_tr >= (P-1) K K
+// floats, s_ci >= (P-1) K ints), by the whole CTA.  Other CTAs wrote them
+// (ordered by their fence and count): they are read from L2, every load of a
+// thread issued before any is stored.  P-1 <= 15 and K <= 16, so a thread
+// of the 256 holds at most 15 table entries and one candidate.
+__device__ __forceinline__ void stage_walk(const SelectParams& p, int b,
+                                           float* s_tr, int* s_ci) {
+  const int P1 = p.positions - 1, K = p.top;
+  const int ntr = P1 * K * K, nci = P1 * K;
+  const float* tr = p.trans + (long long)b * ntr;
+  const int32_t* ci = p.cand_ids + (long long)b * nci;
+  float v[15];
+#pragma unroll
+  for (int i = 0; i < 15; ++i) {
+    const int e = threadIdx.x + 256 * i;
+    v[i] = e < ntr ? __ldcg(tr + e) : 0.f;
+  }
+  const int c = (int)threadIdx.x < nci ? __ldcg(ci + threadIdx.x) : 0;
+#pragma unroll
+  for (int i = 0; i < 15; ++i) {
+    const int e = threadIdx.x + 256 * i;
+    if (e < ntr) s_tr[e] = v[i];
+  }
+  if ((int)threadIdx.x < nci) s_ci[threadIdx.x] = c;
+}
+
 // The greedy or MAP walk of request b by one warp, from the tables and
-// candidates in global memory (staged in shared memory: s_tr >= (P-1) K K
-// floats, s_ci >= (P-1) K ints, s_back >= 16 x 16 ints).
-__device__ void walk_request(const SelectParams& p, int b, float* s_tr,
-                             int* s_ci, int* s_back) {
+// candidates staged in shared memory (s_back >= 16 x 16 ints).
+__device__ void walk_request(const SelectParams& p, int b, const float* s_tr,
+                             const int* s_ci, int* s_back) {
   const int lane = threadIdx.x & 31;
   const int P1 = p.positions - 1, K = p.top;
-  // volatile: other CTAs wrote these; the fence above orders them
-  const volatile float* tr = p.trans + (long long)b * P1 * K * K;
-  const volatile int32_t* ci = p.cand_ids + (long long)b * P1 * K;
-  for (int e = lane; e < P1 * K * K; e += 32) s_tr[e] = tr[e];
-  for (int e = lane; e < P1 * K; e += 32) s_ci[e] = ci[e];
-  __syncwarp();
   int32_t* out = p.draft_ids + (long long)b * p.positions;
   if (lane == 0) out[0] = p.boundary[b];
   if (p.mode == 0) {  // greedy
@@ -449,6 +468,8 @@ __global__ void __launch_bounds__(256) table_kernel(const SelectParams p) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  stage_walk(p, b, &s_ah[0][0], reinterpret_cast<int*>(&s_b[0][0]));
+  __syncthreads();
   if (warp == 0)
     walk_request(p, b, &s_ah[0][0], reinterpret_cast<int*>(&s_b[0][0]),
                  reinterpret_cast<int*>(&s_b[0][0]) + 15 * 16);
