@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(256) table_kernel(const SelectParams p) {
     const int slices = (p.dim + 127) >> 7;
     for (int r = threadIdx.x - 64; r < R; r += 192) {
       float hv = 0.f;
-#pragma unroll 8
+#pragma unroll 20
       for (int z = 0; z < slices; ++z)
         hv += p.proj[((long long)z * rows + row) * R + r];
       s_h[r] = hv;
@@ -449,9 +449,17 @@ __global__ void __launch_bounds__(256) table_kernel(const SelectParams p) {
   if (a < K && c < K) {
     float s = -INFINITY;
     if (a < n_pred) {
-      float acc = 0.f;
-      for (int r = 0; r < R; ++r) acc = fmaf(s_ah[r][a], s_b[r][c], acc);
-      s = s_vals[1][c] + acc;
+      // four interleaved partial sums (ranks r = 4i + j), added in a fixed
+      // order: four independent chains of fused multiply-adds
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      int r = 0;
+      for (; r + 4 <= R; r += 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          acc[j] = fmaf(s_ah[r + j][a], s_b[r + j][c], acc[j]);
+      }
+      for (; r < R; ++r) acc[0] = fmaf(s_ah[r][a], s_b[r][c], acc[0]);
+      s = s_vals[1][c] + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
     }
     p.trans[(((long long)b * P1 + t - 1) * K + a) * K + c] = s;
     if (a == 0) {
