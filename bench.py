@@ -63,12 +63,12 @@ COLD_AND_WARM = ("b1_q8_p4k_ps16", "b1_q16_p256k")
 # (the traffic follows them: every KV byte is read once, and the partials
 # are a small fixed share).
 NCU_TRAFFIC = {
-    "tc": {"source_hash": "27357d13b41597cd", "captured_on": "b1_q16_p256k",
-           "read": 1074340608, "write": 3459840,
+    "tc": {"source_hash": "7ed315a6435a89a6", "captured_on": "b1_q16_p256k",
+           "read": 1074336256, "write": 3595776,
            "algorithmic": 262160 * 4 * 1024},
-    "fp8t": {"source_hash": "d9f64cbfec5bded7",
+    "fp8t": {"source_hash": "de382cd15fc4bf0e",
              "captured_on": "b8_q8_p16k_fp8",
-             "read": 279188992, "write": 4164352,
+             "read": 279382528, "write": 4358144,
              "algorithmic": 8 * 16392 * 4 * 528},
 }
 

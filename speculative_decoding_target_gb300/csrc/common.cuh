@@ -91,7 +91,7 @@ __device__ __forceinline__ int units_of(int len) {
 // total KV cut into more or fewer segments).
 constexpr int kMaxPieceCost = 16;
 constexpr int kTcPieceCost = 3;     // bf16/FP8 tcgen05 kernel, Q in TMEM
-constexpr int kFp8tPieceCost = 14;  // FP8 kernel with K and V^T in TMEM
+constexpr int kFp8tPieceCost = 10;  // FP8 kernel with K and V^T in TMEM
 constexpr int kMmaPieceCost = 3;    // mma.sync kernel (bf16, small pages)
 
 struct Plan {
