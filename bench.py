@@ -63,8 +63,8 @@ COLD_AND_WARM = ("b1_q8_p4k_ps16", "b1_q16_p256k")
 # (the traffic follows them: every KV byte is read once, and the partials
 # are a small fixed share).
 NCU_TRAFFIC = {
-    "tc": {"source_hash": "7ed315a6435a89a6", "captured_on": "b1_q16_p256k",
-           "read": 1074336256, "write": 3595776,
+    "tc": {"source_hash": "a91a4d79ec6eaea3", "captured_on": "b1_q16_p256k",
+           "read": 1074319104, "write": 3234560,
            "algorithmic": 262160 * 4 * 1024},
     "fp8t": {"source_hash": "de382cd15fc4bf0e",
              "captured_on": "b8_q8_p16k_fp8",
