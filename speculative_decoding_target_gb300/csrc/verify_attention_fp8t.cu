@@ -32,14 +32,16 @@
 // buffers (the PV B operand).
 //
 // Warp roles (512 threads; 128 registers each):
-//   warps 0..3    softmax: one thread per token lane.  Load S^T_j in
-//                 16-column chunks, mask, keep a running maximum m per row
-//                 shared by all 128 threads (raised only when a score passes
-//                 it by more than 2^8, which rescales O^T and the partial
-//                 sums), write P^T_j = 2^(s - m) (fp16) to shared memory and
-//                 accumulate per-thread partial row sums; the epilogue sums
-//                 them over the tokens, reads O^T and writes the bf16 output
-//                 or an fp32 partial.
+//   warps 0..3    softmax: one thread per token lane.  One pass per tile
+//                 loads S^T_j in 16-column chunks, masks it and writes
+//                 P^T_j = 2^(s - m) (fp16) to shared memory with a running
+//                 maximum m per row shared by all 128 threads, noting any
+//                 score that passes it by more than 2^8; after a vote of the
+//                 four warps such a tile (rarely) raises m, rescales O^T and
+//                 the partial sums and is written again.  Each thread then
+//                 adds its fp16 P^T row to per-thread partial row sums; the
+//                 epilogue sums them over the tokens, reads O^T and writes
+//                 the bf16 output or an fp32 partial.
 //   warps 4..11   dequant, two sets of four warps taking alternate tiles:
 //                 token lane L converts K row L into TMEM lane L
 //                 (fp16(e4m3 * scale)); then, per 64-token V^T slot, a

@@ -19,7 +19,8 @@
 //   warp 0      producer (all 32 lanes, lane i owns box i of a tile: a run of
 //               min(page_size, 64) tokens of one page; page ids prefetched
 //               one tile ahead).  bf16: 2-D TMA boxes of 64 channels with the
-//               128-byte swizzle straight into a 3-stage K/V ring.  FP8: 1-D
+//               128-byte swizzle straight into a 3-stage K/V ring, fetched
+//               with an evict-first L2 policy.  FP8: 1-D
 //               bulk copies of the page runs of K/V bytes and their scales
 //               into a 2-stage staging ring.
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T (16 MMAs, N = 64) into
