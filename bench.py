@@ -63,12 +63,12 @@ COLD_AND_WARM = ("b1_q8_p4k_ps16", "b1_q16_p256k")
 # (the traffic follows them: every KV byte is read once, and the partials
 # are a small fixed share).
 NCU_TRAFFIC = {
-    "tc": {"source_hash": "a91a4d79ec6eaea3", "captured_on": "b1_q16_p256k",
-           "read": 1074319104, "write": 3234560,
+    "tc": {"source_hash": "77d0aa4b059bd9dc", "captured_on": "b1_q16_p256k",
+           "read": 1074288128, "write": 3451648,
            "algorithmic": 262160 * 4 * 1024},
-    "fp8t": {"source_hash": "de382cd15fc4bf0e",
+    "fp8t": {"source_hash": "75d747b0fc9e2123",
              "captured_on": "b8_q8_p16k_fp8",
-             "read": 279382528, "write": 4358144,
+             "read": 279398400, "write": 4250368,
              "algorithmic": 8 * 16392 * 4 * 528},
 }
 
