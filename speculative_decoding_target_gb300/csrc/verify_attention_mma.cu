@@ -365,13 +365,16 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
 
 // out = sum_s 2^(lse_s - lse) o_s over the splits of a segment; segments
 // with no cached token get zero rows.  Two warps per block row take
-// alternate batches of eight splits, every load of a batch (the partial
+// alternate batches of kBatch splits, every load of a batch (the partial
 // rows and their log-sum-exps) issued before any is used, and keep a
 // running maximum over their batches (rescaling their sums when it grows),
-// so no pass over the log-sum-exps has to come first: up to 16 splits cost
-// one round of dependent loads.  The odd warp hands its maximum and sums to
-// the even one through shared memory.
+// so no pass over the log-sum-exps has to come first: up to 2 kBatch splits
+// cost one round of dependent loads.  The odd warp hands its maximum and
+// sums to the even one through shared memory.  kBatch = 8 keeps the kernel
+// at ~100 registers for calls with many segments and few splits each;
+// kBatch = 12 (~140 registers) serves calls with few, long segments.
 constexpr int kMergeRowsPerBlock = 4;
+template <int kBatch>
 __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
   __shared__ int s_pre[kMaxBatch + 1];
   // a following attention call's split kernel may be scheduled now
@@ -407,11 +410,11 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
   const long long stride = (long long)p.rows * kHeadDim;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float den = 0.f, mx = -INFINITY;
-  for (int sb = 8 * odd; sb < S; sb += 16) {
-    float lv[8];
-    float4 x0[8], x1[8];
+  for (int sb = kBatch * odd; sb < S; sb += 2 * kBatch) {
+    float lv[kBatch];
+    float4 x0[kBatch], x1[kBatch];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kBatch; ++j) {
       const int s = sb + j;
       if (s < S) {
         lv[j] = lse[(long long)s * p.rows];
@@ -424,7 +427,7 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
     }
     float bm = lv[0];
 #pragma unroll
-    for (int j = 1; j < 8; ++j) bm = fmaxf(bm, lv[j]);
+    for (int j = 1; j < kBatch; ++j) bm = fmaxf(bm, lv[j]);
     if (bm == -INFINITY) continue;  // no split of this batch saw a key
     if (bm > mx) {  // the running maximum grows: rescale what is summed
       const float c = exp2f(mx - bm);  // 0 while nothing was summed
@@ -434,7 +437,7 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
       mx = bm;
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kBatch; ++j) {
       const float w = exp2f(lv[j] - mx);  // 0 for an empty split
       den += w;
       acc[0] += w * x0[j].x; acc[1] += w * x0[j].y; acc[2] += w * x0[j].z;
@@ -540,7 +543,11 @@ cudaError_t launch_verify_merge(const AttnParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, verify_merge_kernel, p);
+  // few (request, KV head) segments over the whole grid: each is split many
+  // ways, and fewer, larger merge blocks suit it
+  if ((long long)p.batch * p.hkv * 19 <= p.grid)
+    return cudaLaunchKernelEx(&cfg, verify_merge_kernel<12>, p);
+  return cudaLaunchKernelEx(&cfg, verify_merge_kernel<8>, p);
 }
 
 }  // namespace specv
