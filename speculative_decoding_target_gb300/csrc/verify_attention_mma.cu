@@ -372,7 +372,8 @@ __global__ void __launch_bounds__(Cfg<kWarps>::kThreads, 1)
 // cost one round of dependent loads.  The odd warp hands its maximum and
 // sums to the even one through shared memory.  kBatch = 8 keeps the kernel
 // at ~100 registers for calls with many segments and few splits each;
-// kBatch = 12 (~140 registers) serves calls with few, long segments.
+// kBatch = 12 (~140 registers) and 20 (~210) serve calls with few, long
+// segments, whose rows are few and whose splits are many.
 constexpr int kMergeRowsPerBlock = 4;
 template <int kBatch>
 __global__ void __launch_bounds__(256) verify_merge_kernel(const AttnParams p) {
@@ -545,6 +546,8 @@ cudaError_t launch_verify_merge(const AttnParams& p, cudaStream_t s) {
   cfg.numAttrs = 1;
   // few (request, KV head) segments over the whole grid: each is split many
   // ways, and fewer, larger merge blocks suit it
+  if ((long long)p.batch * p.hkv * 38 <= p.grid)
+    return cudaLaunchKernelEx(&cfg, verify_merge_kernel<20>, p);
   if ((long long)p.batch * p.hkv * 19 <= p.grid)
     return cudaLaunchKernelEx(&cfg, verify_merge_kernel<12>, p);
   return cudaLaunchKernelEx(&cfg, verify_merge_kernel<8>, p);
