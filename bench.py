@@ -63,12 +63,12 @@ COLD_AND_WARM = ("b1_q8_p4k_ps16", "b1_q16_p256k")
 # (the traffic follows them: every KV byte is read once, and the partials
 # are a small fixed share).
 NCU_TRAFFIC = {
-    "tc": {"source_hash": "77d0aa4b059bd9dc", "captured_on": "b1_q16_p256k",
-           "read": 1074288128, "write": 3451648,
+    "tc": {"source_hash": "4940d50b31ed6ff9", "captured_on": "b1_q16_p256k",
+           "read": 1074314496, "write": 3420672,
            "algorithmic": 262160 * 4 * 1024},
-    "fp8t": {"source_hash": "75d747b0fc9e2123",
+    "fp8t": {"source_hash": "a3b122c912ef3bfd",
              "captured_on": "b8_q8_p16k_fp8",
-             "read": 279398400, "write": 4250368,
+             "read": 279394816, "write": 4690176,
              "algorithmic": 8 * 16392 * 4 * 528},
 }
 

@@ -145,7 +145,7 @@ __device__ __forceinline__ void plan_prefix(const AttnParams& p, int* s_pre) {
 // kMinUnitsPerCta units (a small workload cut finer would write more split
 // partials than it saves in parallel reads).  Every CTA below it owns at
 // least one unit, so consecutive CTAs of a segment have consecutive ids.
-constexpr int kMinUnitsPerCta = 4;
+constexpr int kMinUnitsPerCta = 3;
 __device__ __forceinline__ int effective_grid(int grid, long long U) {
   const long long want = (U + kMinUnitsPerCta - 1) / kMinUnitsPerCta;
   return want < grid ? (int)want : grid;
