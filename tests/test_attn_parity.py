@@ -84,6 +84,23 @@ def test_page_sizes(ps):
     _check_all(inp, f"page_size={ps}")
 
 
+@pytest.mark.parametrize("B,hq,hkv", [(1, 4, 1), (2, 24, 4), (4, 24, 4)])
+def test_merge_batches_with_a_late_dominant_key(B, hq, hkv):
+    # Few (request, KV head) segments over the whole grid: one segment split
+    # ~100 ways (the merge's 20-split batches, several rounds per warp), 8
+    # segments ~19 ways (12-split batches) and 16 segments (8-split
+    # batches).  One key near the end of every sequence is scaled up, so the
+    # largest log-sum-exp sits in a late split and each warp's running
+    # maximum has to grow after it has summed earlier splits.
+    prefix = 20000 if B <= 3 else [20000, 12003, 20005, 7000][:B]
+    inp = _case(B, 16, prefix, 64, hq=hq, hkv=hkv, seed=300 + B)
+    pt = inp["page_table"].cpu()
+    for b, n in enumerate(inp["seq_lens"].cpu().tolist()):
+        t = n - 40
+        inp["k_pages"][int(pt[b, t // 64]), :, t % 64, :] *= 8
+    _check_all(inp, f"merge batches B={B} Hkv={hkv}")
+
+
 def test_many_ragged_requests_exercise_the_plan():
     g = torch.Generator().manual_seed(5)
     prefixes = torch.randint(0, 3000, (40,), generator=g).tolist()
