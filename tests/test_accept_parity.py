@@ -38,8 +38,11 @@ def test_random_planted(B, q_len, vocab, p):
     _run_both(inp["logits"], inp["draft_ids"])
 
 
-def test_ties_zeros_and_nan():
-    V, q_len = 3 * 8192 + 17, 8
+@pytest.mark.parametrize("V", [3 * 8192 + 17, 3 * 8192 + 16])
+def test_ties_zeros_and_nan(V):
+    # V % 4 == 0 with aligned rows takes the 16-byte load path, otherwise
+    # the scalar one
+    q_len = 8
     g = torch.Generator().manual_seed(0)
     base = torch.randn((q_len * 4, V), generator=g)
     # row 0: the maximum repeated in several chunks -> lowest index

@@ -146,7 +146,8 @@ def _accept_case(B, q_max, V, seed):
 
 
 @pytest.mark.parametrize("B,q_max,V", [(7, 8, 248320), (33, 16, 5000),
-                                       (3, 1, 100)])
+                                       (3, 1, 100), (40, 8, 2052),
+                                       (1024, 16, 36), (1025, 4, 36)])
 def test_accept_commit_bit_exact(B, q_max, V):
     ensure_built()
     logits, drafts, ql, sl = _accept_case(B, q_max, V, seed=B + q_max)
