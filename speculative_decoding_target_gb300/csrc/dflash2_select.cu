@@ -59,7 +59,11 @@ __device__ __forceinline__ void warp_best(float& v, int& i) {
 // falls back to K block-wide argmax rounds over the whole chunk.
 constexpr int kSelPool = 512;
 
-__global__ void __launch_bounds__(kSelThreads, 3)
+// Four CTAs per SM (64 registers, a few bytes of spill): the pass waits on
+// memory, and the extra resident CTA keeps more loads in flight than the
+// spill costs (three CTAs at 80 registers, or five at 48 with more spill,
+// measured slower).
+__global__ void __launch_bounds__(kSelThreads, 4)
     topk_partial_kernel(const SelectParams p) {
   constexpr int kPer = kSelChunk / kSelThreads;  // 32 logits per thread
   constexpr int kWarps = kSelThreads / 32;
